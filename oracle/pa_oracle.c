@@ -1,0 +1,502 @@
+/*
+ * pa_oracle.c -- plain CPU statement of paged decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the CUDA library is
+ * checked against.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline leg may load it.  It shares no source, header, table or helper with
+ * the CUDA path, and the CUDA path never calls it.
+ *
+ * Everything here is written for a reader to check by eye against the pages:
+ *   - "Paged attention" (k4i.top), section "block table": token t of a sequence
+ *     lives in physical_block = block_table[t // block_size] at offset
+ *     t % block_size; the 38-token example maps logical blocks 0, 1, 2 to
+ *     physical blocks 1, 5, 3 with 6 tokens in the last one.
+ *   - "PagedAttention 在 vLLM 中的实现分析" (blog.chen3feng.top), section 3.2
+ *     "Slot Mapping": slot = block_number * block_size + block_offset, and a
+ *     negative slot is a padding token that is ignored; section 3.3 "KV Cache
+ *     布局": the pool is [2, num_blocks, block_size, num_kv_heads, head_size]
+ *     with key at index 0 and value at index 1; section 7.4: the cache-write
+ *     kernel writes key[token] and value[token] to the slot when slot >= 0.
+ *   - "Paged attention" (k4i.top), section "对非连续 blocks 做 attention": the
+ *     block-wise online softmax is mathematically the same as standard softmax
+ *     attention over the concatenated sequence.  The oracle therefore states
+ *     the standard definition (gather, scores, max, exp, sum, weighted sum of
+ *     values) in two plain passes, in fp64.  The online block merge is stated
+ *     separately (or_online_softmax) only to check that identity.
+ *
+ * Floating point: all attention arithmetic is double precision.  fp16/bf16
+ * inputs are decoded from their bit patterns by the IEEE 754 binary16 and the
+ * bfloat16 (upper half of binary32) definitions; outputs are encoded back with
+ * round-to-nearest, ties-to-even.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - query head h uses kv head h / (num_heads / num_kv_heads) (contiguous
+ *     grouped-query groups);
+ *   - seq_lens[s] counts every cached token of sequence s, the newest included;
+ *   - seq_lens[s] == 0 gives an all-zero output row;
+ *   - scale is an explicit argument (the configs use 1/sqrt(head_size)).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_FP16 0
+#define OR_BF16 1
+
+#define OR_OK 0
+#define OR_ERR_ARG (-1)
+#define OR_ERR_BLOCK_ID (-2)
+#define OR_ERR_SEQ_LEN (-3)
+#define OR_ERR_SLOT (-4)
+#define OR_ERR_NOMEM (-5)
+
+/* ------------------------------------------------------------------------ */
+/* Number formats.                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: sign, 5 exponent bits (bias 15), 10 fraction bits. */
+double or_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24); /* subnormal: f * 2^-10 * 2^-14 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of a binary32 -- 8 exponent bits (bias 127),
+ * 7 fraction bits. */
+double or_bf16_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133); /* subnormal: f * 2^-7 * 2^-126 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134); /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* Encode x in a binary format with `ebits` exponent bits and `fbits` fraction
+ * bits (IEEE-style: bias 2^(ebits-1)-1, subnormals, infinities), rounding to
+ * nearest with ties to even. */
+static uint16_t or_encode(double x, int ebits, int fbits)
+{
+    int bias = (1 << (ebits - 1)) - 1;
+    int emin = 1 - bias;          /* exponent of the smallest normal */
+    int emax_field = (1 << ebits) - 1;
+    uint16_t sbit = (uint16_t)(signbit(x) ? 0x8000 : 0);
+    if (isnan(x))
+        return (uint16_t)(0x7fff & ((emax_field << fbits) | (1 << (fbits - 1))));
+    double a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sbit | (emax_field << fbits));
+    if (a == 0.0)
+        return sbit;
+    int E;
+    frexp(a, &E);
+    E -= 1; /* a lies in [2^E, 2^(E+1)) */
+    if (E < emin)
+        E = emin; /* below the normal range the spacing stays 2^(emin-fbits) */
+    double quantum = ldexp(1.0, E - fbits);
+    double n = nearbyint(a / quantum); /* default mode: nearest, ties to even */
+    double r = n * quantum;
+    if (r >= ldexp(1.0, bias + 1)) /* above the largest finite value */
+        return (uint16_t)(sbit | (emax_field << fbits));
+    if (r < ldexp(1.0, emin)) /* subnormal (or rounded to zero) */
+        return (uint16_t)(sbit | (uint16_t)(r / ldexp(1.0, emin - fbits)));
+    int E2;
+    frexp(r, &E2);
+    E2 -= 1;
+    uint16_t field = (uint16_t)(E2 + bias);
+    uint16_t frac = (uint16_t)(r / ldexp(1.0, E2 - fbits) - (double)(1 << fbits));
+    return (uint16_t)(sbit | (field << fbits) | frac);
+}
+
+uint16_t or_double_to_half(double x) { return or_encode(x, 5, 10); }
+uint16_t or_double_to_bf16(double x) { return or_encode(x, 8, 7); }
+
+static double or_load(const uint16_t *p, size_t i, int dtype)
+{
+    return dtype == OR_BF16 ? or_bf16_to_double(p[i]) : or_half_to_double(p[i]);
+}
+
+void or_round(const double *x, uint16_t *bits, int64_t n, int dtype)
+{
+    for (int64_t i = 0; i < n; i++)
+        bits[i] = dtype == OR_BF16 ? or_double_to_bf16(x[i]) : or_double_to_half(x[i]);
+}
+
+void or_widen(const uint16_t *bits, double *x, int64_t n, int dtype)
+{
+    for (int64_t i = 0; i < n; i++)
+        x[i] = or_load(bits, (size_t)i, dtype);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Address translation and slot mapping.                                     */
+/* ------------------------------------------------------------------------ */
+
+/* k4i.top "Paged attention", section "block table":
+ * physical_block = block_table[t // block_size], offset = t % block_size. */
+void or_translate(const int32_t *block_table_row, int t, int block_size,
+                  int32_t *physical_block, int32_t *offset)
+{
+    *physical_block = block_table_row[t / block_size];
+    *offset = t % block_size;
+}
+
+/* chen3feng vLLM analysis, section 3.2 "Slot Mapping":
+ * slot = block_number * block_size + block_offset. */
+int64_t or_slot_of_token(const int32_t *block_table_row, int t, int block_size)
+{
+    int32_t phys, off;
+    or_translate(block_table_row, t, block_size, &phys, &off);
+    return (int64_t)phys * block_size + off;
+}
+
+/* Element index of (plane, physical block, offset, kv head, dim) in the pool
+ * [2, num_blocks, block_size, num_kv_heads, head_size] (section 3.3). */
+static size_t or_pool_index(int plane, int64_t phys, int64_t off, int kvh, int d,
+                            int num_blocks, int block_size, int num_kv_heads,
+                            int head_size)
+{
+    return ((((size_t)plane * num_blocks + phys) * block_size + off) * num_kv_heads + kvh) *
+               head_size + d;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache write (chen3feng vLLM analysis, sections 3.2 and 7.4).              */
+/* ------------------------------------------------------------------------ */
+
+/* For every token i with slot_mapping[i] >= 0 copy key[i] and value[i]
+ * (num_kv_heads x head_size elements each, rows key_stride/value_stride
+ * elements apart) into the pool at block slot / block_size, offset
+ * slot % block_size.  Negative slots are padding and write nothing.  The copy
+ * moves bit patterns; there is no arithmetic on the values. */
+int or_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *cache,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_size, int block_size, int num_blocks,
+                         int64_t key_stride, int64_t value_stride)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return OR_ERR_ARG;
+    for (int i = 0; i < num_tokens; i++) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        if (slot >= (int64_t)num_blocks * block_size)
+            return OR_ERR_SLOT;
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; h++) {
+            for (int d = 0; d < head_size; d++) {
+                cache[or_pool_index(0, blk, off, h, d, num_blocks, block_size, num_kv_heads,
+                                    head_size)] = key[(size_t)i * key_stride + (size_t)h * head_size + d];
+                cache[or_pool_index(1, blk, off, h, d, num_blocks, block_size, num_kv_heads,
+                                    head_size)] = value[(size_t)i * value_stride + (size_t)h * head_size + d];
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention: the standard definition over the gathered sequence.    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    double *out;                 /* [num_seqs, num_heads, head_size] */
+    const uint16_t *q;           /* [num_seqs, num_heads, head_size] */
+    const uint16_t *cache;       /* [2, num_blocks, block_size, num_kv_heads, head_size] */
+    const int32_t *block_tables; /* [num_seqs, max_blocks_per_seq] */
+    const int32_t *seq_lens;     /* [num_seqs] */
+    int num_seqs, num_heads, num_kv_heads, head_size, block_size, num_blocks,
+        max_blocks_per_seq;
+    double scale;
+    int dtype;
+    const int32_t *items; /* (seq * num_heads + head) indices, or NULL for all */
+    int64_t num_items;
+} or_decode_args;
+
+/* One output row: sequence s, query head h.  Kc/Vc/a are scratch of at least
+ * L*head_size, L*head_size and L doubles. */
+static int or_attend_one(const or_decode_args *A, int s, int h, double *Kc, double *Vc,
+                         double *a)
+{
+    const int D = A->head_size;
+    const int G = A->num_heads / A->num_kv_heads;
+    const int kvh = h / G;
+    double *o = A->out + ((size_t)s * A->num_heads + h) * D;
+    int L = A->seq_lens[s];
+    if (L < 0 || L > A->max_blocks_per_seq * A->block_size)
+        return OR_ERR_SEQ_LEN;
+    if (L == 0) {
+        for (int d = 0; d < D; d++)
+            o[d] = 0.0;
+        return OR_OK;
+    }
+    const int32_t *bt = A->block_tables + (size_t)s * A->max_blocks_per_seq;
+
+    /* 1. Gather the sequence's keys and values into contiguous rows. */
+    for (int t = 0; t < L; t++) {
+        int32_t phys, off;
+        or_translate(bt, t, A->block_size, &phys, &off);
+        if (phys < 0 || phys >= A->num_blocks)
+            return OR_ERR_BLOCK_ID;
+        for (int d = 0; d < D; d++) {
+            Kc[(size_t)t * D + d] = or_load(
+                A->cache, or_pool_index(0, phys, off, kvh, d, A->num_blocks, A->block_size,
+                                        A->num_kv_heads, D), A->dtype);
+            Vc[(size_t)t * D + d] = or_load(
+                A->cache, or_pool_index(1, phys, off, kvh, d, A->num_blocks, A->block_size,
+                                        A->num_kv_heads, D), A->dtype);
+        }
+    }
+
+    /* 2. Scores a_t = scale * sum_d q[d] * K[t][d]. */
+    const size_t qrow = ((size_t)s * A->num_heads + h) * D;
+    for (int t = 0; t < L; t++) {
+        double acc = 0.0;
+        for (int d = 0; d < D; d++)
+            acc += or_load(A->q, qrow + d, A->dtype) * Kc[(size_t)t * D + d];
+        a[t] = A->scale * acc;
+    }
+
+    /* 3. softmax(a) = exp(a_t - max) / sum_u exp(a_u - max). */
+    double m = a[0];
+    for (int t = 1; t < L; t++)
+        if (a[t] > m)
+            m = a[t];
+    double l = 0.0;
+    for (int t = 0; t < L; t++) {
+        a[t] = exp(a[t] - m);
+        l += a[t];
+    }
+
+    /* 4. Output o[d] = sum_t softmax_t * V[t][d]. */
+    for (int d = 0; d < D; d++) {
+        double acc = 0.0;
+        for (int t = 0; t < L; t++)
+            acc += a[t] * Vc[(size_t)t * D + d];
+        o[d] = acc / l;
+    }
+    return OR_OK;
+}
+
+typedef struct {
+    const or_decode_args *A;
+    int tid, nthreads;
+    int status;
+} or_worker;
+
+static void *or_decode_worker(void *p)
+{
+    or_worker *w = (or_worker *)p;
+    const or_decode_args *A = w->A;
+    int64_t n = A->items ? A->num_items : (int64_t)A->num_seqs * A->num_heads;
+    size_t cap = (size_t)A->max_blocks_per_seq * A->block_size;
+    if (cap == 0)
+        cap = 1;
+    double *Kc = (double *)malloc(cap * A->head_size * sizeof(double));
+    double *Vc = (double *)malloc(cap * A->head_size * sizeof(double));
+    double *a = (double *)malloc(cap * sizeof(double));
+    w->status = OR_OK;
+    if (!Kc || !Vc || !a) {
+        w->status = OR_ERR_NOMEM;
+    } else {
+        for (int64_t i = w->tid; i < n; i += w->nthreads) {
+            int64_t item = A->items ? A->items[i] : i;
+            int s = (int)(item / A->num_heads);
+            int h = (int)(item % A->num_heads);
+            int rc = or_attend_one(A, s, h, Kc, Vc, a);
+            if (rc != OR_OK) {
+                w->status = rc;
+                break;
+            }
+        }
+    }
+    free(Kc);
+    free(Vc);
+    free(a);
+    return NULL;
+}
+
+/* Decode attention for every (sequence, query head), or only for the listed
+ * items (seq * num_heads + head) when items != NULL.  Results go to out
+ * [num_seqs, num_heads, head_size] in double precision; rows not listed are
+ * left untouched.  Work items are dealt round-robin to nthreads threads. */
+int or_decode(double *out, const uint16_t *q, const uint16_t *cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+              int num_heads, int num_kv_heads, int head_size, int block_size,
+              int num_blocks, int max_blocks_per_seq, double scale, int dtype,
+              const int32_t *items, int64_t num_items, int nthreads)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || (dtype != OR_FP16 && dtype != OR_BF16))
+        return OR_ERR_ARG;
+    if (nthreads < 1)
+        nthreads = 1;
+    or_decode_args A = {out, q, cache, block_tables, seq_lens, num_seqs, num_heads,
+                        num_kv_heads, head_size, block_size, num_blocks,
+                        max_blocks_per_seq, scale, dtype, items, num_items};
+    or_worker *w = (or_worker *)calloc((size_t)nthreads, sizeof(or_worker));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!w || !th) {
+        free(w);
+        free(th);
+        return OR_ERR_NOMEM;
+    }
+    for (int i = 0; i < nthreads; i++) {
+        w[i].A = &A;
+        w[i].tid = i;
+        w[i].nthreads = nthreads;
+    }
+    int started = 0;
+    for (int i = 1; i < nthreads; i++) {
+        if (pthread_create(&th[i], NULL, or_decode_worker, &w[i]) != 0)
+            break;
+        started = i;
+    }
+    /* Threads that failed to start leave their items to this thread. */
+    if (started < nthreads - 1) {
+        for (int i = 0; i < nthreads; i++)
+            w[i].nthreads = 1;
+        for (int i = 1; i <= started; i++)
+            pthread_join(th[i], NULL);
+        w[0].tid = 0;
+        or_decode_worker(&w[0]);
+        int st = w[0].status;
+        free(w);
+        free(th);
+        return st;
+    }
+    or_decode_worker(&w[0]);
+    for (int i = 1; i < nthreads; i++)
+        pthread_join(th[i], NULL);
+    int st = OR_OK;
+    for (int i = 0; i < nthreads; i++)
+        if (w[i].status != OR_OK)
+            st = w[i].status;
+    free(w);
+    free(th);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The block-wise online softmax, as k4i.top "Paged attention" states it in */
+/* section "对非连续 blocks 做 attention".                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Scores a[0..n) (already scaled) and value rows V[n][D] are cut into blocks
+ * of `block` entries.  Each block j gives m_j = max a, l_j = sum exp(a - m_j),
+ * o_j = sum exp(a - m_j) V; the running (m, l, o) absorbs it with
+ * m_new = max(m, m_j), l = e^(m-m_new) l + e^(m_j-m_new) l_j,
+ * o = e^(m-m_new) o + e^(m_j-m_new) o_j.  The result o / l goes to out[D].
+ * Also returns the final (m, l) so a caller can merge further. */
+int or_online_softmax(double *out, double *m_out, double *l_out, const double *a,
+                      const double *V, int n, int D, int block)
+{
+    if (n <= 0 || D <= 0 || block <= 0)
+        return OR_ERR_ARG;
+    double *o = (double *)calloc((size_t)D, sizeof(double));
+    double *oj = (double *)malloc((size_t)D * sizeof(double));
+    if (!o || !oj) {
+        free(o);
+        free(oj);
+        return OR_ERR_NOMEM;
+    }
+    double m = -INFINITY, l = 0.0;
+    for (int j0 = 0; j0 < n; j0 += block) {
+        int j1 = j0 + block < n ? j0 + block : n;
+        double mj = a[j0];
+        for (int t = j0 + 1; t < j1; t++)
+            if (a[t] > mj)
+                mj = a[t];
+        double lj = 0.0;
+        for (int d = 0; d < D; d++)
+            oj[d] = 0.0;
+        for (int t = j0; t < j1; t++) {
+            double p = exp(a[t] - mj);
+            lj += p;
+            for (int d = 0; d < D; d++)
+                oj[d] += p * V[(size_t)t * D + d];
+        }
+        double m_new = m > mj ? m : mj;
+        double c_old = exp(m - m_new); /* exp(-inf) = 0 on the first block */
+        double c_new = exp(mj - m_new);
+        l = c_old * l + c_new * lj;
+        for (int d = 0; d < D; d++)
+            o[d] = c_old * o[d] + c_new * oj[d];
+        m = m_new;
+    }
+    for (int d = 0; d < D; d++)
+        out[d] = o[d] / l;
+    if (m_out)
+        *m_out = m;
+    if (l_out)
+        *l_out = l;
+    free(o);
+    free(oj);
+    return OR_OK;
+}
+
+/* Merge of independently computed partial states (m_p, l_p, o_p), with o_p
+ * the unnormalised weighted value sum of part p (chen3feng vLLM analysis,
+ * section 7.3: the partitioned kernel's parts are combined by rescaling with
+ * the online-softmax correction).  out[d] = sum_p e^(m_p - M) o_p[d] /
+ * sum_p e^(m_p - M) l_p with M = max_p m_p. */
+int or_merge_partials(double *out, const double *m, const double *l, const double *o,
+                      int parts, int D)
+{
+    if (parts <= 0 || D <= 0)
+        return OR_ERR_ARG;
+    double M = m[0];
+    for (int p = 1; p < parts; p++)
+        if (m[p] > M)
+            M = m[p];
+    double denom = 0.0;
+    for (int p = 0; p < parts; p++)
+        denom += exp(m[p] - M) * l[p];
+    for (int d = 0; d < D; d++) {
+        double num = 0.0;
+        for (int p = 0; p < parts; p++)
+            num += exp(m[p] - M) * o[(size_t)p * D + d];
+        out[d] = num / denom;
+    }
+    return OR_OK;
+}
+
+/* Host check of the caller preconditions the CUDA library documents:
+ * 0 <= seq_lens[s] <= max_blocks_per_seq * block_size and every block id a
+ * sequence uses lies in [0, num_blocks).  Returns OR_OK or an error code. */
+int or_check_tables(const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                    int max_blocks_per_seq, int block_size, int num_blocks)
+{
+    for (int s = 0; s < num_seqs; s++) {
+        int L = seq_lens[s];
+        if (L < 0 || L > max_blocks_per_seq * block_size)
+            return OR_ERR_SEQ_LEN;
+        int nb = (L + block_size - 1) / block_size;
+        for (int j = 0; j < nb; j++) {
+            int32_t b = block_tables[(size_t)s * max_blocks_per_seq + j];
+            if (b < 0 || b >= num_blocks)
+                return OR_ERR_BLOCK_ID;
+        }
+    }
+    return OR_OK;
+}

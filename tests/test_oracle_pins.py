@@ -1,0 +1,468 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks the oracle against something independent: the pages' worked
+example, another implementation of a number format (numpy, torch), a library
+attention routine (torch's scaled_dot_product_attention in fp64), brute force,
+closed forms, or invariants the pages state.  Together they are chosen so that
+a plausible slip anywhere in the oracle (a dropped term, a wrong sign, index or
+head mapping, a transposed operand, a wrong rounding) fails at least one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.oracle import BF16, FP16, Oracle, OracleError, get
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def orc():
+    # PA_ORACLE_SO points the pins at another build of the oracle source (the
+    # mutation test uses it to show that planted mistakes are caught).
+    so = os.environ.get("PA_ORACLE_SO")
+    return Oracle(so) if so else get()
+
+
+ALL_BITS = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Number formats
+# ---------------------------------------------------------------------------
+
+def test_half_decode_matches_numpy(orc):
+    got = orc.widen(ALL_BITS, FP16)
+    ref = ALL_BITS.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_bf16_decode_matches_torch(orc):
+    got = orc.widen(ALL_BITS, BF16)
+    ref = torch.from_numpy(ALL_BITS.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def _finite_table(orc, dtype):
+    vals = orc.widen(ALL_BITS, dtype)
+    fin = np.isfinite(vals)
+    return ALL_BITS[fin], vals[fin]
+
+
+def _brute_round(x, bits_tab, vals_tab, maxval, dtype_bits):
+    """Nearest finite value, ties to the even significand; beyond the
+    overflow threshold the result is infinity."""
+    out = []
+    for v in x:
+        a = abs(v)
+        if a >= maxval:
+            out.append(None)
+            continue
+        d = np.abs(vals_tab - v)
+        best = d.min()
+        cand = bits_tab[d == best]
+        cand = [c for c in cand if (int(c) >> 15) == (1 if v < 0 or (v == 0 and math.copysign(1, v) < 0) else 0)] or list(cand)
+        if len(cand) > 1:
+            cand = [c for c in cand if int(c) & 1 == 0] or cand
+        out.append(int(cand[0]))
+    return out
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+def test_encode_matches_brute_force(orc, dtype):
+    rng = np.random.default_rng(7)
+    bits_tab, vals_tab = _finite_table(orc, dtype)
+    # Random values over the whole range, exact ties between neighbours, and
+    # subnormals.
+    if dtype == FP16:
+        mags = np.exp(rng.uniform(np.log(1e-8), np.log(6e4), 400))
+    else:
+        mags = np.exp(rng.uniform(np.log(1e-39), np.log(3e38), 400))
+    x = mags * rng.choice([-1.0, 1.0], mags.size)
+    pos = np.sort(vals_tab[vals_tab > 0])
+    idx = rng.integers(0, pos.size - 1, 200)
+    ties = (pos[idx] + pos[idx + 1]) / 2.0      # exact in double
+    x = np.concatenate([x, ties, -ties[:50], [0.0, -0.0]])
+    got = orc.round_to(x, dtype)
+    # Overflow threshold: halfway between the largest finite value and the
+    # next power of two (which is where a wider exponent would put it).
+    maxfin = pos[-1]
+    step = maxfin - pos[-2]
+    thresh = maxfin + step / 2.0
+    ref = _brute_round(x, bits_tab, vals_tab, thresh, dtype)
+    for xi, g, r in zip(x, got, ref):
+        if r is None:
+            assert (int(g) & 0x7fff) == (0x7c00 if dtype == FP16 else 0x7f80), xi
+        else:
+            assert int(g) == r, (xi, hex(int(g)), hex(r))
+
+
+def test_half_encode_matches_numpy(orc):
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(20000) * 4.0,
+                        rng.standard_normal(2000) * 1e-6,      # subnormal range
+                        rng.standard_normal(200) * 7e4])       # overflow range
+    got = orc.round_to(x, FP16)
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_encode_matches_torch_for_float32_inputs(orc):
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal(20000) * 3.0).astype(np.float32).astype(np.float64)
+    got = orc.round_to(x, BF16)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# Address translation: the pages' worked example
+# ---------------------------------------------------------------------------
+
+def test_38_token_example(orc):
+    g = json.load(open(os.path.join(GOLDEN, "block_table_38_tokens.json")))
+    bs, n, bt = g["block_size"], g["num_tokens"], g["block_table"]
+    counts = {}
+    offsets = {}
+    order = []
+    for t in range(n):
+        phys, off = orc.translate(bt, t, bs)
+        counts[phys] = counts.get(phys, 0) + 1
+        offsets.setdefault(phys, []).append(off)
+        if not order or order[-1] != phys:
+            order.append(phys)
+    assert order == [b["physical"] for b in g["blocks"]]
+    for b in g["blocks"]:
+        assert counts[b["physical"]] == b["tokens"]
+        assert offsets[b["physical"]] == list(range(b["tokens"]))
+    assert orc.slot_of_token(bt, g["derived"]["last_token"], bs) == g["derived"]["last_token_slot"]
+
+
+# ---------------------------------------------------------------------------
+# Cache write
+# ---------------------------------------------------------------------------
+
+def _rand_bits(rng, shape, dtype):
+    x = rng.standard_normal(shape)
+    if dtype == FP16:
+        return x.astype(np.float16).view(np.uint16)
+    return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("stride_pad", [0, 24])
+def test_reshape_matches_flat_slot_indexing(orc, stride_pad):
+    rng = np.random.default_rng(11)
+    T, Hkv, D, bs, NB = 9, 3, 32, 16, 7
+    sentinel = np.uint16(0xABCD)
+    cache = np.full((2, NB, bs, Hkv, D), sentinel, dtype=np.uint16)
+    row = Hkv * D + stride_pad
+    key = _rand_bits(rng, (T, row), FP16)
+    value = _rand_bits(rng, (T, row), FP16)
+    slots = rng.choice(NB * bs, T, replace=False).astype(np.int64)
+    slots[[1, 5]] = -1
+    got = orc.reshape_and_cache(key, value, cache, slots, bs, key_stride=row, value_stride=row)
+    # The page's statement with the pool viewed as [2, num_slots, Hkv*D]:
+    # key_cache[slot] = key[token], value_cache[slot] = value[token].
+    ref = cache.reshape(2, NB * bs, Hkv * D).copy()
+    ok = slots >= 0
+    ref[0, slots[ok]] = key[ok, :Hkv * D]
+    ref[1, slots[ok]] = value[ok, :Hkv * D]
+    assert np.array_equal(got.reshape(2, NB * bs, Hkv * D), ref)
+    # Padding tokens wrote nothing: exactly the valid slots changed.
+    changed = np.any(got.reshape(2, NB * bs, -1) != sentinel, axis=2)
+    assert set(np.nonzero(changed[0])[0]) <= set(slots[ok])
+
+
+def test_reshape_rejects_out_of_range_slot(orc):
+    cache = np.zeros((2, 2, 16, 1, 8), np.uint16)
+    k = np.zeros((1, 8), np.uint16)
+    with pytest.raises(OracleError):
+        orc.reshape_and_cache(k, k, cache, np.array([32], np.int64), 16)
+
+
+# ---------------------------------------------------------------------------
+# Decode attention against a library attention routine
+# ---------------------------------------------------------------------------
+
+def _case(rng, lens, H, Hkv, D, bs, dtype, contiguous=True, extra_blocks=3):
+    B = len(lens)
+    nblk = [-(-L // bs) for L in lens]
+    MB = max(max(nblk), 1)
+    NB = sum(nblk) + extra_blocks
+    cache = _rand_bits(rng, (2, NB, bs, Hkv, D), dtype)
+    q = _rand_bits(rng, (B, H, D), dtype)
+    bt = np.full((B, MB), -1, np.int32)
+    ids = np.arange(NB, dtype=np.int32) if contiguous else rng.permutation(NB).astype(np.int32)
+    c = 0
+    starts = []
+    for s in range(B):
+        bt[s, :nblk[s]] = ids[c:c + nblk[s]]
+        starts.append(c)
+        c += nblk[s]
+    return q, cache, bt, np.array(lens, np.int32), NB, starts
+
+
+def _sdpa_contiguous(orc, q, cache, lens, starts, H, Hkv, D, bs, scale, dtype):
+    """torch SDPA in fp64 over each sequence's rows, read as a flat slice of
+    the pool (the blocks of a sequence are consecutive here)."""
+    B = len(lens)
+    qd = torch.from_numpy(orc.widen(q, dtype))
+    kd = torch.from_numpy(orc.widen(cache[0], dtype)).reshape(-1, Hkv, D)
+    vd = torch.from_numpy(orc.widen(cache[1], dtype)).reshape(-1, Hkv, D)
+    out = np.zeros((B, H, D))
+    G = H // Hkv
+    for s in range(B):
+        L = int(lens[s])
+        if L == 0:
+            continue
+        k = kd[starts[s] * bs: starts[s] * bs + L].permute(1, 0, 2)      # [Hkv, L, D]
+        v = vd[starts[s] * bs: starts[s] * bs + L].permute(1, 0, 2)
+        k = k.repeat_interleave(G, dim=0)                                  # q head h -> kv head h // G
+        v = v.repeat_interleave(G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qd[s][:, None, :], k, v, scale=scale)
+        out[s] = o[:, 0, :].numpy()
+    return out
+
+
+CASES = [
+    # lens, H, Hkv, D, bs, dtype
+    ([1, 17, 33, 64], 4, 4, 64, 16, FP16),
+    ([15, 16, 17, 100], 8, 2, 64, 16, BF16),
+    ([31, 32, 33, 511, 513], 8, 1, 128, 32, BF16),
+    ([200, 7], 16, 2, 128, 16, FP16),
+]
+
+
+@pytest.mark.parametrize("lens,H,Hkv,D,bs,dtype", CASES)
+def test_decode_matches_sdpa(orc, lens, H, Hkv, D, bs, dtype):
+    rng = np.random.default_rng(sum(lens) + H)
+    q, cache, bt, sl, NB, starts = _case(rng, lens, H, Hkv, D, bs, dtype)
+    scale = 1.0 / math.sqrt(D)
+    got = orc.decode(q, cache, bt, sl, Hkv, bs, scale, dtype, nthreads=2)
+    ref = _sdpa_contiguous(orc, q, cache, sl, starts, H, Hkv, D, bs, scale, dtype)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_decode_scale_is_applied(orc):
+    rng = np.random.default_rng(21)
+    lens = [40, 9]
+    q, cache, bt, sl, NB, starts = _case(rng, lens, 4, 2, 64, 16, FP16)
+    for scale in (0.05, 1.0, 0.3):
+        got = orc.decode(q, cache, bt, sl, 2, 16, scale, FP16)
+        ref = _sdpa_contiguous(orc, q, cache, sl, starts, 4, 2, 64, 16, scale, FP16)
+        np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Invariants the pages state
+# ---------------------------------------------------------------------------
+
+def test_permutation_of_physical_blocks_is_invisible(orc):
+    """The block table only relabels storage ("KV cache 不需要物理连续，只需要可寻址")."""
+    rng = np.random.default_rng(5)
+    lens = [50, 3, 129, 64]
+    q, cache, bt, sl, NB, _ = _case(rng, lens, 8, 4, 64, 16, BF16, contiguous=False)
+    ref = orc.decode(q, cache, bt, sl, 4, 16, 0.125, BF16)
+    pi = rng.permutation(NB).astype(np.int32)
+    cache2 = np.empty_like(cache)
+    cache2[:, pi] = cache                       # block b moves to pi[b]
+    bt2 = np.where(bt >= 0, pi[np.maximum(bt, 0)], -1).astype(np.int32)
+    got = orc.decode(q, cache2, bt2, sl, 4, 16, 0.125, BF16)
+    assert np.array_equal(got, ref)
+
+
+def test_shared_blocks_equal_copied_blocks(orc):
+    """Prefix blocks shared by reference give the same result as private copies."""
+    rng = np.random.default_rng(6)
+    bs, Hkv, D, H = 16, 2, 64, 4
+    prefix_blocks, B = 3, 4
+    suffix = [5, 16, 17, 1]
+    MB = prefix_blocks + 2
+    NB = prefix_blocks * (B + 1) + 2 * B
+    cache = _rand_bits(rng, (2, NB, bs, Hkv, D), FP16)
+    q = _rand_bits(rng, (B, H, D), FP16)
+    shared = np.arange(prefix_blocks, dtype=np.int32)
+    bt_ref = np.full((B, MB), -1, np.int32)
+    bt_cpy = np.full((B, MB), -1, np.int32)
+    cache_cpy = cache.copy()
+    nxt = prefix_blocks
+    for s in range(B):
+        bt_ref[s, :prefix_blocks] = shared
+        copies = np.arange(nxt, nxt + prefix_blocks, dtype=np.int32)
+        nxt += prefix_blocks
+        cache_cpy[:, copies] = cache[:, shared]
+        bt_cpy[s, :prefix_blocks] = copies
+        k = -(-suffix[s] // bs)
+        own = np.arange(nxt, nxt + k, dtype=np.int32)
+        nxt += k
+        bt_ref[s, prefix_blocks:prefix_blocks + k] = own
+        bt_cpy[s, prefix_blocks:prefix_blocks + k] = own
+    sl = np.array([prefix_blocks * bs + x for x in suffix], np.int32)
+    a = orc.decode(q, cache, bt_ref, sl, Hkv, bs, 0.125, FP16)
+    b = orc.decode(q, cache_cpy, bt_cpy, sl, Hkv, bs, 0.125, FP16)
+    assert np.array_equal(a, b)
+
+
+def test_tail_of_last_block_is_ignored(orc):
+    """Rows past seq_len in the last block never reach the output."""
+    rng = np.random.default_rng(8)
+    q, cache, bt, sl, NB, _ = _case(rng, [20, 33], 4, 4, 64, 16, FP16, contiguous=False)
+    ref = orc.decode(q, cache, bt, sl, 4, 16, 0.125, FP16)
+    poisoned = cache.copy()
+    for s, L in enumerate(sl):
+        last = bt[s, (L - 1) // 16]
+        poisoned[:, last, (L - 1) % 16 + 1:] = 0x7E00        # fp16 NaN
+    got = orc.decode(q, poisoned, bt, sl, 4, 16, 0.125, FP16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# Closed forms
+# ---------------------------------------------------------------------------
+
+def _gathered_v(orc, cache, bt, L, kvh, bs, dtype):
+    rows = [cache[1, bt[t // bs], t % bs, kvh] for t in range(L)]
+    return orc.widen(np.stack(rows), dtype)
+
+
+def test_zero_query_gives_mean_of_values(orc):
+    rng = np.random.default_rng(9)
+    lens = [1, 16, 45]
+    q, cache, bt, sl, NB, _ = _case(rng, lens, 4, 2, 64, 16, BF16, contiguous=False)
+    q[:] = 0
+    got = orc.decode(q, cache, bt, sl, 2, 16, 0.125, BF16)
+    for s, L in enumerate(lens):
+        for h in range(4):
+            v = _gathered_v(orc, cache, bt[s], L, h // 2, 16, BF16)
+            np.testing.assert_allclose(got[s, h], v.mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_zero_scale_gives_mean_of_values(orc):
+    rng = np.random.default_rng(10)
+    q, cache, bt, sl, NB, _ = _case(rng, [30], 2, 1, 64, 16, FP16, contiguous=False)
+    got = orc.decode(q, cache, bt, sl, 1, 16, 0.0, FP16)
+    v = _gathered_v(orc, cache, bt[0], 30, 0, 16, FP16)
+    np.testing.assert_allclose(got[0, 0], v.mean(axis=0), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(got[0, 1], v.mean(axis=0), rtol=1e-12, atol=1e-13)
+
+
+def test_single_token_returns_its_value(orc):
+    rng = np.random.default_rng(12)
+    q, cache, bt, sl, NB, _ = _case(rng, [1, 1], 4, 2, 64, 16, FP16, contiguous=False)
+    got = orc.decode(q, cache, bt, sl, 2, 16, 0.125, FP16)
+    for s in range(2):
+        for h in range(4):
+            v = orc.widen(cache[1, bt[s, 0], 0, h // 2], FP16)
+            assert np.array_equal(got[s, h], v)
+
+
+def test_one_hot_score_selects_one_value(orc):
+    rng = np.random.default_rng(13)
+    L, D, bs, jstar = 40, 64, 16, 27
+    q, cache, bt, sl, NB, _ = _case(rng, [L], 1, 1, D, bs, FP16, contiguous=False)
+    q[:] = 0
+    q[0, 0, 5] = np.float16(1.0).view(np.uint16)
+    for t in range(L):
+        cache[0, bt[0, t // bs], t % bs, 0, :] = 0
+    cache[0, bt[0, jstar // bs], jstar % bs, 0, 5] = np.float16(64.0).view(np.uint16)
+    got = orc.decode(q, cache, bt, sl, 1, bs, 1.0, FP16)
+    v = _gathered_v(orc, cache, bt[0], L, 0, bs, FP16)
+    # weight of every other token is e^-64 relative to token j*.
+    bound = (L - 1) * math.exp(-64) * np.abs(v).max() * 2
+    assert np.abs(got[0, 0] - v[jstar]).max() <= bound
+
+
+def test_empty_sequence_gives_zero_row(orc):
+    rng = np.random.default_rng(14)
+    q, cache, bt, sl, NB, _ = _case(rng, [5, 9], 2, 2, 64, 16, FP16)
+    sl = np.array([0, 9], np.int32)
+    got = orc.decode(q, cache, bt, sl, 2, 16, 0.125, FP16)
+    assert np.array_equal(got[0], np.zeros((2, 64)))
+
+
+# ---------------------------------------------------------------------------
+# Online softmax: the pages' identity, and the partition merge
+# ---------------------------------------------------------------------------
+
+def test_online_softmax_equals_two_pass(orc):
+    rng = np.random.default_rng(15)
+    n, D = 1000, 32
+    a = rng.standard_normal(n) * 6.0
+    V = rng.standard_normal((n, D))
+    w = np.exp(a - a.max())
+    ref = (w[:, None] * V).sum(0) / w.sum()
+    for block in (1, 3, 16, 512, n):
+        out, m, l = orc.online_softmax(a, V, block)
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+        assert m == a.max()
+        np.testing.assert_allclose(l, w.sum(), rtol=1e-12)
+
+
+def test_merge_of_partition_states_equals_whole(orc):
+    rng = np.random.default_rng(16)
+    n, D, P = 1300, 16, 512
+    a = rng.standard_normal(n) * 5.0
+    V = rng.standard_normal((n, D))
+    ms, ls, os_ = [], [], []
+    for p0 in range(0, n, P):
+        aa = a[p0:p0 + P]
+        m = aa.max()
+        w = np.exp(aa - m)
+        ms.append(m)
+        ls.append(w.sum())
+        os_.append((w[:, None] * V[p0:p0 + P]).sum(0))
+    got = orc.merge_partials(np.array(ms), np.array(ls), np.array(os_))
+    w = np.exp(a - a.max())
+    ref = (w[:, None] * V).sum(0) / w.sum()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_decode_equals_online_merge_over_blocks(orc):
+    """Two-pass decode == online merge over the gathered blocks."""
+    rng = np.random.default_rng(17)
+    L, D, bs = 77, 64, 16
+    q, cache, bt, sl, NB, _ = _case(rng, [L], 1, 1, D, bs, BF16, contiguous=False)
+    got = orc.decode(q, cache, bt, sl, 1, bs, 0.125, BF16)[0, 0]
+    qd = orc.widen(q[0, 0], BF16)
+    K = np.stack([orc.widen(cache[0, bt[0, t // bs], t % bs, 0], BF16) for t in range(L)])
+    V = _gathered_v(orc, cache, bt[0], L, 0, bs, BF16)
+    out, _, _ = orc.online_softmax(0.125 * (K @ qd), V, bs)
+    np.testing.assert_allclose(got, out, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Preconditions
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_is_rejected(orc):
+    rng = np.random.default_rng(18)
+    q, cache, bt, sl, NB, _ = _case(rng, [20], 2, 2, 64, 16, FP16)
+    bt[0, 1] = NB
+    with pytest.raises(OracleError):
+        orc.decode(q, cache, bt, sl, 2, 16, 0.125, FP16)
+    assert orc.check_tables(bt, sl, 16, NB) != 0
+
+
+def test_seq_len_beyond_table_is_rejected(orc):
+    rng = np.random.default_rng(19)
+    q, cache, bt, sl, NB, _ = _case(rng, [20], 2, 2, 64, 16, FP16)
+    sl[0] = bt.shape[1] * 16 + 1
+    with pytest.raises(OracleError):
+        orc.decode(q, cache, bt, sl, 2, 16, 0.125, FP16)
+
+
+def test_output_rounding_matches_numpy_half(orc):
+    rng = np.random.default_rng(20)
+    q, cache, bt, sl, NB, _ = _case(rng, [33, 64], 4, 4, 64, 16, FP16, contiguous=False)
+    out = orc.decode(q, cache, bt, sl, 4, 16, 0.125, FP16)
+    assert np.array_equal(orc.round_to(out, FP16), out.astype(np.float16).view(np.uint16))

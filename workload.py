@@ -1,0 +1,255 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module only draws inputs: sequence lengths, a shuffled pool of physical
+blocks dealt out to block tables, N(0,1) queries/keys/values, NaN poison for
+memory no sequence owns, and the per-token write targets of the cache-write
+step.  It computes nothing that the attention path computes.  Both the CUDA
+library's tests/benchmark and the CPU oracle receive the same tensors from it;
+neither side imports the other.
+
+The write target of a new token is stated the way a serving engine's metadata
+builder hands it to the cache-write kernel: the flat slot index
+``block_number * block_size + block_offset`` ("PagedAttention 在 vLLM 中的实现
+分析", section 3.2 "Slot Mapping").  Each new token lands at its sequence's last
+position ``seq_len - 1``, so the decode step that follows reads it.
+
+Workloads (seed = the config index unless given):
+
+- ``tiny``: 4 sequences of lengths {1, 17, 33, 64}, block_size 16, 4 q / 4 kv
+  heads, head_size 64, fp16, pool of 32 blocks, tables taken from a random
+  permutation of the pool, scale 1/8, 4 new tokens of which token 2 is padding
+  (slot -1).
+- ``mha7b``: 64 sequences, lengths uniform on [128, 2048], 32/32 heads,
+  head_size 128, block_size 16, fp16, pool 1.25x the blocks in use, blocks
+  scattered at random, 64 new tokens.
+- ``gqa8b``: 256 sequences, lengths round(exp(ln 500 + z)), z ~ N(0,1),
+  clipped to [16, 4096], 32 q / 8 kv heads, head_size 128, block_size 16, bf16.
+- ``long``: 8 sequences of 131072 tokens, 64 q / 8 kv heads, head_size 128,
+  block_size 32, bf16; 1% of the (token, kv head) key rows are scaled by 8.
+- ``prefix``: 128 sequences sharing one 2000-token prefix (the same 125
+  physical blocks in every table) followed by a private suffix of uniform
+  [50, 500] tokens starting at a block boundary, 32 q / 8 kv heads,
+  head_size 128, block_size 16, bf16.
+
+Q, K and V are N(0,1) draws rounded to the cache dtype.  With ``poison=True``
+every pool row that no sequence owns (unused blocks and the tail of each
+sequence's last block) holds NaN, so a read past a sequence's end shows up in
+its output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+CONFIG_NAMES = ("tiny", "mha7b", "gqa8b", "long", "prefix")
+
+
+@dataclass
+class Workload:
+    name: str
+    q: torch.Tensor                 # [B, H, D]
+    kv_cache: torch.Tensor          # [2, NB, bs, Hkv, D]
+    block_tables: torch.Tensor      # [B, MB] int32, unused entries -1
+    seq_lens: torch.Tensor          # [B] int32
+    key: torch.Tensor               # [T, Hkv, D] new tokens
+    value: torch.Tensor             # [T, Hkv, D]
+    slot_mapping: torch.Tensor      # [T] int64, -1 = padding
+    block_size: int
+    scale: float
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    partition_size: int = 512
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kv_cache.shape[1])
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.q.dtype
+
+    def kv_bytes(self) -> int:
+        """Bytes of K and V the decode must read: one row per
+        (sequence, token, kv head) for K and for V."""
+        el = self.kv_cache.element_size()
+        tokens = int(self.seq_lens.to(torch.int64).sum().item())
+        return tokens * self.num_kv_heads * self.head_size * el * 2
+
+    def unique_kv_bytes(self) -> int:
+        """Bytes of distinct pool rows in use (shared blocks counted once)."""
+        el = self.kv_cache.element_size()
+        bt = self.block_tables.cpu().numpy()
+        sl = self.seq_lens.cpu().numpy()
+        rows = set()
+        for s in range(bt.shape[0]):
+            L = int(sl[s])
+            nb = -(-L // self.block_size)
+            for j in range(nb):
+                n = min(self.block_size, L - j * self.block_size)
+                rows.add((int(bt[s, j]), n))
+        used = {}
+        for b, n in rows:
+            used[b] = max(used.get(b, 0), n)
+        tokens = sum(used.values())
+        return tokens * self.num_kv_heads * self.head_size * el * 2
+
+    def to(self, device) -> "Workload":
+        w = Workload(**{k: getattr(self, k) for k in self.__dataclass_fields__})
+        for k in ("q", "kv_cache", "block_tables", "seq_lens", "key", "value", "slot_mapping"):
+            setattr(w, k, getattr(self, k).to(device))
+        return w
+
+
+@dataclass
+class Spec:
+    name: str
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    dtype: torch.dtype
+    pool_factor: float = 1.25
+
+
+SPECS = {
+    "tiny": Spec("tiny", 4, 4, 4, 64, 16, torch.float16),
+    "mha7b": Spec("mha7b", 64, 32, 32, 128, 16, torch.float16),
+    "gqa8b": Spec("gqa8b", 256, 32, 8, 128, 16, torch.bfloat16),
+    "long": Spec("long", 8, 64, 8, 128, 32, torch.bfloat16),
+    "prefix": Spec("prefix", 128, 32, 8, 128, 16, torch.bfloat16),
+}
+
+
+def _lengths(name: str, rng: np.random.Generator, spec: Spec) -> np.ndarray:
+    if name == "tiny":
+        return np.array([1, 17, 33, 64], dtype=np.int64)
+    if name == "mha7b":
+        return rng.integers(128, 2048, size=spec.num_seqs, endpoint=True)
+    if name == "gqa8b":
+        z = rng.standard_normal(spec.num_seqs)
+        return np.clip(np.rint(np.exp(math.log(500.0) + z)), 16, 4096).astype(np.int64)
+    if name == "long":
+        return np.full(spec.num_seqs, 131072, dtype=np.int64)
+    if name == "prefix":
+        return 2000 + rng.integers(50, 500, size=spec.num_seqs, endpoint=True)
+    raise KeyError(name)
+
+
+def _randn(shape, gen: torch.Generator, device, dtype, chunk_rows: int = 1 << 14):
+    """N(0,1) rounded to dtype, drawn chunk by chunk along dim 0 to bound
+    the fp32 transient."""
+    out = torch.empty(shape, dtype=dtype, device=device)
+    n0 = shape[0]
+    for i in range(0, n0, chunk_rows):
+        j = min(n0, i + chunk_rows)
+        out[i:j] = torch.randn((j - i,) + tuple(shape[1:]), generator=gen, device=device,
+                               dtype=torch.float32).to(dtype)
+    return out
+
+
+def make(name: str, seed: int | None = None, device="cpu", poison: bool = False,
+         num_seqs: int | None = None, lengths=None, **overrides) -> Workload:
+    """Build one workload.  ``num_seqs``/``lengths``/spec fields may be
+    overridden to make smaller cases with the same structure."""
+    if seed is None:
+        seed = CONFIG_NAMES.index(name) + 1
+    spec = SPECS[name]
+    spec = Spec(**{**spec.__dict__, **{k: v for k, v in overrides.items()
+                                       if k in spec.__dict__}})
+    if num_seqs is not None:
+        spec.num_seqs = num_seqs
+    rng = np.random.default_rng(seed)
+    if lengths is not None:
+        L = np.asarray(lengths, dtype=np.int64)
+        spec.num_seqs = L.size
+    else:
+        L = _lengths(name, rng, spec)[: spec.num_seqs]
+    B, H, Hkv, D, bs = spec.num_seqs, spec.num_heads, spec.num_kv_heads, spec.head_size, spec.block_size
+    nblk = -(-L // bs)                      # blocks each sequence owns
+    MB = max(1, int(nblk.max()) if B else 1)
+
+    if name == "prefix" and lengths is None:
+        shared = 2000 // bs                 # 125 blocks shared by every sequence
+        private = nblk - shared
+        need = shared + int(private.sum())
+    else:
+        shared = 0
+        need = int(nblk.sum())
+    if name == "tiny" and lengths is None:
+        NB = 32
+    else:
+        NB = max(need, int(math.ceil(spec.pool_factor * need)))
+
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((B, MB), -1, dtype=np.int32)
+    cursor = 0
+    prefix_ids = perm[:shared]
+    cursor = shared
+    for s in range(B):
+        tables[s, :shared] = prefix_ids
+        k = int(nblk[s]) - shared
+        tables[s, shared:shared + k] = perm[cursor:cursor + k]
+        cursor += k
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    q = _randn((B, H, D), gen, device, spec.dtype)
+    cache = torch.empty((2, NB, bs, Hkv, D), dtype=spec.dtype, device=device)
+    cache[0] = _randn((NB, bs, Hkv, D), gen, device, spec.dtype, chunk_rows=1 << 12)
+    cache[1] = _randn((NB, bs, Hkv, D), gen, device, spec.dtype, chunk_rows=1 << 12)
+    if name == "long":
+        # 1% of the (token, kv head) key rows get 8x magnitude.
+        for i in range(0, NB, 1 << 12):
+            j = min(NB, i + (1 << 12))
+            sel = torch.rand((j - i, bs, Hkv, 1), generator=gen, device=device) < 0.01
+            blk = cache[0, i:j]
+            blk.copy_(torch.where(sel, blk.float() * 8.0, blk.float()).to(spec.dtype))
+
+    # New tokens, one per sequence, written at position seq_len - 1.
+    T = B
+    key = _randn((T, Hkv, D), gen, device, spec.dtype)
+    value = _randn((T, Hkv, D), gen, device, spec.dtype)
+    slots = np.empty(T, dtype=np.int64)
+    for s in range(T):
+        pos = int(L[s]) - 1
+        slots[s] = int(tables[s, pos // bs]) * bs + pos % bs if pos >= 0 else -1
+    if name == "tiny" and T > 2:
+        slots[2] = -1                       # one padding token
+
+    if poison:
+        owned = np.zeros((NB, bs), dtype=bool)
+        for s in range(B):
+            for j in range(int(nblk[s])):
+                n = min(bs, int(L[s]) - j * bs)
+                owned[tables[s, j], :n] = True
+        mask = torch.from_numpy(~owned).to(device)
+        nan = torch.tensor(float("nan"), dtype=spec.dtype, device=device)
+        for plane in range(2):
+            cache[plane][mask] = nan
+
+    return Workload(
+        name=name, q=q, kv_cache=cache,
+        block_tables=torch.from_numpy(tables).to(device),
+        seq_lens=torch.from_numpy(L.astype(np.int32)).to(device),
+        key=key, value=value, slot_mapping=torch.from_numpy(slots).to(device),
+        block_size=bs, scale=1.0 / math.sqrt(D), num_heads=H, num_kv_heads=Hkv,
+        head_size=D, meta={"seed": seed, "shared_blocks": shared, "poison": poison},
+    )
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """Host uint16 view of an fp16/bf16 tensor's bit patterns."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+ORACLE_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
