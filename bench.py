@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode-attention hot path.
+
+Metric: effective KV-read GB/s (and % of the HBM peak) plus sequences/s.
+KV bytes per step = sum_s seq_len_s * num_kv_heads * head_size * 2 (K and V)
+* element size: each (sequence, token, kv head) row of K and of V counted once,
+no block-tail padding and no re-reads by grouped query heads.
+
+Default workload (one GPU): the MHA 7B-like decode layer -- 64 sequences with
+lengths uniform on [128, 2048], 32 q / 32 kv heads, head_size 128,
+block_size 16, fp16 pool [2, num_blocks, 16, 32, 128] 1.25x the blocks in use
+with blocks scattered at random, N(0,1) data.  One step = the cache write of
+the 64 new tokens (pa_reshape_and_cache) followed by one decode pass over all
+sequences (pa_decode_splitk with 512-token partitions, or pa_decode with
+--decode onepass).  The KV pool (1.4 GB) is larger than the 129 MB L2, so no
+L2 flush is needed between steps.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 the script runs under torch.distributed.run, one replica per GPU on
+its own seeded batch (weak scaling, no data-path collective); the timed region
+is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: effective KV-read GB/s (% of HBM peak), seqs/s"
+UNIT = "GB/s"
+WORKLOAD_TEXT = {
+    "mha7b": "MHA 7B-like decode layer: 64 seqs, seq_lens U[128,2048], 32 q / 32 kv heads, "
+             "head_size 128, block_size 16, fp16 cache, blocks scattered in a 1.25x pool, "
+             "+ cache write of 64 new tokens",
+    "gqa8b": "GQA 8B-like decode: 256 seqs, lognormal seq_lens (median 500, sigma 1) clipped to "
+             "[16,4096], 32 q / 8 kv heads, head_size 128, block_size 16, bf16",
+    "long": "long-context split-K: 8 seqs x 131072 tokens, 64 q / 8 kv heads, head_size 128, "
+            "block_size 32, bf16, 512-token partitions",
+    "prefix": "prefix sharing: 128 seqs sharing a 2000-token prefix + U[50,500] suffix, "
+              "32 q / 8 kv heads, head_size 128, block_size 16, bf16",
+    "tiny": "tiny: 4 seqs {1,17,33,64}, 4/4 heads, head_size 64, block_size 16, fp16",
+}
+DECODE_SOURCES = ["paged_kv_cache_136_gb300/csrc/pa_decode.cuh",
+                  "paged_kv_cache_136_gb300/csrc/pa_ptx.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas only: barriers and max/sum of scalars)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_scalar(x: float, op: str, dist_mod, device="cpu") -> float:
+    """max or sum of one float over all ranks (identity on one rank)."""
+    if dist_mod is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX if op == "max" else dist_mod.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(dist_mod):
+    if dist_mod is not None:
+        dist_mod.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.4)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting (algorithmic, per step / per launch)
+# ---------------------------------------------------------------------------
+
+def kv_bytes(w) -> int:
+    return w.kv_bytes()
+
+
+def decode_launch_bytes(w, split: bool, partition: int) -> int:
+    """Bytes the decode call must move: KV rows once, q, out, the block-table
+    entries in use, seq_lens, and for split-K the partial states written by
+    the partition kernel and read back by the reduce."""
+    import torch
+    el = w.kv_cache.element_size()
+    L = w.seq_lens.to(torch.int64)
+    nblk = int(((L + w.block_size - 1) // w.block_size).sum().item())
+    b = kv_bytes(w) + 2 * w.q.numel() * el + nblk * 4 + w.num_seqs * 4
+    if split:
+        parts = int(((L + partition - 1) // partition).sum().item())
+        b += 2 * parts * w.num_heads * (w.head_size + 2) * 4
+    return b
+
+
+def reshape_launch_bytes(w) -> int:
+    valid = int((w.slot_mapping >= 0).sum().item())
+    row = w.num_kv_heads * w.head_size * w.kv_cache.element_size()
+    return 2 * 2 * valid * row + w.slot_mapping.numel() * 8
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str, decode: str) -> int | None:
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"decode_{decode}_{config}.md")
+    if not os.path.exists(path):
+        return None
+    m = re.search(r"bench-traffic:\s*bytes=(\d+)\s+source=([0-9a-f]+)", open(path).read())
+    if not m or m.group(2) != source_digest():
+        return None
+    return int(m.group(1))
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_run(w, groups, nthreads: int):
+    """Run the oracle on (seq, kv head) groups, all query heads of each group;
+    returns (seconds, kv bytes covered)."""
+    import numpy as np
+    import workload as wl
+    from oracle.oracle import get
+    orc = get()
+    G = w.num_heads // w.num_kv_heads
+    items = np.array([s * w.num_heads + kvh * G + g for s, kvh in groups for g in range(G)],
+                     dtype=np.int32)
+    q = wl.bits(w.q)
+    cache = wl.bits(w.kv_cache)
+    bt = w.block_tables.cpu().numpy()
+    sl = w.seq_lens.cpu().numpy()
+    el = w.kv_cache.element_size()
+    t = time.perf_counter()
+    orc.decode(q, cache, bt, sl, w.num_kv_heads, w.block_size, w.scale,
+               wl.ORACLE_DTYPE[w.dtype], items=items, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    covered = sum(int(sl[s]) for s, _ in groups) * w.head_size * el * 2
+    return dt, covered
+
+
+def cpu_baseline(w, budget_s: float = 10.0) -> dict:
+    nthreads = os.cpu_count() or 1
+    groups_all = [(s, k) for s in range(w.num_seqs) for k in range(w.num_kv_heads)]
+    # pilot: one sequence's groups, then scale the sample to the budget
+    pilot = groups_all[: w.num_kv_heads]
+    dt, _ = oracle_sample_run(w, pilot, nthreads)
+    per_group = max(dt / len(pilot), 1e-6)
+    n = int(min(len(groups_all), max(len(pilot), budget_s / per_group)))
+    n = max(w.num_kv_heads, n // w.num_kv_heads * w.num_kv_heads)   # whole sequences
+    sample = groups_all[:n]
+    dt, covered = oracle_sample_run(w, sample, nthreads)
+    seqs = n // w.num_kv_heads
+    return {"value": covered / dt / 1e9, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"decode of sequences 0-{seqs - 1} of {w.num_seqs} (all heads), "
+                      f"fp64 two-pass oracle, {dt:.2f} s",
+            "seconds": dt, "seqs_per_s": seqs / dt}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args) -> dict | None:
+    import torch
+    rank, world, local = dist_env()
+    dist_mod = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+
+    split = args.decode == "splitk"
+    P = args.partition
+    w = wl.make(args.config, seed=args.seed + rank, device="cuda")
+    dev = w.q.device
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(w.q)
+    msl = int(w.seq_lens.max().item())
+    ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                                        msl, P), dtype=torch.uint8, device=dev)
+
+    def decode():
+        if split:
+            pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                                w.block_size, msl, ws, P)
+        else:
+            pa.pa_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                         w.block_size)
+
+    def step():
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        decode()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    pa.pa_device_errors(clear=True)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(dist_mod)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist_mod)
+    clk = clocks.stop() if clocks else None
+    ms_local = t_start.elapsed_time(t_stop)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    rsh_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    flags = pa.pa_device_errors(clear=True)
+
+    ms_max = reduce_scalar(ms_local, "max", dist_mod, dev)
+    bytes_all = reduce_scalar(float(kv_bytes(w)) * K, "sum", dist_mod, dev)
+    seqs_all = reduce_scalar(float(w.num_seqs) * K, "sum", dist_mod, dev)
+    value = bytes_all / (ms_max / 1e3) / 1e9
+
+    # End to end through the public API: per step, copy the step's inputs
+    # from pinned host memory, run the step, read the result back.
+    host = {k: getattr(w, k).cpu().pin_memory() for k in
+            ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = max(1, min(K, 200))
+
+    def e2e_step():
+        for k, t in host.items():
+            getattr(w, k).copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(dist_mod)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_local = time.perf_counter() - t0
+    barrier(dist_mod)
+    e2e_max = reduce_scalar(e2e_local, "max", dist_mod, dev)
+    e2e_bytes = reduce_scalar(float(kv_bytes(w)) * e2e_steps, "sum", dist_mod, dev)
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    dec_bytes = decode_launch_bytes(w, split, P)
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_max / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "batch": w.num_seqs, "num_heads": w.num_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
+                   "block_size": w.block_size, "storage_dtype": str(w.dtype).replace("torch.", ""),
+                   "decode": "pa_decode_splitk" if split else "pa_decode",
+                   "partition_size": P if split else None,
+                   "kv_bytes_per_step": kv_bytes(w),
+                   "l2": "inputs larger than L2: the KV pool exceeds the 129 MB L2, no flush",
+                   "parallelism": f"replicas x{world}", "seed": args.seed},
+        "seqs_per_s": round(seqs_all / (ms_max / 1e3), 1),
+        "pct_hbm_peak": round(100.0 * value / peaks["hbm_gbs"], 2),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode_splitk (partition+reduce)" if split
+                     else "pa_decode", "achieved": round(achieved, 2),
+                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": recorded_traffic(args.config, "splitk" if split else "onepass"),
+                     "algorithmic_bytes_per_launch": dec_bytes,
+                     "ms_per_launch": round(dec_ms, 5)},
+        "reshape": {"ms_per_launch": round(rsh_ms, 5),
+                    "algorithmic_bytes_per_launch": reshape_launch_bytes(w)},
+        "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": K * (3 if split else 2),
+        "clocks": clk,
+        "device_error_flags": flags,
+        "kernel_source": source_digest(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import workload as wl
+    w = wl.make(args.config, seed=args.seed, device="cpu")
+    nthreads = os.cpu_count() or 1
+    groups_all = [(s, k) for s in range(w.num_seqs) for k in range(w.num_kv_heads)]
+    dt, _ = oracle_sample_run(w, groups_all[:1], nthreads)
+    budget_per_step = max(0.05, args.ref_budget / max(1, args.steps + args.warmup))
+    n = int(max(1, min(len(groups_all), budget_per_step / max(dt, 1e-6))))
+    sample = groups_all[:n]
+    for _ in range(args.warmup):
+        oracle_sample_run(w, sample, nthreads)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, b = oracle_sample_run(w, sample, nthreads)
+        tot_t += dt
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    desc = f"{n} (sequence, kv head) groups of {len(groups_all)} per step, all query heads"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": nthreads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(WORKLOAD_TEXT), default="mha7b")
+    ap.add_argument("--decode", choices=["splitk", "onepass"], default="splitk")
+    ap.add_argument("--partition", type=int, default=512)
+    ap.add_argument("--seed", type=int, default=2)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

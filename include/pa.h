@@ -1,0 +1,186 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache decode-attention library (libpa.so).
+ *
+ * Decode-time attention over a paged KV cache, for NVIDIA GB300 (sm_103a):
+ *
+ *   pa_reshape_and_cache  scatter each new token's key/value into the pool
+ *   pa_decode             one-pass paged decode attention
+ *   pa_decode_splitk      partitioned decode attention + log-sum-exp reduce
+ *
+ * Data layout (all tensors contiguous, row-major, caller-owned):
+ *
+ *   kv_cache      [2, num_blocks, block_size, num_kv_heads, head_size]
+ *                 index 0 holds keys, index 1 values ("PagedAttention 在 vLLM
+ *                 中的实现分析", section 3.3 "KV Cache 布局", the NHD layout).
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]; entry j of row s is the
+ *                 physical block holding tokens [j*block_size, (j+1)*block_size)
+ *                 of sequence s (same page, section 3.1; "Paged attention",
+ *                 k4i.top, section "block table").  Entries past a sequence's
+ *                 last block are never read.
+ *   seq_lens      int32 [num_seqs]; number of cached tokens of each sequence,
+ *                 the token just written included.
+ *   slot_mapping  int64 [num_tokens]; slot = block_number * block_size +
+ *                 block_offset; a negative slot marks a padding token that is
+ *                 skipped (same page, section 3.2 "Slot Mapping").
+ *   q, out        [num_seqs, num_heads, head_size]; one query token per
+ *                 sequence (same page, section 7.2, stage 5 output shape).
+ *
+ * Grouped-query attention: query head h reads kv head h / (num_heads /
+ * num_kv_heads).
+ *
+ * Conventions for every entry point:
+ *   - Tensor arguments are DEVICE pointers on the current CUDA device, 16-byte
+ *     aligned.  The library never takes ownership and never frees them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls only enqueue work on it and return; results are ready
+ *     once the stream reaches that point.
+ *   - The library allocates no device memory.  The split-K path uses a
+ *     workspace the caller provides.
+ *   - Arguments are checked on the host before any launch.  Bad arguments
+ *     return PA_ERR_INVALID_ARG, shapes outside the supported set return
+ *     PA_ERR_UNSUPPORTED, and nothing is launched in either case.
+ *     PA_ERR_CUDA reports a failed launch (the CUDA error is left for the
+ *     caller's next cudaGetLastError/synchronize).
+ *   - Supported: head_size in {64, 128}; block_size in {16, 32};
+ *     num_heads / num_kv_heads in {1, 2, 4, 8}; fp16 or bf16 for q, cache and
+ *     out alike.
+ *   - Device-side guards: a block id outside [0, num_blocks), a seq_len
+ *     outside [0, max_blocks_per_seq*block_size] (or, for split-K, above
+ *     max_seq_len), or a slot at or beyond num_blocks*block_size is never
+ *     dereferenced.  The kernel skips it (ids read as zeros, lengths are
+ *     clamped, slots write nothing) and sets a bit in a sticky per-device
+ *     error word that pa_device_errors reads.  Kernels never trap.
+ *   - Every wait inside a kernel is bounded; a wait that runs out sets
+ *     PA_DEVERR_TIMEOUT and the kernel returns.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+    PA_ERR_UNSUPPORTED = 2, /* head_size / block_size / group size not built */
+    PA_ERR_WORKSPACE = 3,   /* split-K workspace missing or too small */
+    PA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+    PA_ERR_OUT_OF_RANGE = 5 /* host validation found a bad id/length/slot */
+} pa_status;
+
+typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the sticky device error word (pa_device_errors). */
+#define PA_DEVERR_BLOCK_ID 0x1u /* a block id outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 0x2u  /* a seq_len outside its allowed range */
+#define PA_DEVERR_SLOT 0x4u     /* a slot >= num_blocks * block_size */
+#define PA_DEVERR_TIMEOUT 0x8u  /* a bounded in-kernel wait ran out */
+
+/*
+ * Write new tokens into the pool ("PagedAttention 在 vLLM 中的实现分析",
+ * sections 3.2 and 7.4: for each token, slot = slot_mapping[token]; if
+ * slot >= 0, key[token] goes to key_cache[slot] and value[token] to
+ * value_cache[slot]).
+ *
+ *   key, value    [num_tokens, num_kv_heads, head_size] rows; row i starts
+ *                 at key + i*key_stride elements (key_stride >=
+ *                 num_kv_heads*head_size, multiple of 8), likewise value.
+ *   kv_cache      the pool, updated in place at block slot / block_size,
+ *                 offset slot % block_size.  Bytes are copied unchanged.
+ *   slot_mapping  int64 [num_tokens]; negative = padding, nothing written.
+ *                 Two tokens must not share a non-negative slot.
+ * num_tokens == 0 is a no-op.
+ */
+pa_status pa_reshape_and_cache(const void *key, const void *value, void *kv_cache,
+                               const int64_t *slot_mapping, int num_tokens,
+                               int num_kv_heads, int head_size, int block_size,
+                               int num_blocks, int64_t key_stride, int64_t value_stride,
+                               pa_dtype dtype, void *stream);
+
+/*
+ * One-pass paged decode attention.  For every sequence s and query head h:
+ *   out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K_t) V_t  over the
+ * sequence's tokens t < seq_lens[s], with K_t/V_t found through the block
+ * table ("Paged attention", k4i.top, section "对非连续 blocks 做 attention":
+ * blocks gathered through the table, softmax merged block by block online,
+ * equal to softmax over the whole sequence).  seq_lens[s] == 0 gives a zero
+ * row.  Accumulation is fp32; out is rounded to the input dtype (nearest
+ * even).
+ */
+pa_status pa_decode(void *out, const void *q, const void *kv_cache,
+                    const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                    int num_heads, int num_kv_heads, int head_size, int block_size,
+                    int num_blocks, int max_blocks_per_seq, float scale, pa_dtype dtype,
+                    void *stream);
+
+/*
+ * Bytes of workspace pa_decode_splitk needs for these sizes: partial states
+ * (running max, normaliser, unnormalised head_size-vector, fp32) for every
+ * (sequence, query head, partition), partitions = ceil(max_seq_len /
+ * partition_size).  Returns 0 for invalid sizes.
+ */
+size_t pa_decode_splitk_workspace_size(int num_seqs, int num_heads, int head_size,
+                                       int max_seq_len, int partition_size);
+
+/*
+ * Partitioned ("V2") paged decode attention ("PagedAttention 在 vLLM 中的实现
+ * 分析", section 7.3: each sequence's tokens are cut into partitions of
+ * partition_size tokens that are processed independently, then merged by
+ * rescaling with the online-softmax correction).  Same result as pa_decode
+ * within fp32 rounding.  Arguments as pa_decode, plus:
+ *   max_seq_len     upper bound on every seq_lens[s] (sizes the workspace)
+ *   partition_size  tokens per partition, a positive multiple of 64 (512 is
+ *                   the pages' choice)
+ *   workspace       device buffer of at least
+ *                   pa_decode_splitk_workspace_size(...) bytes, 256-byte
+ *                   aligned; its contents on entry do not matter and it is
+ *                   scratch after return.  Calls that overlap in time must
+ *                   not share a workspace.
+ */
+pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int num_heads, int num_kv_heads, int head_size, int block_size,
+                           int num_blocks, int max_blocks_per_seq, float scale,
+                           pa_dtype dtype, int max_seq_len, int partition_size,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Host-side check of the decode preconditions on HOST copies of the tables:
+ * 0 <= seq_lens[s] <= max_blocks_per_seq*block_size and every block id a
+ * sequence uses (entries j < ceil(seq_lens[s]/block_size)) in [0, num_blocks).
+ * Returns PA_OK, PA_ERR_OUT_OF_RANGE, or PA_ERR_INVALID_ARG.  No CUDA call.
+ */
+pa_status pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,
+                             int num_seqs, int max_blocks_per_seq, int block_size,
+                             int num_blocks);
+
+/*
+ * Host-side check of a HOST copy of slot_mapping: every non-negative slot
+ * below num_blocks*block_size and no slot used twice.  Returns PA_OK,
+ * PA_ERR_OUT_OF_RANGE, or PA_ERR_INVALID_ARG.  No CUDA call.
+ */
+pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int block_size,
+                            int num_blocks);
+
+/*
+ * Read (and with clear != 0, reset) the current device's sticky error word
+ * (PA_DEVERR_* bits).  Synchronises the device.  Returns PA_ERR_CUDA if the
+ * read fails.
+ */
+pa_status pa_device_errors(unsigned int *flags, int clear);
+
+/* Static, human-readable name of a status code. */
+const char *pa_status_string(pa_status status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

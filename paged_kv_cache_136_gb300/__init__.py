@@ -1,0 +1,203 @@
+"""Python binding of libpa.so: paged KV-cache decode attention on GB300.
+
+Argument marshalling only.  Each function takes torch tensors, checks their
+device/dtype/shape, and calls the C entry point of the same name
+(``include/pa.h``) with raw device pointers and the current CUDA stream.  All
+computation runs in the library's CUDA kernels; there is no fallback path.
+Importing this package fails loudly if libpa.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpa.so")
+
+__all__ = [
+    "PAError", "lib_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
+    "pa_decode_splitk_workspace_size", "pa_validate_tables", "pa_validate_slots",
+    "pa_device_errors", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
+    "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
+]
+
+PA_OK = 0
+DEVERR_BLOCK_ID = 0x1
+DEVERR_SEQ_LEN = 0x2
+DEVERR_SLOT = 0x4
+DEVERR_TIMEOUT = 0x8
+
+_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libpa.so not found at {_LIB_PATH}; build it first with "
+        "`python paged_kv_cache_136_gb300/build.py` (nvcc, sm_103a)")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+_P, _I, _I64, _F, _SZ, _U = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t, ctypes.c_uint)
+_lib.pa_reshape_and_cache.restype = _I
+_lib.pa_reshape_and_cache.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I64, _I, _P]
+_lib.pa_decode.restype = _I
+_lib.pa_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]
+_lib.pa_decode_splitk_workspace_size.restype = _SZ
+_lib.pa_decode_splitk_workspace_size.argtypes = [_I, _I, _I, _I, _I]
+_lib.pa_decode_splitk.restype = _I
+_lib.pa_decode_splitk.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                  _I, _I, _P, _SZ, _P]
+_lib.pa_validate_tables.restype = _I
+_lib.pa_validate_tables.argtypes = [_P, _P, _I, _I, _I, _I]
+_lib.pa_validate_slots.restype = _I
+_lib.pa_validate_slots.argtypes = [_P, _I, _I, _I]
+_lib.pa_device_errors.restype = _I
+_lib.pa_device_errors.argtypes = [ctypes.POINTER(_U), _I]
+_lib.pa_status_string.restype = ctypes.c_char_p
+_lib.pa_status_string.argtypes = [_I]
+_lib.pa_version.restype = _I
+_lib.pa_version.argtypes = []
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {pa_status_string(status)} ({status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def pa_status_string(status: int) -> str:
+    return _lib.pa_status_string(status).decode()
+
+
+def pa_version() -> int:
+    return _lib.pa_version()
+
+
+def _check(status: int, where: str):
+    if status != PA_OK:
+        raise PAError(status, where)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _pool_dims(kv_cache: torch.Tensor, block_size: int):
+    if kv_cache.dim() != 5 or kv_cache.shape[0] != 2 or kv_cache.shape[2] != block_size:
+        raise ValueError("kv_cache must be [2, num_blocks, block_size, num_kv_heads, head_size]")
+    if not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be contiguous")
+    _, nb, _, hkv, d = kv_cache.shape
+    return int(nb), int(hkv), int(d)
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, kv_cache: torch.Tensor,
+                         slot_mapping: torch.Tensor, block_size: int, stream=None) -> None:
+    """Scatter new tokens' K/V ([T, Hkv, D], rows may be strided) into the pool
+    at slot_mapping (int64, negative = padding)."""
+    nb, hkv, d = _pool_dims(kv_cache, block_size)
+    T = int(key.shape[0])
+    for name, t in (("key", key), ("value", value)):
+        if t.dtype != kv_cache.dtype or t.shape[0] != T:
+            raise ValueError(f"{name} must match kv_cache dtype and token count")
+        if t.dim() != 3 or t.shape[1] != hkv or t.shape[2] != d or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, num_kv_heads, head_size] with contiguous rows")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64 [T]")
+    if kv_cache.dtype not in _DTYPE:
+        raise ValueError("dtype must be float16 or bfloat16")
+    if T == 0:
+        return
+    _check(_lib.pa_reshape_and_cache(_dev(key, "key"), _dev(value, "value"),
+                                     _dev(kv_cache, "kv_cache"), _dev(slot_mapping, "slot_mapping"),
+                                     T, hkv, d, block_size, nb, key.stride(0), value.stride(0),
+                                     _DTYPE[kv_cache.dtype], _stream(stream)),
+           "pa_reshape_and_cache")
+
+
+def _decode_common(out, q, kv_cache, block_tables, seq_lens, block_size):
+    nb, hkv, d = _pool_dims(kv_cache, block_size)
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, H, head_size]")
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be contiguous and match q")
+    if q.dtype != kv_cache.dtype or q.dtype not in _DTYPE:
+        raise ValueError("q, kv_cache and out must share dtype float16 or bfloat16")
+    B, H = int(q.shape[0]), int(q.shape[1])
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != B \
+            or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be contiguous int32 [B, max_blocks_per_seq]")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != B or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be contiguous int32 [B]")
+    return B, H, hkv, d, nb, int(block_tables.shape[1])
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+              block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+              block_size: int, stream=None) -> torch.Tensor:
+    """One-pass paged decode attention; writes and returns ``out``."""
+    B, H, hkv, d, nb, mb = _decode_common(out, q, kv_cache, block_tables, seq_lens, block_size)
+    _check(_lib.pa_decode(_dev(out, "out"), _dev(q, "q"), _dev(kv_cache, "kv_cache"),
+                          _dev(block_tables, "block_tables"), _dev(seq_lens, "seq_lens"),
+                          B, H, hkv, d, block_size, nb, mb, float(scale), _DTYPE[q.dtype],
+                          _stream(stream)), "pa_decode")
+    return out
+
+
+def pa_decode_splitk_workspace_size(num_seqs: int, num_heads: int, head_size: int,
+                                    max_seq_len: int, partition_size: int = 512) -> int:
+    return int(_lib.pa_decode_splitk_workspace_size(num_seqs, num_heads, head_size,
+                                                    max_seq_len, partition_size))
+
+
+def pa_decode_splitk(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                     block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     block_size: int, max_seq_len: int, workspace: torch.Tensor,
+                     partition_size: int = 512, stream=None) -> torch.Tensor:
+    """Partitioned paged decode attention with log-sum-exp reduce; ``workspace``
+    is a CUDA byte tensor of at least pa_decode_splitk_workspace_size bytes."""
+    B, H, hkv, d, nb, mb = _decode_common(out, q, kv_cache, block_tables, seq_lens, block_size)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_splitk(_dev(out, "out"), _dev(q, "q"), _dev(kv_cache, "kv_cache"),
+                                 _dev(block_tables, "block_tables"), _dev(seq_lens, "seq_lens"),
+                                 B, H, hkv, d, block_size, nb, mb, float(scale), _DTYPE[q.dtype],
+                                 int(max_seq_len), int(partition_size),
+                                 _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
+           "pa_decode_splitk")
+    return out
+
+
+def pa_validate_tables(block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int,
+                       num_blocks: int) -> int:
+    """Host check of the decode preconditions on CPU copies; returns a status."""
+    bt = block_tables.detach().to("cpu", torch.int32).contiguous()
+    sl = seq_lens.detach().to("cpu", torch.int32).contiguous()
+    return _lib.pa_validate_tables(ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(sl.data_ptr()),
+                                   int(sl.numel()), int(bt.shape[1]), block_size, num_blocks)
+
+
+def pa_validate_slots(slot_mapping: torch.Tensor, block_size: int, num_blocks: int) -> int:
+    sm = slot_mapping.detach().to("cpu", torch.int64).contiguous()
+    return _lib.pa_validate_slots(ctypes.c_void_p(sm.data_ptr()), int(sm.numel()), block_size,
+                                  num_blocks)
+
+
+def pa_device_errors(clear: bool = True) -> int:
+    """Sticky device error bits (DEVERR_*) of the current device; synchronises."""
+    flags = ctypes.c_uint(0)
+    _check(_lib.pa_device_errors(ctypes.byref(flags), 1 if clear else 0), "pa_device_errors")
+    return int(flags.value)

@@ -1,0 +1,87 @@
+"""Build libpa.so in-tree with nvcc for sm_103a.
+
+The library is a handful of translation units compiled in parallel (the decode
+kernel instantiations are split by dtype and head_size) and linked into
+``paged_kv_cache_136_gb300/_lib/libpa.so``.  Run ``python
+paged_kv_cache_136_gb300/build.py`` or call :func:`build`.
+"""
+from __future__ import annotations
+
+import concurrent.futures
+import glob
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OBJ_DIR = os.path.join(HERE, "_build")
+LIB_DIR = os.path.join(HERE, "_lib")
+LIB = os.path.join(LIB_DIR, "libpa.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
+              "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
+
+UNITS = [
+    ("pa_api", "pa_api.cu", []),
+    ("pa_decode_f16_d64", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=0", "-DPA_INST_D=64"]),
+    ("pa_decode_f16_d128", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=0", "-DPA_INST_D=128"]),
+    ("pa_decode_bf16_d64", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=1", "-DPA_INST_D=64"]),
+    ("pa_decode_bf16_d128", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=1", "-DPA_INST_D=128"]),
+]
+
+
+def _nvcc() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def _sources() -> list[str]:
+    return (glob.glob(os.path.join(CSRC, "*")) + [os.path.join(INCLUDE, "pa.h"),
+                                                  os.path.abspath(__file__)])
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    return any(os.path.getmtime(s) > t for s in _sources())
+
+
+def _compile(unit, verbose: bool):
+    name, src, defs = unit
+    obj = os.path.join(OBJ_DIR, name + ".o")
+    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {name}:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    return obj, r.stderr
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link libpa.so if any source changed; return its path."""
+    if not force and not _stale():
+        return LIB
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    os.makedirs(LIB_DIR, exist_ok=True)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+        results = list(ex.map(lambda u: _compile(u, verbose), UNITS))
+    if verbose:
+        for _, log in results:
+            sys.stderr.write(log)
+    tmp = LIB + f".{os.getpid()}.tmp"
+    cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,429 @@
+// pa_api.cu -- the C ABI of libpa.so (declared in include/pa.h): host-side
+// argument checks, TMA tensor-map encoding, the cache-write kernel, the split-K
+// reduce launcher and the device error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+#include <unordered_set>
+#include <vector>
+
+#include "pa.h"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// Sticky per-device error word (PA_DEVERR_* bits).  Kernels receive its
+// device address as a parameter.
+__device__ unsigned int g_device_errors = 0;
+
+static unsigned int *device_error_word(cudaError_t *err)
+{
+    static unsigned int *addr[64] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev & 63]) {
+        void *p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_device_errors);
+        if (*err != cudaSuccess)
+            return nullptr;
+        addr[dev & 63] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev & 63];
+}
+
+// ---------------------------------------------------------------------------
+// TMA tensor map over the pool [2, NB, BS, Hkv, D], seen as 4-D
+// {D, Hkv, NB*BS, 2} (innermost first).  A box is 64 elements (128 bytes) of
+// one kv head for BS consecutive rows of one plane, loaded with the 128-byte
+// swizzle.  Rows at or past NB*BS are out of bounds and read as zeros.
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    static cudaError_t init_err = cudaSuccess;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        init_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                    cudaEnableDefault, &q);
+        if (init_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            init_err = cudaErrorNotSupported;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    *err = init_err;
+    return fn;
+}
+
+static bool make_pool_map(CUtensorMap *map, const void *cache, int dtype, int num_blocks,
+                          int block_size, int num_kv_heads, int head_size)
+{
+    cudaError_t err;
+    auto fn = encode_fn(&err);
+    if (!fn)
+        return false;
+    const cuuint64_t es = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads,
+                          (cuuint64_t)num_blocks * block_size, 2};
+    cuuint64_t strides[3] = {head_size * es, (cuuint64_t)num_kv_heads * head_size * es,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * head_size * es};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)block_size, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    4, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_decode(const DecodeKey &key, const CUtensorMap &tmap, const DecodeParams &p,
+                          dim3 grid, cudaStream_t stream)
+{
+    if (key.dtype == PA_FP16 && key.head_size == 64)
+        return launch_decode_f16_d64(key, tmap, p, grid, stream);
+    if (key.dtype == PA_FP16 && key.head_size == 128)
+        return launch_decode_f16_d128(key, tmap, p, grid, stream);
+    if (key.dtype == PA_BF16 && key.head_size == 64)
+        return launch_decode_bf16_d64(key, tmap, p, grid, stream);
+    if (key.dtype == PA_BF16 && key.head_size == 128)
+        return launch_decode_bf16_d128(key, tmap, p, grid, stream);
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int num_seqs,
+                          cudaStream_t stream)
+{
+    dim3 grid(p.num_heads, num_seqs);
+    if (dtype == PA_FP16 && head_size == 64)
+        splitk_reduce_kernel<__half, 64><<<grid, 64, 0, stream>>>(p);
+    else if (dtype == PA_FP16 && head_size == 128)
+        splitk_reduce_kernel<__half, 128><<<grid, 128, 0, stream>>>(p);
+    else if (dtype == PA_BF16 && head_size == 64)
+        splitk_reduce_kernel<__nv_bfloat16, 64><<<grid, 64, 0, stream>>>(p);
+    else if (dtype == PA_BF16 && head_size == 128)
+        splitk_reduce_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(p);
+    else
+        return cudaErrorNotSupported;
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Cache write ("PagedAttention 在 vLLM 中的实现分析", sections 3.2 and 7.4).
+// In the NHD pool the row of (block, offset) is block*block_size + offset,
+// which is the slot itself, so each token's [Hkv, D] row is copied to row
+// `slot` of the key plane and of the value plane with 16-byte moves.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                             uint4 *__restrict__ cache, const int64_t *__restrict__ slots,
+                             int num_tokens, int row_vecs, int64_t key_stride_vecs,
+                             int64_t value_stride_vecs, int64_t num_slots, unsigned int *err)
+{
+    const int tok = blockIdx.y;
+    const int64_t slot = slots[tok];
+    if (slot < 0)
+        return; // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            atomicOr(err, PA_DEVERR_SLOT);
+        return;
+    }
+    const int64_t plane = num_slots * row_vecs;
+    for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < row_vecs; w += gridDim.x * blockDim.x) {
+        const uint4 k = key[tok * key_stride_vecs + w];
+        const uint4 v = value[tok * value_stride_vecs + w];
+        cache[slot * row_vecs + w] = k;
+        cache[plane + slot * row_vecs + w] = v;
+    }
+}
+
+} // namespace pa
+
+using namespace pa;
+
+// ---------------------------------------------------------------------------
+// Host-side checks
+// ---------------------------------------------------------------------------
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+static bool supported_shape(int head_size, int block_size, int group, int dtype)
+{
+    return (head_size == 64 || head_size == 128) && (block_size == 16 || block_size == 32) &&
+           (group == 1 || group == 2 || group == 4 || group == 8) &&
+           (dtype == PA_FP16 || dtype == PA_BF16);
+}
+
+static pa_status check_decode_args(const void *out, const void *q, const void *kv_cache,
+                                   const int32_t *block_tables, const int32_t *seq_lens,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                   int block_size, int num_blocks, int max_blocks_per_seq,
+                                   float scale, pa_dtype dtype)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || !isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!out || !q || !kv_cache || !block_tables || !seq_lens))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!supported_shape(head_size, block_size, num_heads / num_kv_heads, (int)dtype))
+        return PA_ERR_UNSUPPORTED;
+    // TMA row coordinates and kernel token counters are 32-bit.
+    if ((int64_t)num_blocks * block_size >= (int64_t)INT32_MAX ||
+        (int64_t)max_blocks_per_seq * block_size >= (int64_t)INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    if (num_kv_heads > 65535 || num_seqs > 65535)
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+static const float kLog2e = 1.4426950408889634f;
+
+extern "C" {
+
+int pa_version(void) { return 10000; }
+
+const char *pa_status_string(pa_status status)
+{
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+pa_status pa_reshape_and_cache(const void *key, const void *value, void *kv_cache,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_size, int block_size, int num_blocks,
+                               int64_t key_stride, int64_t value_stride, pa_dtype dtype,
+                               void *stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_FP16 && dtype != PA_BF16)
+        return PA_ERR_UNSUPPORTED;
+    const int64_t row = (int64_t)num_kv_heads * head_size;
+    if (key_stride < row || value_stride < row || key_stride % 8 || value_stride % 8 || row % 8)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!key || !value || !kv_cache || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > 65535 || row / 8 > INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    const int row_vecs = (int)(row / 8);
+    const int threads = 256;
+    int bx = (row_vecs + threads - 1) / threads;
+    dim3 grid(bx, num_tokens);
+    reshape_and_cache_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(kv_cache), slot_mapping, num_tokens, row_vecs, key_stride / 8,
+        value_stride / 8, (int64_t)num_blocks * block_size, err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_t *block_tables,
+                    const int32_t *seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                    int head_size, int block_size, int num_blocks, int max_blocks_per_seq,
+                    float scale, pa_dtype dtype, void *stream)
+{
+    pa_status st = check_decode_args(out, q, kv_cache, block_tables, seq_lens, num_seqs,
+                                     num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                                     max_blocks_per_seq, scale, dtype);
+    if (st != PA_OK || num_seqs == 0)
+        return st;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    alignas(64) CUtensorMap tmap;
+    if (!make_pool_map(&tmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads, head_size))
+        return PA_ERR_CUDA;
+    DecodeParams p = {};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.err = err;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.part_tokens = 0;
+    p.max_parts = 1;
+    p.len_cap = max_blocks_per_seq * block_size;
+    p.qscale = scale * kLog2e;
+    DecodeKey key = {(int)dtype, head_size, block_size, num_heads / num_kv_heads, false};
+    e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, 1),
+                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
+}
+
+static size_t splitk_parts(int max_seq_len, int partition_size)
+{
+    size_t parts = ((size_t)max_seq_len + partition_size - 1) / partition_size;
+    return parts ? parts : 1;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t pa_decode_splitk_workspace_size(int num_seqs, int num_heads, int head_size,
+                                       int max_seq_len, int partition_size)
+{
+    if (num_seqs < 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 ||
+        partition_size <= 0)
+        return 0;
+    const size_t rows = (size_t)num_seqs * num_heads * splitk_parts(max_seq_len, partition_size);
+    return round_up(rows * head_size * sizeof(float), 256) + round_up(rows * 2 * sizeof(float), 256);
+}
+
+pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int num_heads, int num_kv_heads, int head_size, int block_size,
+                           int num_blocks, int max_blocks_per_seq, float scale, pa_dtype dtype,
+                           int max_seq_len, int partition_size, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    pa_status st = check_decode_args(out, q, kv_cache, block_tables, seq_lens, num_seqs,
+                                     num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                                     max_blocks_per_seq, scale, dtype);
+    if (st != PA_OK)
+        return st;
+    if (max_seq_len < 0 || partition_size <= 0 || partition_size % kTok != 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PA_OK;
+    const size_t parts = splitk_parts(max_seq_len, partition_size);
+    if (parts > 65535)
+        return PA_ERR_UNSUPPORTED;
+    const size_t need = pa_decode_splitk_workspace_size(num_seqs, num_heads, head_size,
+                                                        max_seq_len, partition_size);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return PA_ERR_WORKSPACE;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    alignas(64) CUtensorMap tmap;
+    if (!make_pool_map(&tmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads, head_size))
+        return PA_ERR_CUDA;
+    const size_t rows = (size_t)num_seqs * num_heads * parts;
+    float *ws_o = static_cast<float *>(workspace);
+    float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             round_up(rows * head_size * sizeof(float), 256));
+    const int64_t cap_tab = (int64_t)max_blocks_per_seq * block_size;
+    const int64_t cap_ws = (int64_t)parts * partition_size;
+    const int len_cap = (int)(cap_tab < cap_ws ? cap_tab : cap_ws);
+
+    DecodeParams p = {};
+    p.ws_o = ws_o;
+    p.ws_ml = ws_ml;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.err = err;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.part_tokens = partition_size;
+    p.max_parts = (int)parts;
+    p.len_cap = len_cap;
+    p.qscale = scale * kLog2e;
+    DecodeKey key = {(int)dtype, head_size, block_size, num_heads / num_kv_heads, true};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
+    if (e != cudaSuccess)
+        return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
+    ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size, len_cap};
+    e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,
+                             int num_seqs, int max_blocks_per_seq, int block_size,
+                             int num_blocks)
+{
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!block_tables || !seq_lens))
+        return PA_ERR_INVALID_ARG;
+    const int64_t cap = (int64_t)max_blocks_per_seq * block_size;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int64_t L = seq_lens[s];
+        if (L < 0 || L > cap)
+            return PA_ERR_OUT_OF_RANGE;
+        const int64_t nb = (L + block_size - 1) / block_size;
+        const int32_t *row = block_tables + (size_t)s * max_blocks_per_seq;
+        for (int64_t j = 0; j < nb; ++j)
+            if (row[j] < 0 || row[j] >= num_blocks)
+                return PA_ERR_OUT_OF_RANGE;
+    }
+    return PA_OK;
+}
+
+pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int block_size,
+                            int num_blocks)
+{
+    if (num_tokens < 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > 0 && !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    const int64_t cap = (int64_t)num_blocks * block_size;
+    std::unordered_set<int64_t> seen;
+    seen.reserve((size_t)num_tokens * 2);
+    for (int i = 0; i < num_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue;
+        if (s >= cap || !seen.insert(s).second)
+            return PA_ERR_OUT_OF_RANGE;
+    }
+    return PA_OK;
+}
+
+pa_status pa_device_errors(unsigned int *flags, int clear)
+{
+    if (!flags)
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e;
+    unsigned int *word = device_error_word(&e);
+    if (!word)
+        return PA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaMemcpy(flags, word, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (clear && cudaMemset(word, 0, sizeof(unsigned int)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (clear && cudaDeviceSynchronize() != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+} // extern "C"

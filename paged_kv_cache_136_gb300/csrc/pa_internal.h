@@ -1,0 +1,69 @@
+// pa_internal.h -- declarations shared by the library's translation units
+// (kernel parameter blocks and the per-instantiation launchers).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Kernel parameters of the decode kernels (one-pass and split-K partition).
+struct DecodeParams {
+    void *out;                   // [B, H, D] (one-pass)
+    float *ws_o;                 // [B, H, max_parts, D] unnormalised partial outputs
+    float *ws_ml;                // [B, H, max_parts, 2] running max (log2 units), normaliser
+    const void *q;               // [B, H, D]
+    const int32_t *block_tables; // [B, max_blocks]
+    const int32_t *seq_lens;     // [B]
+    unsigned int *err;           // sticky device error word
+    int num_heads;
+    int num_kv_heads;
+    int num_blocks;
+    int max_blocks;
+    int part_tokens;             // split-K: tokens per partition
+    int max_parts;               // split-K: partitions reserved per (seq, head)
+    int len_cap;                 // largest seq_len the tables (and workspace) allow
+    float qscale;                // scale * log2(e)
+};
+
+// Parameters of the split-K log-sum-exp reduce.
+struct ReduceParams {
+    void *out;
+    const float *ws_o;
+    const float *ws_ml;
+    const int32_t *seq_lens;
+    int num_heads;
+    int max_parts;
+    int part_tokens;
+    int len_cap;
+};
+
+// Key of a decode kernel instantiation.
+struct DecodeKey {
+    int dtype;      // 0 fp16, 1 bf16
+    int head_size;  // 64, 128
+    int block_size; // 16, 32
+    int group;      // 1, 2, 4, 8
+    bool split;
+};
+
+// Launch the decode kernel matching `key` on grid (Hkv, B, parts).  Returns
+// cudaErrorNotSupported if no instantiation matches.
+cudaError_t launch_decode(const DecodeKey &key, const CUtensorMap &tmap, const DecodeParams &p,
+                          dim3 grid, cudaStream_t stream);
+
+cudaError_t launch_decode_f16_d64(const DecodeKey &, const CUtensorMap &, const DecodeParams &,
+                                  dim3, cudaStream_t);
+cudaError_t launch_decode_f16_d128(const DecodeKey &, const CUtensorMap &, const DecodeParams &,
+                                   dim3, cudaStream_t);
+cudaError_t launch_decode_bf16_d64(const DecodeKey &, const CUtensorMap &, const DecodeParams &,
+                                   dim3, cudaStream_t);
+cudaError_t launch_decode_bf16_d128(const DecodeKey &, const CUtensorMap &, const DecodeParams &,
+                                    dim3, cudaStream_t);
+
+// Launch the split-K reduce on grid (H, B).
+cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int num_seqs,
+                          cudaStream_t stream);
+
+} // namespace pa

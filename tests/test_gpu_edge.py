@@ -1,0 +1,147 @@
+"""Edge cases of the CUDA path: empty sequences, guard bands, device-side
+range guards, streams, partition-size invariance, determinism and batch
+invariance.  Bad ids/lengths/slots below are ones the kernels' own bounds
+checks turn into an error bit without dereferencing them."""
+import numpy as np
+import pytest
+import torch
+
+import workload as wl
+from tests._parity import check_attention, oracle_decode, splitk_workspace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from __graft_entry__ import build_library
+    build_library()
+    import paged_kv_cache_136_gb300 as pa
+    pa.pa_device_errors(clear=True)
+    return pa
+
+
+def _decode(pa, w, split, partition_size=512, max_seq_len=None, out=None, stream=None):
+    out = torch.empty_like(w.q) if out is None else out
+    if split:
+        msl = int(w.seq_lens.max().item()) if max_seq_len is None else max_seq_len
+        ws = splitk_workspace(pa, w, msl, partition_size)
+        pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                            w.block_size, msl, ws, partition_size, stream=stream)
+    else:
+        pa.pa_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale, w.block_size,
+                     stream=stream)
+    return out
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_empty_sequences_give_zero_rows(pa, split):
+    w = wl.make("gqa8b", device="cuda", poison=True, lengths=[0, 5, 0, 130], seed=3)
+    out = _decode(pa, w, split, partition_size=64)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
+    check_attention(out, oracle_decode(w), what="empty rows")
+    assert pa.pa_device_errors() == 0
+
+
+def test_all_sequences_empty_split(pa):
+    w = wl.make("tiny", device="cuda", lengths=[0, 0], seed=4)
+    out = _decode(pa, w, True, partition_size=64, max_seq_len=0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_output_guard_bands_untouched(pa, split):
+    w = wl.make("tiny", device="cuda", poison=True)
+    n = w.q.numel()
+    buf = torch.full((n + 2048,), 7.0, dtype=w.dtype, device="cuda")
+    out = buf[1024:1024 + n].view_as(w.q)
+    _decode(pa, w, split, partition_size=64, out=out)
+    torch.cuda.synchronize()
+    assert bool((buf[:1024] == 7.0).all()) and bool((buf[1024 + n:] == 7.0).all())
+    check_attention(out, oracle_decode(w), what="guarded out")
+
+
+def test_bad_block_id_sets_flag_and_is_not_read(pa):
+    w = wl.make("tiny", device="cuda", seed=5)
+    bt = w.block_tables.clone()
+    bt[3, 2] = w.num_blocks + 5          # seq 3 (64 tokens) uses blocks 0..3
+    bt[1, 0] = -7
+    out = torch.empty_like(w.q)
+    pa.pa_decode(out, w.q, w.kv_cache, bt, w.seq_lens, w.scale, w.block_size)
+    flags = pa.pa_device_errors(clear=True)
+    assert flags & pa.DEVERR_BLOCK_ID
+    # Rows that use only valid ids are still right.
+    ref = oracle_decode(w)
+    check_attention(out[[0, 2]], ref[[0, 2]], what="valid rows next to bad ids")
+
+
+def test_seq_len_beyond_table_is_clamped_and_flagged(pa):
+    w = wl.make("tiny", device="cuda", seed=6)
+    sl = w.seq_lens.clone()
+    sl[0] = w.block_tables.shape[1] * w.block_size + 100
+    sl[1] = -3
+    out = torch.empty_like(w.q)
+    pa.pa_decode(out, w.q, w.kv_cache, w.block_tables, sl, w.scale, w.block_size)
+    assert pa.pa_device_errors(clear=True) & pa.DEVERR_SEQ_LEN
+    assert torch.count_nonzero(out[1]) == 0
+
+
+def test_seq_len_beyond_max_seq_len_is_flagged(pa):
+    w = wl.make("gqa8b", device="cuda", lengths=[300, 700], seed=7)
+    out = _decode(pa, w, True, partition_size=128, max_seq_len=256)
+    assert pa.pa_device_errors(clear=True) & pa.DEVERR_SEQ_LEN
+    assert torch.isfinite(out).all()
+
+
+def test_out_of_range_slot_writes_nothing_and_is_flagged(pa):
+    w = wl.make("tiny", device="cuda", seed=8)
+    before = w.kv_cache.clone()
+    sm = torch.full_like(w.slot_mapping, -1)
+    sm[0] = w.num_blocks * w.block_size          # one past the pool
+    pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, sm, w.block_size)
+    assert pa.pa_device_errors(clear=True) & pa.DEVERR_SLOT
+    assert torch.equal(w.kv_cache.view(torch.int16), before.view(torch.int16))
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_runs_on_a_side_stream(pa, split):
+    w = wl.make("gqa8b", device="cuda", poison=True, num_seqs=16, seed=9)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = _decode(pa, w, split, partition_size=256, stream=s)
+    s.synchronize()
+    check_attention(out, oracle_decode(w), what="side stream")
+
+
+def test_partition_size_invariance(pa):
+    w = wl.make("gqa8b", device="cuda", poison=True, lengths=[1, 700, 1500, 4096, 64, 65],
+                seed=10)
+    ref = oracle_decode(w)
+    one = _decode(pa, w, False)
+    check_attention(one, ref, what="one-pass")
+    for P in (64, 128, 192, 512, 1024, 4096):
+        out = _decode(pa, w, True, partition_size=P)
+        check_attention(out, ref, what=f"partition {P}")
+        diff = (out.float() - one.float()).abs().max().item()
+        assert diff <= 2e-2, (P, diff)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_deterministic_and_batch_invariant(pa, split):
+    """Same inputs give identical bits; a sequence's output does not depend on
+    which other sequences share the batch."""
+    w = wl.make("gqa8b", device="cuda", num_seqs=32, seed=11)
+    a = _decode(pa, w, split)
+    b = _decode(pa, w, split)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    sub = [3, 17, 30]
+    ws = wl.Workload(**{k: getattr(w, k) for k in w.__dataclass_fields__})
+    ws.q = w.q[sub].contiguous()
+    ws.block_tables = w.block_tables[sub].contiguous()
+    ws.seq_lens = w.seq_lens[sub].contiguous()
+    c = _decode(pa, ws, split, max_seq_len=int(w.seq_lens.max().item()))
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16), a[sub].view(torch.int16))

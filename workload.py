@@ -188,7 +188,7 @@ def make(name: str, seed: int | None = None, device="cpu", poison: bool = False,
     if name == "tiny" and lengths is None:
         NB = 32
     else:
-        NB = max(need, int(math.ceil(spec.pool_factor * need)))
+        NB = max(1, need, int(math.ceil(spec.pool_factor * need)))
 
     perm = rng.permutation(NB).astype(np.int32)
     tables = np.full((B, MB), -1, dtype=np.int32)
