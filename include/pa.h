@@ -149,6 +149,34 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode_splitk without a caller-provided workspace, for callers that
+ * cannot allocate device memory (for example code hosted inside a framework
+ * that owns all device memory and gives it no allocator, or a latency-critical
+ * loop where an allocation, which may synchronise the device, is not
+ * allowed).  The pages have no counterpart of this entry point.
+ *
+ * Arguments and result are those of pa_decode_splitk.  Its scratch is a fixed
+ * array of PA_NOALLOC_SCRATCH_BYTES inside the library; the call allocates
+ * nothing.  Sizes whose pa_decode_splitk_workspace_size exceeds that return
+ * PA_ERR_WORKSPACE before any launch.
+ *   - The array occupies PA_NOALLOC_SCRATCH_BYTES of device memory on every
+ *     GPU where the library's module is loaded, until the process exits.
+ *   - The first call on a device looks up the array's device address and
+ *     caches it; make that first call before any stream capture.
+ *   - All calls on one device share the array.  Calls that overlap on the GPU
+ *     race; order them (one stream, or events).  Nothing in the array needs
+ *     to start at zero.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pa_status pa_decode_splitk_noalloc(void *out, const void *q, const void *kv_cache,
+                                   const int32_t *block_tables, const int32_t *seq_lens,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                   int block_size, int num_blocks, int max_blocks_per_seq,
+                                   float scale, pa_dtype dtype, int max_seq_len,
+                                   int partition_size, void *stream);
+
+/*
  * Host-side check of the decode preconditions on HOST copies of the tables:
  * 0 <= seq_lens[s] <= max_blocks_per_seq*block_size and every block id a
  * sequence uses (entries j < ceil(seq_lens[s]/block_size)) in [0, num_blocks).

@@ -17,7 +17,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 __all__ = [
     "PAError", "lib_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
-    "pa_decode_splitk_workspace_size", "pa_validate_tables", "pa_validate_slots",
+    "pa_decode_splitk_workspace_size", "pa_decode_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "pa_validate_tables", "pa_validate_slots",
     "pa_device_errors", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
@@ -47,6 +48,9 @@ _lib.pa_decode_splitk_workspace_size.argtypes = [_I, _I, _I, _I, _I]
 _lib.pa_decode_splitk.restype = _I
 _lib.pa_decode_splitk.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                   _I, _I, _P, _SZ, _P]
+_lib.pa_decode_splitk_noalloc.restype = _I
+_lib.pa_decode_splitk_noalloc.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                          _I, _I, _I, _P]
 _lib.pa_validate_tables.restype = _I
 _lib.pa_validate_tables.argtypes = [_P, _P, _I, _I, _I, _I]
 _lib.pa_validate_slots.restype = _I
@@ -178,6 +182,29 @@ def pa_decode_splitk(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
                                  int(max_seq_len), int(partition_size),
                                  _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
            "pa_decode_splitk")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20   # PA_NOALLOC_SCRATCH_BYTES in pa.h
+
+
+def pa_decode_splitk_noalloc(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                             block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             block_size: int, max_seq_len: int, partition_size: int = 512,
+                             stream=None) -> torch.Tensor:
+    """pa_decode_splitk for callers that cannot allocate device memory: the
+    partial states go to a fixed scratch array inside the library
+    (NOALLOC_SCRATCH_BYTES per device), so nothing is allocated per call.
+    Calls that overlap on the GPU share that array and must be ordered."""
+    B, H, hkv, d, nb, mb = _decode_common(out, q, kv_cache, block_tables, seq_lens, block_size)
+    _check(_lib.pa_decode_splitk_noalloc(_dev(out, "out"), _dev(q, "q"),
+                                         _dev(kv_cache, "kv_cache"),
+                                         _dev(block_tables, "block_tables"),
+                                         _dev(seq_lens, "seq_lens"), B, H, hkv, d, block_size,
+                                         nb, mb, float(scale), _DTYPE[q.dtype],
+                                         int(max_seq_len), int(partition_size),
+                                         _stream(stream)),
+           "pa_decode_splitk_noalloc")
     return out
 
 

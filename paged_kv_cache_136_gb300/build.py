@@ -27,6 +27,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
 
 UNITS = [
     ("pa_api", "pa_api.cu", []),
+    ("pa_noalloc", "pa_noalloc.cu", []),
     ("pa_decode_f16_d64", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=0", "-DPA_INST_D=64"]),
     ("pa_decode_f16_d128", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=0", "-DPA_INST_D=128"]),
     ("pa_decode_bf16_d64", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=1", "-DPA_INST_D=64"]),
