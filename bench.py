@@ -322,7 +322,7 @@ def run_ours(args) -> dict | None:
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
-    e2e_steps = max(1, min(K, 200))
+    e2e_steps = max(1, min(K, args.e2e_steps))
 
     def e2e_step():
         for k, t in host.items():
@@ -437,6 +437,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200,
+                    help="steps in the end-to-end (host buffers) measurement")
     return ap.parse_args(argv)
 
 

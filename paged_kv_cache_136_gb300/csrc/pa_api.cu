@@ -12,8 +12,11 @@
 #include <unordered_set>
 #include <vector>
 
+#include <stdlib.h>
+
 #include "pa.h"
 #include "pa_decode.cuh"
+#include "pa_decode_tc.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -84,6 +87,70 @@ static bool make_pool_map(CUtensorMap *map, const void *cache, int dtype, int nu
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Query rows as a 2-D tensor {D, B*H}; a box is 64 elements of G consecutive
+// query heads (one kv head's group), loaded with the 128-byte swizzle.
+static bool make_q_map(CUtensorMap *map, const void *q, int dtype, int rows, int head_size,
+                       int group)
+{
+    cudaError_t err;
+    auto fn = encode_fn(&err);
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_size * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)group};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, const_cast<void *>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int sm_count(cudaError_t *err)
+{
+    static int count[64] = {0};
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess)
+        return 0;
+    if (!count[dev & 63]) {
+        int c = 0;
+        *err = cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+        if (*err != cudaSuccess)
+            return 0;
+        count[dev & 63] = c;
+    }
+    return count[dev & 63];
+}
+
+// Decode kernel family: PA_DECODE_KERNEL=simt or =tcgen05 forces one
+// (head_size 128 only for tcgen05); unset or anything else picks per shape.
+enum { kKernelAuto = 0, kKernelSimt = 1, kKernelTc = 2 };
+static int kernel_choice()
+{
+    static int choice = -1;
+    if (choice < 0) {
+        const char *v = getenv("PA_DECODE_KERNEL");
+        choice = (v && !strcmp(v, "simt")) ? kKernelSimt
+                 : (v && !strcmp(v, "tcgen05")) ? kKernelTc
+                                                : kKernelAuto;
+    }
+    return choice;
+}
+
+static bool use_tc(int head_size, int group, bool split)
+{
+    if (head_size != 128)
+        return false;
+    const int c = kernel_choice();
+    if (c == kKernelSimt)
+        return false;
+    if (c == kKernelTc)
+        return true;
+    return split || group >= 2;
 }
 
 cudaError_t launch_decode(const DecodeKey &key, const CUtensorMap &tmap, const DecodeParams &p,
@@ -185,7 +252,7 @@ static pa_status check_decode_args(const void *out, const void *q, const void *k
     if ((int64_t)num_blocks * block_size >= (int64_t)INT32_MAX ||
         (int64_t)max_blocks_per_seq * block_size >= (int64_t)INT32_MAX)
         return PA_ERR_UNSUPPORTED;
-    if (num_kv_heads > 65535 || num_seqs > 65535)
+    if (num_kv_heads > 65535 || num_seqs > 65535 || (int64_t)num_seqs * num_heads > INT32_MAX)
         return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
@@ -264,6 +331,29 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_
     alignas(64) CUtensorMap tmap;
     if (!make_pool_map(&tmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads, head_size))
         return PA_ERR_CUDA;
+    const int group = num_heads / num_kv_heads;
+    if (use_tc(head_size, group, false)) {
+        alignas(64) CUtensorMap qmap;
+        if (!make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, group))
+            return PA_ERR_CUDA;
+        tc::TcParams t = {};
+        t.out = out;
+        t.block_tables = block_tables;
+        t.seq_lens = seq_lens;
+        t.err = err;
+        t.num_heads = num_heads;
+        t.num_kv_heads = num_kv_heads;
+        t.num_blocks = num_blocks;
+        t.max_blocks = max_blocks_per_seq;
+        t.part_tokens = max_blocks_per_seq * block_size;
+        t.max_parts = 1;
+        t.len_cap = max_blocks_per_seq * block_size;
+        t.qscale = scale * kLog2e;
+        auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
+        e = launch(block_size, group, false, tmap, qmap, t, dim3(num_kv_heads, num_seqs),
+                   static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
+    }
     DecodeParams p = {};
     p.out = out;
     p.q = q;
@@ -292,14 +382,33 @@ static size_t splitk_parts(int max_seq_len, int partition_size)
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Split-K workspace: [header 256 B: work counter, item count]
+// [arrival counters, one per (sequence, head)] [unit list, one per
+// (sequence, partition)] [partial o, fp32 D per row] [partial (m, l)],
+// each region 256-byte aligned; rows = B * H * partitions.
+struct WsLayout {
+    size_t arrive, units, o, ml, total;
+};
+
+static WsLayout ws_layout(int num_seqs, int num_heads, int head_size, size_t parts)
+{
+    WsLayout w;
+    const size_t rows = (size_t)num_seqs * num_heads * parts;
+    w.arrive = 256;
+    w.units = w.arrive + round_up((size_t)num_seqs * num_heads * 4, 256);
+    w.o = w.units + round_up((size_t)num_seqs * parts * 4, 256);
+    w.ml = w.o + round_up(rows * head_size * sizeof(float), 256);
+    w.total = w.ml + round_up(rows * 2 * sizeof(float), 256);
+    return w;
+}
+
 size_t pa_decode_splitk_workspace_size(int num_seqs, int num_heads, int head_size,
                                        int max_seq_len, int partition_size)
 {
     if (num_seqs < 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 ||
         partition_size <= 0)
         return 0;
-    const size_t rows = (size_t)num_seqs * num_heads * splitk_parts(max_seq_len, partition_size);
-    return round_up(rows * head_size * sizeof(float), 256) + round_up(rows * 2 * sizeof(float), 256);
+    return ws_layout(num_seqs, num_heads, head_size, splitk_parts(max_seq_len, partition_size)).total;
 }
 
 pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
@@ -332,13 +441,60 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
     alignas(64) CUtensorMap tmap;
     if (!make_pool_map(&tmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads, head_size))
         return PA_ERR_CUDA;
-    const size_t rows = (size_t)num_seqs * num_heads * parts;
-    float *ws_o = static_cast<float *>(workspace);
-    float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                             round_up(rows * head_size * sizeof(float), 256));
+    const WsLayout lay = ws_layout(num_seqs, num_heads, head_size, parts);
+    char *wsb = static_cast<char *>(workspace);
+    float *ws_o = reinterpret_cast<float *>(wsb + lay.o);
+    float *ws_ml = reinterpret_cast<float *>(wsb + lay.ml);
     const int64_t cap_tab = (int64_t)max_blocks_per_seq * block_size;
     const int64_t cap_ws = (int64_t)parts * partition_size;
     const int len_cap = (int)(cap_tab < cap_ws ? cap_tab : cap_ws);
+    const int group = num_heads / num_kv_heads;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (use_tc(head_size, group, true)) {
+        alignas(64) CUtensorMap qmap;
+        if (!make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, group))
+            return PA_ERR_CUDA;
+        uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
+        uint32_t *arrive = reinterpret_cast<uint32_t *>(wsb + lay.arrive);
+        uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
+        if (dtype == PA_BF16)
+            tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
+                seq_lens, num_seqs, num_heads, num_kv_heads, partition_size, len_cap, hdr, arrive,
+                units, static_cast<__nv_bfloat16 *>(out), err);
+        else
+            tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
+                seq_lens, num_seqs, num_heads, num_kv_heads, partition_size, len_cap, hdr, arrive,
+                units, static_cast<__half *>(out), err);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return PA_ERR_CUDA;
+        tc::TcParams t = {};
+        t.out = out;
+        t.block_tables = block_tables;
+        t.seq_lens = seq_lens;
+        t.err = err;
+        t.hdr = hdr;
+        t.arrive = arrive;
+        t.units = units;
+        t.ws_o = ws_o;
+        t.ws_ml = ws_ml;
+        t.num_heads = num_heads;
+        t.num_kv_heads = num_kv_heads;
+        t.num_blocks = num_blocks;
+        t.max_blocks = max_blocks_per_seq;
+        t.part_tokens = partition_size;
+        t.max_parts = (int)parts;
+        t.len_cap = len_cap;
+        t.qscale = scale * kLog2e;
+        const int sms = sm_count(&e);
+        if (!sms)
+            return PA_ERR_CUDA;
+        const size_t bound = (size_t)num_seqs * num_kv_heads * parts;
+        const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
+        auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
+        e = launch(block_size, group, true, tmap, qmap, t, dim3(grid), s);
+        return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
+    }
 
     DecodeParams p = {};
     p.ws_o = ws_o;
@@ -355,8 +511,7 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
     p.max_parts = (int)parts;
     p.len_cap = len_cap;
     p.qscale = scale * kLog2e;
-    DecodeKey key = {(int)dtype, head_size, block_size, num_heads / num_kv_heads, true};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DecodeKey key = {(int)dtype, head_size, block_size, group, true};
     e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
     if (e != cudaSuccess)
         return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     using Geo = Geometry<D>;
     constexpr int SB = kTok / BS; // physical blocks per stage
     static_assert(kTok % BS == 0 && 32 % SB == 0, "stage/block geometry");
+    static_assert(SB * 2 * Geometry<D>::kRegions <= 32, "one TMA box per producer lane");
     static_assert(D == 64 || D == 128, "head_size");
 
     const int kvh = blockIdx.x;
@@ -187,27 +188,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint8_t *stage = smem + slot * Geo::kStageBytes;
             if (lane == 0)
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)(nblk * BS * D * 2 * 2));
-#pragma unroll
-            for (int jj = 0; jj < SB; ++jj) {
-                const int phys = __shfl_sync(0xffffffffu, cur, (jf - cbase + jj) & 31);
-                if (jj < nblk && lane == 0) {
-                    int row;
-                    if (phys < 0 || phys >= p.num_blocks) {
-                        // Never dereference a bad id: a row past the tensor's
-                        // extent makes TMA fill the tile with zeros.
-                        atomicOr(p.err, PA_DEVERR_BLOCK_ID_);
-                        row = p.num_blocks * BS;
-                    } else {
-                        row = phys * BS;
-                    }
-#pragma unroll
-                    for (int plane = 0; plane < 2; ++plane)
-#pragma unroll
-                        for (int r = 0; r < Geo::kRegions; ++r)
-                            tma_load_4d_hint(stage + plane * Geo::kPlaneBytes + r * Geo::kRegionBytes +
-                                                 jj * BS * 128,
-                                             &tmap, &full[slot], r * 64, kvh, row, plane, policy);
+            __syncwarp();
+            // One TMA box per lane: box i covers block jj = i / (2*kRegions),
+            // plane, 64-element region.  Issuing from many lanes at once keeps
+            // the copy engine fed (one issuing thread cannot).
+            constexpr int kBoxesPerBlock = 2 * Geo::kRegions;
+            const int jj = lane / kBoxesPerBlock;
+            const int phys = __shfl_sync(0xffffffffu, cur, (jf - cbase + (jj < SB ? jj : 0)) & 31);
+            if (lane < nblk * kBoxesPerBlock) {
+                const int rem = lane % kBoxesPerBlock;
+                const int plane = rem / Geo::kRegions;
+                const int r = rem % Geo::kRegions;
+                int row;
+                if (phys < 0 || phys >= p.num_blocks) {
+                    // Never dereference a bad id: a row past the tensor's
+                    // extent makes TMA fill the tile with zeros.
+                    atomicOr(p.err, PA_DEVERR_BLOCK_ID_);
+                    row = p.num_blocks * BS;
+                } else {
+                    row = phys * BS;
                 }
+                tma_load_4d_hint(stage + plane * Geo::kPlaneBytes + r * Geo::kRegionBytes + jj * BS * 128,
+                                 &tmap, &full[slot], r * 64, kvh, row, plane, policy);
             }
         }
         return;

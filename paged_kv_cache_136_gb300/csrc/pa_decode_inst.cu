@@ -3,6 +3,9 @@
 // -DPA_INST_D (64, 128).  The build compiles this file once per pair so the
 // four units compile in parallel.
 #include "pa_decode.cuh"
+#if PA_INST_D == 128
+#include "pa_decode_tc.cuh"
+#endif
 
 #if !defined(PA_INST_DTYPE) || !defined(PA_INST_D)
 #error "compile with -DPA_INST_DTYPE=<0|1> -DPA_INST_D=<64|128>"
@@ -26,4 +29,14 @@ cudaError_t PA_LAUNCHER(const DecodeKey &key, const CUtensorMap &tmap, const Dec
 {
     return launch_by_group<InstT, PA_INST_D>(key, tmap, p, grid, stream);
 }
+
+#if PA_INST_D == 128
+#define PA_TC_LAUNCHER PA_CAT(launch_decode_tc_, PA_DT_NAME, )
+cudaError_t PA_TC_LAUNCHER(int block_size, int group, bool split, const CUtensorMap &pool,
+                           const CUtensorMap &qmap, const tc::TcParams &p, dim3 grid,
+                           cudaStream_t stream)
+{
+    return tc::launch_tc<InstT>(block_size, group, split, pool, qmap, p, grid, stream);
+}
+#endif
 } // namespace pa

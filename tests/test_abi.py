@@ -47,17 +47,22 @@ def test_status_strings(pa):
     assert pa.pa_version() >= 10000
 
 
-def test_workspace_size(pa):
-    # B*H*parts*(D floats) rounded to 256 B + B*H*parts*2 floats rounded to 256 B.
-    B, H, D, L, P = 8, 64, 128, 131072, 512
-    parts = L // P
+def _expected_ws(B, H, D, L, P):
+    """Header 256 B, then arrival counters (B*H), the unit list (B*parts) and
+    the partial o (fp32 D) and (m, l) per (sequence, head, partition), each
+    region rounded up to 256 bytes."""
+    r = lambda x: -(-x // 256) * 256
+    parts = max(1, -(-L // P))
     rows = B * H * parts
-    expect = -(-rows * D * 4 // 256) * 256 + -(-rows * 2 * 4 // 256) * 256
-    assert pa.pa_decode_splitk_workspace_size(B, H, D, L, P) == expect
-    assert pa.pa_decode_splitk_workspace_size(B, H, D, 513, 512) == \
-        -(-B * H * 2 * D * 4 // 256) * 256 + -(-B * H * 2 * 2 * 4 // 256) * 256
-    assert pa.pa_decode_splitk_workspace_size(-1, H, D, L, P) == 0
-    assert pa.pa_decode_splitk_workspace_size(B, H, D, L, 0) == 0
+    return 256 + r(B * H * 4) + r(B * parts * 4) + r(rows * D * 4) + r(rows * 2 * 4)
+
+
+def test_workspace_size(pa):
+    for B, H, D, L, P in [(8, 64, 128, 131072, 512), (8, 64, 128, 513, 512), (3, 4, 64, 0, 64),
+                          (64, 32, 128, 2048, 512)]:
+        assert pa.pa_decode_splitk_workspace_size(B, H, D, L, P) == _expected_ws(B, H, D, L, P)
+    assert pa.pa_decode_splitk_workspace_size(-1, 8, 128, 100, 512) == 0
+    assert pa.pa_decode_splitk_workspace_size(8, 8, 128, 100, 0) == 0
 
 
 def _raw(pa):
