@@ -47,7 +47,8 @@ static unsigned int *device_error_word(cudaError_t *err)
 // ---------------------------------------------------------------------------
 // TMA tensor map over the pool [2, NB, BS, Hkv, D], seen as 4-D
 // {D, Hkv, NB*BS, 2} (innermost first).  A box is 64 elements (128 bytes) of
-// one kv head for BS consecutive rows of one plane, loaded with the 128-byte
+// `box_heads` consecutive kv heads for `box_rows` consecutive token rows
+// (default: one head, one block) of one plane, loaded with the 128-byte
 // swizzle.  Rows at or past NB*BS are out of bounds and read as zeros.
 // ---------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
@@ -69,7 +70,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
 }
 
 static bool make_pool_map(CUtensorMap *map, const void *cache, int dtype, int num_blocks,
-                          int block_size, int num_kv_heads, int head_size)
+                          int block_size, int num_kv_heads, int head_size, int box_heads = 1,
+                          int box_rows = 0)
 {
     cudaError_t err;
     auto fn = encode_fn(&err);
@@ -80,7 +82,8 @@ static bool make_pool_map(CUtensorMap *map, const void *cache, int dtype, int nu
                           (cuuint64_t)num_blocks * block_size, 2};
     cuuint64_t strides[3] = {head_size * es, (cuuint64_t)num_kv_heads * head_size * es,
                              (cuuint64_t)num_blocks * block_size * num_kv_heads * head_size * es};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)block_size, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_heads,
+                         (cuuint32_t)(box_rows > 0 ? box_rows : block_size), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     4, const_cast<void *>(cache), dims, strides, box, estr,
@@ -89,10 +92,11 @@ static bool make_pool_map(CUtensorMap *map, const void *cache, int dtype, int nu
     return r == CUDA_SUCCESS;
 }
 
-// Query rows as a 2-D tensor {D, B*H}; a box is 64 elements of G consecutive
-// query heads (one kv head's group), loaded with the 128-byte swizzle.
+// Query rows as a 2-D tensor {D, B*H}; a box is 64 elements of `box_rows`
+// consecutive query heads (the groups of the CTA's kv heads), loaded with the
+// 128-byte swizzle.
 static bool make_q_map(CUtensorMap *map, const void *q, int dtype, int rows, int head_size,
-                       int group)
+                       int box_rows)
 {
     cudaError_t err;
     auto fn = encode_fn(&err);
@@ -100,7 +104,7 @@ static bool make_q_map(CUtensorMap *map, const void *q, int dtype, int rows, int
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)head_size * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)group};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     2, const_cast<void *>(q), dims, strides, box, estr,
@@ -333,8 +337,12 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_
         return PA_ERR_CUDA;
     const int group = num_heads / num_kv_heads;
     if (use_tc(head_size, group, false)) {
-        alignas(64) CUtensorMap qmap;
-        if (!make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, group))
+        const int hg = tc::heads_per_cta(group, num_kv_heads);
+        const int rows = block_size < 128 / hg ? block_size : 128 / hg;
+        alignas(64) CUtensorMap pmap, qmap;
+        if (!make_pool_map(&pmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads,
+                           head_size, hg, rows) ||
+            !make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, hg * group))
             return PA_ERR_CUDA;
         tc::TcParams t = {};
         t.out = out;
@@ -343,6 +351,7 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_
         t.err = err;
         t.num_heads = num_heads;
         t.num_kv_heads = num_kv_heads;
+        t.num_groups = num_kv_heads / hg;
         t.num_blocks = num_blocks;
         t.max_blocks = max_blocks_per_seq;
         t.part_tokens = max_blocks_per_seq * block_size;
@@ -350,8 +359,8 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_
         t.len_cap = max_blocks_per_seq * block_size;
         t.qscale = scale * kLog2e;
         auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
-        e = launch(block_size, group, false, tmap, qmap, t, dim3(num_kv_heads, num_seqs),
-                   static_cast<cudaStream_t>(stream));
+        e = launch(block_size, group, hg, false, pmap, qmap, t,
+                   dim3(num_kv_heads / hg, num_seqs), static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
     }
     DecodeParams p = {};
@@ -452,19 +461,24 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (use_tc(head_size, group, true)) {
-        alignas(64) CUtensorMap qmap;
-        if (!make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, group))
+        const int hg = tc::heads_per_cta(group, num_kv_heads);
+        const int ngroups = num_kv_heads / hg;
+        const int rows = block_size < 128 / hg ? block_size : 128 / hg;
+        alignas(64) CUtensorMap pmap, qmap;
+        if (!make_pool_map(&pmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads,
+                           head_size, hg, rows) ||
+            !make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, hg * group))
             return PA_ERR_CUDA;
         uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
         uint32_t *arrive = reinterpret_cast<uint32_t *>(wsb + lay.arrive);
         uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
         if (dtype == PA_BF16)
             tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, num_kv_heads, partition_size, len_cap, hdr, arrive,
+                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, arrive,
                 units, static_cast<__nv_bfloat16 *>(out), err);
         else
             tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, num_kv_heads, partition_size, len_cap, hdr, arrive,
+                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, arrive,
                 units, static_cast<__half *>(out), err);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -480,20 +494,30 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         t.ws_ml = ws_ml;
         t.num_heads = num_heads;
         t.num_kv_heads = num_kv_heads;
+        t.num_groups = ngroups;
         t.num_blocks = num_blocks;
         t.max_blocks = max_blocks_per_seq;
         t.part_tokens = partition_size;
         t.max_parts = (int)parts;
         t.len_cap = len_cap;
+        t.fused_merge = parts <= (size_t)tc::kFusedMergeMax;
         t.qscale = scale * kLog2e;
         const int sms = sm_count(&e);
         if (!sms)
             return PA_ERR_CUDA;
-        const size_t bound = (size_t)num_seqs * num_kv_heads * parts;
+        const size_t bound = (size_t)num_seqs * ngroups * parts;
         const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
         auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
-        e = launch(block_size, group, true, tmap, qmap, t, dim3(grid), s);
-        return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
+        e = launch(block_size, group, hg, true, pmap, qmap, t, dim3(grid), s);
+        if (e != cudaSuccess)
+            return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
+        if (!t.fused_merge) {
+            // Many partitions per sequence: merge them with the parallel reduce.
+            ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
+                              len_cap};
+            e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
+        }
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
 
     DecodeParams p = {};

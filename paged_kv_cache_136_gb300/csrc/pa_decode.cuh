@@ -397,9 +397,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // Log-sum-exp merge of the partitions of one (sequence, query head):
 // M = max_p m_p, out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
+// The partition weights are computed once into shared memory (chunks of
+// kReduceChunk partitions); each thread then sums its head_size element with
+// independent loads.
+constexpr int kReduceChunk = 512;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
 {
+    __shared__ float w_s[kReduceChunk];
+    __shared__ float red_s[D / 32];
+    __shared__ float M_s;
     const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
@@ -410,16 +418,38 @@ __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
         out[d] = Elem<T>::from(0.f);
         return;
     }
+    // global max of m over the partitions
     float M = -INFINITY;
-    for (int q = 0; q < np; ++q)
+    for (int q = d; q < np; q += D)
         M = fmaxf(M, p.ws_ml[(row0 + q) * 2]);
-    float acc = 0.f, den = 0.f;
-    for (int q = 0; q < np; ++q) {
-        const float w = ex2(p.ws_ml[(row0 + q) * 2] - M);
-        den = fmaf(w, p.ws_ml[(row0 + q) * 2 + 1], den);
-        acc = fmaf(w, p.ws_o[(row0 + q) * D + d], acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if ((d & 31) == 0)
+        red_s[d >> 5] = M;
+    __syncthreads();
+    if (d == 0) {
+        float mm = red_s[0];
+        for (int i = 1; i < D / 32; ++i)
+            mm = fmaxf(mm, red_s[i]);
+        M_s = mm;
     }
-    out[d] = Elem<T>::from(acc / den);
+    __syncthreads();
+    M = M_s;
+    float num = 0.f, den = 0.f;
+    for (int q0 = 0; q0 < np; q0 += kReduceChunk) {
+        const int nq = min(kReduceChunk, np - q0);
+        __syncthreads();
+        for (int q = d; q < nq; q += D)
+            w_s[q] = ex2(p.ws_ml[(row0 + q0 + q) * 2] - M);
+        __syncthreads();
+        for (int q = 0; q < nq; ++q)
+            den = fmaf(w_s[q], p.ws_ml[(row0 + q0 + q) * 2 + 1], den);
+#pragma unroll 8
+        for (int q = 0; q < nq; ++q)
+            num = fmaf(w_s[q], p.ws_o[(row0 + q0 + q) * D + d], num);
+    }
+    out[d] = Elem<T>::from(num / den);
 }
 
 // Launch helper shared by the instantiation units.

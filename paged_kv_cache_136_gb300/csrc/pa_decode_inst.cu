@@ -32,11 +32,11 @@ cudaError_t PA_LAUNCHER(const DecodeKey &key, const CUtensorMap &tmap, const Dec
 
 #if PA_INST_D == 128
 #define PA_TC_LAUNCHER PA_CAT(launch_decode_tc_, PA_DT_NAME, )
-cudaError_t PA_TC_LAUNCHER(int block_size, int group, bool split, const CUtensorMap &pool,
-                           const CUtensorMap &qmap, const tc::TcParams &p, dim3 grid,
-                           cudaStream_t stream)
+cudaError_t PA_TC_LAUNCHER(int block_size, int group, int hg, bool split,
+                           const CUtensorMap &pool, const CUtensorMap &qmap,
+                           const tc::TcParams &p, dim3 grid, cudaStream_t stream)
 {
-    return tc::launch_tc<InstT>(block_size, group, split, pool, qmap, p, grid, stream);
+    return tc::launch_tc<InstT>(block_size, group, hg, split, pool, qmap, p, grid, stream);
 }
 #endif
 } // namespace pa

@@ -1,38 +1,48 @@
 // pa_decode_tc.cuh -- paged decode attention on the 5th-generation tensor
 // cores (tcgen05, accumulators in tensor memory), head_size 128.
 //
-// Work item: (sequence s, kv head, token range).  Its tokens are walked in
-// stages of 128.  Roles in a CTA of 192 threads:
+// A CTA works on HG kv heads at once (HG = 16/G when num_kv_heads allows).  A
+// pipeline stage holds 128 rows ordered (token, kv head) -- TPS = 128/HG
+// tokens of all HG heads -- which is the order the NHD pool
+// [2, num_blocks, block_size, num_kv_heads, head_size] stores them in, so one
+// TMA box {64 elements, HG heads, R token rows} fetches all HG heads of R rows
+// ("Paged attention", k4i.top, section "block table": physical_block =
+// block_table[t // block_size]).  Roles in a CTA of 224 threads:
 //
-//   warp 4 (producer)   takes work items, reads each item's block-table
-//                       entries into lane registers, and TMA-loads per stage
-//                       the item's query rows (Q, G x 128) and, per physical
-//                       block, the block's K and V rows of the kv head
-//                       ("Paged attention", k4i.top, section "block table").
-//   warp 5 (MMA)        allocates 64 TMEM columns and issues, per stage,
-//                         S^T[128 tok x 16] = K[128 x 128] . Q^T   (scores)
-//                         O^T[128 d  x 16] = V^T[128 x 128 tok] . P (values)
-//                       with tcgen05.mma (M=128, N=16, K=16 per instruction).
-//                       S and O are double-buffered in TMEM.
-//   warps 0-3           one TMEM lane each: read the scores of their token,
-//   (softmax/epilogue)  scale, mask the tail, stage max over the 128 tokens,
-//                       online-softmax rescale ("Paged attention",
+//   warp 4 (producer)   takes work items, keeps the item's block-table entries
+//                       in lane registers, and TMA-loads per stage the query
+//                       rows of the HG heads (Q, HG*G x 128) and the K and V
+//                       row chunks, one box per lane.
+//   warp 5 (scores)     owns 128 TMEM columns and issues
+//                         S^T[128 rows x 16] = K[128 x 128] . Q^T
+//                       (tcgen05.mma, M=128, N=16, K=16 per instruction); row
+//                       (t, h) uses columns h*G .. h*G+G-1.
+//   warp 6 (values)     issues O^T[128 d x 32] = V^T[128 x 128 rows] . P,
+//                       contracting over all 128 rows of the stage; P holds
+//                       row (t, h)'s probabilities only in the columns of head
+//                       h (high parts in columns 0-15, low parts in 16-31), so
+//                       the other heads' rows add exact zeros.
+//   warps 0-3           one TMEM lane (stage row) each: scale and mask the
+//   (softmax/epilogue)  scores, stage max per (head, query) over the tokens,
+//                       online-softmax rescale ("Paged attention", section
 //                       "对非连续 blocks 做 attention"), write P as a bf16/fp16
-//                       high part (B rows 0-7) plus low part (rows 8-15), so
-//                       one N=16 MMA carries P to ~16 bits, zero V rows past
-//                       the sequence end, then read O for their head_size row
-//                       and accumulate o = alpha*o + O[g] + O[8+g].
+//                       high part plus low part (~16-bit accuracy), zero V rows
+//                       past the sequence end, and as head_size row d
+//                       accumulate o = alpha*o + O_high + O_low for every
+//                       (head, query) column.  S and O are double-buffered, so
+//                       the values of stage k run while stage k+1's softmax is
+//                       computed.
 //
 // The K and V tiles are read by the tensor cores straight from the TMA
-// layout: K as a K-major operand, V as an MN-major (transposed) operand; both
-// use the 128-byte swizzle (shared-memory matrix descriptors).
+// layout: K as a K-major operand, V as an MN-major (transposed) operand, both
+// with the 128-byte swizzle (shared-memory matrix descriptors).
 //
 // Split-K ("PagedAttention 在 vLLM 中的实现分析", section 7.3): items are
-// (partition of P tokens, kv head) pairs dealt dynamically to a persistent
+// (partition of P tokens, head group) pairs dealt dynamically to a persistent
 // grid through an atomic counter.  A sequence with one partition writes its
 // output directly; otherwise each partition writes its unnormalised (o, m, l)
 // to the workspace and the last partition to finish (an arrival counter per
-// (sequence, kv head)) merges them with the log-sum-exp rescale.
+// (sequence, head group)) merges them with the log-sum-exp rescale.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -45,19 +55,24 @@
 namespace pa {
 namespace tc {
 
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+// Warp roles.
+constexpr int kThreads = 224;
+constexpr int kEpiThreads = 128;          // warps 0-3: softmax / epilogue
+constexpr int kProducerWarp = 4;          // TMA
+constexpr int kQkWarp = 5;                // scores MMA issuer, owns TMEM
+constexpr int kPvWarp = 6;                // values MMA issuer
+
 constexpr int kStages = 3;
-constexpr int kTT = 128;                  // tokens per stage
+constexpr int kRows = 128;                // (token, kv head) rows per stage
 constexpr int kD = 128;                   // head_size
-constexpr int kRegion = kTT * 128;        // one 64-element half of 128 rows
+constexpr int kRegion = kRows * 128;      // one 64-element half of 128 rows
 constexpr int kPlane = 2 * kRegion;       // K (or V) of a stage
 constexpr int kStageBytes = 2 * kPlane;   // K + V
-constexpr int kQBytes = 2 * 1024;         // two 64-element halves x 8 rows
-constexpr int kPBytes = 4 * 1024;         // two 64-token halves x 16 rows (8 high, 8 low)
-constexpr int kTmemCols = 64;
+constexpr int kNQ = 16;                   // score columns: (head, query) pairs
+constexpr int kNP = 32;                   // value columns: high parts, then low parts
+constexpr int kQBytes = 2 * kNQ * 128;    // two 64-element halves x 16 rows
+constexpr int kPBytes = 2 * kNP * 128;    // two 64-row halves of K x 32 rows
+constexpr int kTmemCols = 128;            // S: 2 x 16 columns, O: 2 x 32 columns
 constexpr int kBarEpi = 1;                // named barrier of the softmax warps
 
 constexpr int kOffQ = kStages * kStageBytes;
@@ -65,21 +80,23 @@ constexpr int kOffP = kOffQ + kStages * kQBytes;
 constexpr int kOffMisc = kOffP + 2 * kPBytes;
 
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagStop = 4;
+constexpr int kFusedMergeMax = 8;         // partitions merged in-kernel by the last arriver
 
 struct StageDesc {
-    int s, kvh, part, nvalid, flags, nparts, tok0, pad;
+    int s, group, part, nvalid, flags, nparts, pad0, pad1;
 };
 
 struct Misc {
     StageDesc desc[kStages];
-    float red[2][4][8];   // per-stage max, double-buffered by stage parity
-    float red2[4][8];     // normaliser sums at item end
+    float red[2][4][kNQ];  // per-stage max, double-buffered by stage parity
+    float red2[4][kNQ];    // normaliser sums at item end
+    float ml[kNQ * kFusedMergeMax][2]; // (m, l) of every partition being merged
     int bcast[4];
     uint32_t tmem_base;
     uint32_t pad;
     uint64_t full[kStages], empty[kStages];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
-    uint64_t mma_done;
+    uint64_t mma_done[2];
 };
 
 constexpr int kSmemBytes = 1024 + kOffMisc + (int)sizeof(Misc);
@@ -91,12 +108,13 @@ struct TcParams {
     unsigned int *err;
     // split-K workspace (null in one-pass mode)
     uint32_t *hdr;               // [0] work counter, [1] total items
-    uint32_t *arrive;            // [B * Hkv] arrival counters
+    uint32_t *arrive;            // [B * num_groups] arrival counters
     const uint32_t *units;       // (s << 16) | partition
     float *ws_o;                 // [B, H, max_parts, 128]
     float *ws_ml;                // [B, H, max_parts, 2]
-    int num_heads, num_kv_heads, num_blocks, max_blocks;
+    int num_heads, num_kv_heads, num_groups, num_blocks, max_blocks;
     int part_tokens, max_parts, len_cap;
+    int fused_merge;             // split: last partition merges (else a reduce kernel follows)
     float qscale;
 };
 
@@ -141,18 +159,32 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int la
     return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
 }
 
-template <typename T, int BS, int G, bool SPLIT>
+// Byte offset of element (row n, column k) of a K-major operand with 128-byte
+// swizzle, stored as 64-column regions of `rows` rows each.
+__device__ __forceinline__ int sw128_offset(int n, int k, int rows)
+{
+    return (k >> 6) * rows * 128 + (n >> 3) * 1024 + (n & 7) * 128 +
+           ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
+}
+
+// HG kv heads per CTA; a stage holds TPS = 128/HG tokens of all HG heads,
+// rows ordered (token, head) exactly as the NHD pool stores them, so one TMA
+// box covers all HG heads of R consecutive token rows.
+template <typename T, int BS, int G, int HG, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap pool_map,
                      const __grid_constant__ CUtensorMap q_map, const TcParams p)
 {
-    static_assert(G >= 1 && G <= 8, "group size");
-    static_assert(kTT % BS == 0, "block size");
-    static_assert((kTT / BS) * 4 <= 32, "one TMA box per producer lane");
-    constexpr int SB = kTT / BS;               // physical blocks per stage
+    constexpr int NV = HG * G;                 // valid (head, query) columns
+    constexpr int TPS = kRows / HG;            // tokens per stage
+    constexpr int R = BS < TPS ? BS : TPS;     // token rows per TMA box
+    constexpr int CH = TPS / R;                // row chunks per stage
+    constexpr int BOX_BYTES = R * HG * 128;
+    static_assert(G >= 1 && NV <= kNQ && (HG & (HG - 1)) == 0, "heads per CTA");
+    static_assert(TPS % R == 0 && BS % R == 0 && CH * 4 <= 32, "stage geometry");
     constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-    constexpr uint32_t kIdescQK = idesc_f16_f32(kFmt, 0, 0, 128, 16);
-    constexpr uint32_t kIdescPV = idesc_f16_f32(kFmt, 1, 0, 128, 16);
+    constexpr uint32_t kIdescQK = idesc_f16_f32(kFmt, 0, 0, 128, kNQ);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kFmt, 1, 0, 128, kNP);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -162,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
+    // P entries of other heads' columns stay zero for the whole kernel: a
+    // row (token, head h) only ever writes the columns of head h.
+    for (int i = tid; i < 2 * kPBytes / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&m->full[i], 1);
@@ -172,11 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&m->p_full[i], 4);
             mbar_init(&m->o_full[i], 1);
             mbar_init(&m->o_free[i], 4);
+            mbar_init(&m->mma_done[i], 1);
         }
-        mbar_init(&m->mma_done, 1);
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kQkWarp) {
         tmem_alloc(&m->tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -198,53 +235,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (SPLIT)
             total = __ldcg(p.hdr + 1);
         int static_done = 0;
+        // Split mode resolves the NEXT work item a step at a time while the last
+        // stages of the current item are issued, so its chain of dependent
+        // loads (work counter -> unit -> seq_len and block table) overlaps the
+        // waits for free stage slots instead of stalling the ring at item
+        // changes.
+        int nstep = 0;                    // steps of the next item done so far
+        uint32_t nj_raw = 0, nj = 0, nu = 0;
+        int nL_raw = 0, ncur = -1, nnxt = -1, n_s = 0, n_group = 0, n_part = 0;
+        bool n_have = false;
+        auto next_step = [&]() {
+            if (nstep == 0) {
+                if (lane == 0)
+                    nj_raw = atomicAdd(p.hdr, 1u);
+            } else if (nstep == 1) {
+                nj = __shfl_sync(0xffffffffu, nj_raw, 0);
+                n_have = nj < total;
+                if (n_have)
+                    nu = __ldg(p.units + nj / p.num_groups);
+            } else if (nstep == 2 && n_have) {
+                n_group = (int)(nj % p.num_groups);
+                n_s = (int)(nu >> 16);
+                n_part = (int)(nu & 0xFFFFu);
+                nL_raw = __ldg(p.seq_lens + n_s);
+                // Table entries past the item's end are loaded but never used.
+                const int jb = n_part * p.part_tokens / BS;
+                const int32_t *btn = p.block_tables + (size_t)n_s * p.max_blocks;
+                ncur = (jb + lane < p.max_blocks) ? __ldg(btn + jb + lane) : -1;
+                nnxt = (jb + 32 + lane < p.max_blocks) ? __ldg(btn + jb + 32 + lane) : -1;
+            }
+            ++nstep;
+        };
+        bool have_tab = false; // cur/nxt already hold the item's first table entries
+        int cur = -1, nxt = -1;
         while (alive) {
-            // ---- next work item
-            int s = 0, kvh = 0, part = 0, L = 0, nparts = 1;
+            // ---- next work item: (sequence, group of HG kv heads, partition)
+            int s = 0, group = 0, part = 0, L = 0, nparts = 1;
             bool have = false;
             if (SPLIT) {
-                uint32_t j = 0;
-                if (lane == 0)
-                    j = atomicAdd(p.hdr, 1u);
-                j = __shfl_sync(0xffffffffu, j, 0);
-                if (j < total) {
-                    const uint32_t u = __ldg(p.units + j / p.num_kv_heads);
-                    kvh = (int)(j % p.num_kv_heads);
-                    s = (int)(u >> 16);
-                    part = (int)(u & 0xFFFFu);
-                    L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
+                while (nstep < 3)
+                    next_step();
+                if (n_have) {
+                    s = n_s;
+                    group = n_group;
+                    part = n_part;
+                    int Lr = nL_raw;
+                    if (lane == 0)
+                        Lr = clamp_len(Lr, p.len_cap, p.err);
+                    L = __shfl_sync(0xffffffffu, Lr, 0);
                     nparts = (L + p.part_tokens - 1) / p.part_tokens;
+                    cur = ncur;
+                    nxt = nnxt;
+                    have_tab = true;
                     have = true;
+                    nstep = 0;
                 }
             } else if (!static_done) {
-                kvh = blockIdx.x;
+                group = blockIdx.x;
                 s = blockIdx.y;
                 int Lr = __ldg(p.seq_lens + s);
                 if (lane == 0)
                     Lr = clamp_len(Lr, p.len_cap, p.err);
-                L = __shfl_sync(0xffffffffu, Lr < 0 ? 0 : (Lr > p.len_cap ? p.len_cap : Lr), 0);
+                L = __shfl_sync(0xffffffffu, Lr, 0);
                 nparts = 1;
                 have = L > 0;
                 static_done = 1;
                 if (!have) {
                     // Empty sequence: its output rows are zero.
-                    T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + kvh * G) * kD;
-                    for (int i = lane; i < G * kD; i += 32)
+                    T *out = reinterpret_cast<T *>(p.out) +
+                             ((size_t)s * p.num_heads + group * NV) * kD;
+                    for (int i = lane; i < NV * kD; i += 32)
                         out[i] = Elem<T>::from(0.f);
                 }
             }
             if (!have)
                 break;
+            const int kvh0 = group * HG;
             const int tok0 = SPLIT ? part * p.part_tokens : 0;
             const int tok1 = SPLIT ? min(L, tok0 + p.part_tokens) : L;
             const int jb0 = tok0 / BS;
             const int jend = (tok1 + BS - 1) / BS;
-            const int nst = (tok1 - tok0 + kTT - 1) / kTT;
+            const int nst = (tok1 - tok0 + TPS - 1) / TPS;
             const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks;
             int cbase = jb0;
-            int cur = (cbase + lane < jend) ? __ldg(bt + cbase + lane) : -1;
-            int nxt = (cbase + 32 + lane < jend) ? __ldg(bt + cbase + 32 + lane) : -1;
-            const int qrow = s * p.num_heads + kvh * G;
+            if (!have_tab) {
+                cur = (cbase + lane < jend) ? __ldg(bt + cbase + lane) : -1;
+                nxt = (cbase + 32 + lane < jend) ? __ldg(bt + cbase + 32 + lane) : -1;
+            }
+            have_tab = false;
+            const int qrow = s * p.num_heads + kvh0 * G;
             for (int st = 0; st < nst; ++st, ++gk) {
                 const int slot = gk % kStages;
                 if (gk >= kStages && !warp_wait(&m->empty[slot], ((gk / kStages) - 1) & 1, lane)) {
@@ -253,35 +332,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alive = false;
                     break;
                 }
-                const int jf = jb0 + st * SB;
-                if (jf >= cbase + 32) {
+                const int t_lo = tok0 + st * TPS;
+                const int nvalid = min(TPS, tok1 - t_lo);
+                const int nch = (nvalid + R - 1) / R;
+                if (t_lo / BS >= cbase + 32) {
                     cbase += 32;
                     cur = nxt;
                     nxt = (cbase + 32 + lane < jend) ? __ldg(bt + cbase + 32 + lane) : -1;
                 }
-                const int nblk = min(SB, jend - jf);
-                const int t_lo = tok0 + st * kTT;
                 uint8_t *kv = smem + slot * kStageBytes;
                 uint8_t *qb = smem + kOffQ + slot * kQBytes;
                 if (lane == 0) {
                     StageDesc &d = m->desc[slot];
                     d.s = s;
-                    d.kvh = kvh;
+                    d.group = group;
                     d.part = part;
-                    d.nvalid = min(kTT, tok1 - t_lo);
+                    d.nvalid = nvalid;
                     d.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
                     d.nparts = nparts;
-                    d.tok0 = t_lo;
                     mbar_arrive_expect_tx(&m->full[slot],
-                                          (uint32_t)(nblk * BS * 128 * 2 * 2 + 2 * G * 128));
+                                          (uint32_t)(nch * 4 * BOX_BYTES + 2 * NV * 128));
                     tma_load_2d(qb, &q_map, &m->full[slot], 0, qrow);
-                    tma_load_2d(qb + 1024, &q_map, &m->full[slot], 64, qrow);
+                    tma_load_2d(qb + kNQ * 128, &q_map, &m->full[slot], 64, qrow);
                 }
                 __syncwarp();
-                // One K/V box per lane (box i: block i/4, plane, 64-element half).
-                const int jj = lane >> 2;
-                const int phys = __shfl_sync(0xffffffffu, cur, (jf - cbase + (jj < SB ? jj : 0)) & 31);
-                if (lane < nblk * 4) {
+                // One K/V box per lane: box i covers row chunk i/4 of plane
+                // (i/2)&1, 64-element half i&1, for all HG heads.
+                const int c = lane >> 2;
+                const int t = t_lo + (c < CH ? c : 0) * R;
+                const int phys = __shfl_sync(0xffffffffu, cur, (t / BS - cbase) & 31);
+                if (lane < nch * 4) {
                     const int plane = (lane >> 1) & 1;
                     const int r = lane & 1;
                     int row;
@@ -289,11 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         atomicOr(p.err, PA_DEVERR_BLOCK_ID_);
                         row = p.num_blocks * BS; // past the extent: zero fill
                     } else {
-                        row = phys * BS;
+                        row = phys * BS + t % BS;
                     }
-                    tma_load_4d_hint(kv + plane * kPlane + r * kRegion + jj * BS * 128, &pool_map,
-                                     &m->full[slot], r * 64, kvh, row, plane, policy);
+                    tma_load_4d_hint(kv + plane * kPlane + r * kRegion + c * BOX_BYTES, &pool_map,
+                                     &m->full[slot], r * 64, kvh0, row, plane, policy);
                 }
+                // Next item: claim it when three stages of this one are left
+                // to issue (claiming earlier would unbalance the tail), then
+                // its unit, then its length and table.
+                if (SPLIT && nst - 1 - st <= 2 && nstep < 3 - (nst - 1 - st))
+                    next_step();
             }
         }
         // ---- tell the other roles that no work is left
@@ -308,117 +393,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT_);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ===================================================================== MMA
-        int kq = 0, kp = 0, stop_at = -1;
-        unsigned long long idle_since = 0;
-        while (stop_at < 0 || kp < stop_at) {
-            bool progress = false;
-            // Scores of stage kq once it has landed and its S buffer is free.
-            if (stop_at < 0 && kq <= kp + 1) {
-                const int slot = kq % kStages;
-                int ready = 0;
+    } else if (warp == kQkWarp || warp == kPvWarp) {
+        // ==================================================== MMA issuers
+        const bool qk = warp == kQkWarp;
+        for (int k = 0;; ++k) {
+            const int slot = k % kStages;
+            const int b = k & 1;
+            const int u = k >> 1;
+            if (!warp_wait(&m->full[slot], (k / kStages) & 1, lane)) {
                 if (lane == 0)
-                    ready = mbar_test_wait(&m->full[slot], (kq / kStages) & 1);
-                if (__shfl_sync(0xffffffffu, ready, 0)) {
-                    progress = true;
-                    int stop = 0;
-                    if (lane == 0) // lane 0 did the acquiring wait
-                        stop = m->desc[slot].flags & kFlagStop;
-                    if (__shfl_sync(0xffffffffu, stop, 0)) {
-                        stop_at = kq;
-                    } else {
-                        tc_fence_after_sync();
-                        if (lane == 0) {
-                            const uint32_t kbase = smem_addr(smem + slot * kStageBytes);
-                            const uint32_t qbase = smem_addr(smem + kOffQ + slot * kQBytes);
-                            const uint32_t d_tmem = tmem + (uint32_t)((kq & 1) * 16);
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint32_t koff = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
-                                const uint32_t qoff = (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 32);
-                                umma_f16(d_tmem, smem_desc_sw128(kbase + koff, 16, 1024),
-                                         smem_desc_sw128(qbase + qoff, 16, 1024), kIdescQK,
-                                         kk > 0 ? 1u : 0u);
-                            }
-                            umma_commit(&m->s_full[kq & 1]);
-                        }
-                        __syncwarp();
-                        ++kq;
-                    }
-                }
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+                break;
             }
-            // Values of stage kp once its P is written and its O buffer is free.
-            if (kp < kq) {
-                const int b = kp & 1;
-                const int u = kp >> 1;
-                int ready = 0;
-                if (lane == 0)
-                    ready = mbar_test_wait(&m->p_full[b], u & 1) &&
-                            (u == 0 || mbar_test_wait(&m->o_free[b], (u - 1) & 1));
-                if (__shfl_sync(0xffffffffu, ready, 0)) {
-                    progress = true;
-                    tc_fence_after_sync();
-                    if (lane == 0) {
-                        const int slot = kp % kStages;
-                        const uint32_t vbase = smem_addr(smem + slot * kStageBytes + kPlane);
-                        const uint32_t pbase = smem_addr(smem + kOffP + b * kPBytes);
-                        const uint32_t d_tmem = tmem + (uint32_t)(32 + b * 16);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t a = smem_desc_sw128(vbase + kk * 2048, kRegion, 1024);
-                            const uint32_t poff = (uint32_t)((kk >> 2) * 2048 + (kk & 3) * 32);
-                            umma_f16(d_tmem, a, smem_desc_sw128(pbase + poff, 16, 1024), kIdescPV,
-                                     kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(&m->o_full[b]);
-                        umma_commit(&m->empty[slot]);
-                    }
-                    __syncwarp();
-                    ++kp;
-                }
-            }
-            if (progress) {
-                idle_since = 0;
+            int stop = 0;
+            if (lane == 0)
+                stop = m->desc[slot].flags & kFlagStop;
+            if (__shfl_sync(0xffffffffu, stop, 0))
+                break;
+            bool ok = true;
+            if (qk) {
+                // S[b] is free once the softmax of stage k-2 is done.
+                if (u > 0)
+                    ok = warp_wait(&m->p_full[b], (u - 1) & 1, lane);
             } else {
-                const unsigned long long now = global_ns();
-                if (idle_since == 0) {
-                    idle_since = now;
-                } else if (now - idle_since > kWaitLimitNs) {
-                    if (lane == 0)
-                        atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-                    break;
+                ok = warp_wait(&m->p_full[b], u & 1, lane);
+                if (ok && u > 0)
+                    ok = warp_wait(&m->o_free[b], (u - 1) & 1, lane);
+            }
+            if (!ok) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+                break;
+            }
+            tc_fence_after_sync();
+            if (lane == 0) {
+                const uint32_t kvbase = smem_addr(smem + slot * kStageBytes);
+                if (qk) {
+                    const uint32_t qbase = smem_addr(smem + kOffQ + slot * kQBytes);
+                    const uint32_t d_tmem = tmem + (uint32_t)(b * kNQ);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
+                        const uint32_t qoff = (uint32_t)((kk >> 2) * kNQ * 128 + (kk & 3) * 32);
+                        umma_f16(d_tmem, smem_desc_sw128(kvbase + koff, 16, 1024),
+                                 smem_desc_sw128(qbase + qoff, 16, 1024), kIdescQK,
+                                 kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&m->s_full[b]);
+                } else {
+                    const uint32_t vbase = kvbase + kPlane;
+                    const uint32_t pbase = smem_addr(smem + kOffP + b * kPBytes);
+                    const uint32_t d_tmem = tmem + (uint32_t)(2 * kNQ + b * kNP);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t poff = (uint32_t)((kk >> 2) * kNP * 128 + (kk & 3) * 32);
+                        umma_f16(d_tmem, smem_desc_sw128(vbase + kk * 2048, kRegion, 1024),
+                                 smem_desc_sw128(pbase + poff, 16, 1024), kIdescPV,
+                                 kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&m->o_full[b]);
+                    umma_commit(&m->empty[slot]);
                 }
             }
+            __syncwarp();
         }
-        // Drain: every issued MMA completes before TMEM is released.
+        // Drain: every MMA this warp issued completes before TMEM is freed.
+        const int wi = qk ? 0 : 1;
         if (lane == 0)
-            umma_commit(&m->mma_done);
-        warp_wait(&m->mma_done, 0, lane);
-    } else {
+            umma_commit(&m->mma_done[wi]);
+        warp_wait(&m->mma_done[wi], 0, lane);
+    } else if (warp < 4) {
         // ======================================================== softmax/epilogue
-        const int t = tid; // token slot of the stage and head_size row of O
+        const int t = tid;                 // stage row (token t/HG, head t%HG); O row d = t
+        const int h = t % HG;
         const uint32_t lane_base = (uint32_t)((warp * 32) << 16);
-        float m_run[G], l_part[G], o_acc[G], alpha_prev[G];
+        float m_run[NV], o_acc[NV], alpha_prev[NV], l_part[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            m_run[g] = -INFINITY;
-            l_part[g] = 0.f;
-            o_acc[g] = 0.f;
-            alpha_prev[g] = 0.f;
+        for (int n = 0; n < NV; ++n) {
+            m_run[n] = -INFINITY;
+            o_acc[n] = 0.f;
+            alpha_prev[n] = 0.f;
         }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            l_part[g] = 0.f;
         bool pending = false; // the previous stage's O is still to be accumulated
-        // o = alpha*o + O(stage k), then hand the O buffer back to the MMA warp.
-        auto take_o = [&](int k, const float (&alpha)[G]) -> bool {
+        // o = alpha*o + O_high + O_low for stage k, then free the O buffer.
+        auto take_o = [&](int k, const float (&alpha)[NV]) -> bool {
             const int b = k & 1;
             const bool okw = mbar_wait(&m->o_full[b], (k >> 1) & 1);
             __syncwarp();
             tc_fence_after_sync();
-            float ov[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(32 + b * 16), ov);
+            float lo16[16], hi16[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)(2 * kNQ + b * kNP), hi16);
+            tmem_ld16(tmem + lane_base + (uint32_t)(2 * kNQ + b * kNP + 16), lo16);
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-                o_acc[g] = fmaf(o_acc[g], alpha[g], ov[g] + ov[8 + g]);
+            for (int n = 0; n < NV; ++n)
+                o_acc[n] = fmaf(o_acc[n], alpha[n], hi16[n] + lo16[n]);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
@@ -440,59 +511,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             if (d.flags & kFlagFirst) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    m_run[g] = -INFINITY;
-                    l_part[g] = 0.f;
-                    o_acc[g] = 0.f;
+                for (int n = 0; n < NV; ++n) {
+                    m_run[n] = -INFINITY;
+                    o_acc[n] = 0.f;
                 }
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    l_part[g] = 0.f;
                 pending = false;
             }
             ok = mbar_wait(&m->s_full[b], u & 1);
             __syncwarp();
             tc_fence_after_sync();
-            float sv[8];
-            tmem_ld8(tmem + lane_base + (uint32_t)(b * 16), sv);
-            const bool valid = t < d.nvalid;
+            float sv[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)(b * kNQ), sv);
+            const bool valid = (t / HG) < d.nvalid;
             float x[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                x[g] = valid ? sv[g] * p.qscale : -INFINITY;
-                float v = x[g];
+                float v = sv[g];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-                if (lane == 0)
-                    m->red[b][warp][g] = v;
+                for (int hh = 1; hh < HG; ++hh)
+                    if (h == hh)
+                        v = sv[hh * G + g];
+                x[g] = valid ? v * p.qscale : -INFINITY;
+                // max over this warp's tokens of the same head
+                float mx = x[g];
+#pragma unroll
+                for (int off = HG; off < 32; off <<= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                if (lane < HG)
+                    m->red[b][warp][lane * G + g] = mx;
             }
             if (bar_sync_or(kBarEpi, kEpiThreads, !ok)) {
                 if (t == 0)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT_);
                 break;
             }
-            float alpha[G];
+            float alpha[NV];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float mst = fmaxf(fmaxf(m->red[b][0][g], m->red[b][1][g]),
-                                        fmaxf(m->red[b][2][g], m->red[b][3][g]));
-                const float m_new = fmaxf(m_run[g], mst);
-                alpha[g] = ex2(m_run[g] - m_new);
-                m_run[g] = m_new;
+            for (int n = 0; n < NV; ++n) {
+                const float mst = fmaxf(fmaxf(m->red[b][0][n], m->red[b][1][n]),
+                                        fmaxf(m->red[b][2][n], m->red[b][3][n]));
+                const float m_new = fmaxf(m_run[n], mst);
+                alpha[n] = ex2(m_run[n] - m_new);
+                m_run[n] = m_new;
             }
-            // P as the K-major B operand: high part in row g, low part in
-            // row 8+g (the next 8-row swizzle atom), column = token t.
-            uint8_t *phi = smem + kOffP + b * kPBytes;
-            uint8_t *plo = phi + 1024;
-            const int poff = (t >> 6) * 2048 + (t & 7) * 2;
-            const int pc = (t & 63) >> 3;
+            // P as the K-major B operand of the values MMA: column (k index)
+            // = this row t; row h*G+g holds the high part, 16+h*G+g the low.
+            uint8_t *pb = smem + kOffP + b * kPBytes;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float pr = ex2(x[g] - m_run[g]);
-                l_part[g] = fmaf(l_part[g], alpha[g], pr);
+                float mg = m_run[g], ag = alpha[g];
+#pragma unroll
+                for (int hh = 1; hh < HG; ++hh)
+                    if (h == hh) {
+                        mg = m_run[hh * G + g];
+                        ag = alpha[hh * G + g];
+                    }
+                const float pr = ex2(x[g] - mg);
+                l_part[g] = fmaf(l_part[g], ag, pr);
                 uint16_t hi, lo;
                 Bits<T>::split(pr, hi, lo);
-                const int off = poff + g * 128 + ((pc ^ g) << 4);
-                *reinterpret_cast<uint16_t *>(phi + off) = hi;
-                *reinterpret_cast<uint16_t *>(plo + off) = lo;
+                const int n = h * G + g;
+                *reinterpret_cast<uint16_t *>(pb + sw128_offset(n, t, kNP)) = hi;
+                *reinterpret_cast<uint16_t *>(pb + sw128_offset(kNQ + n, t, kNP)) = lo;
             }
             if (!valid) {
                 // V rows past the end may hold anything (stale tiles, NaN
@@ -514,8 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pending && !take_o(k - 1, alpha_prev) && t == 0)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT_);
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-                alpha_prev[g] = alpha[g];
+            for (int n = 0; n < NV; ++n)
+                alpha_prev[n] = alpha[n];
             pending = true;
 
             if (!(d.flags & kFlagLast))
@@ -523,62 +606,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!take_o(k, alpha_prev) && t == 0)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT_);
             pending = false;
-            // ---- end of the item: normaliser over the 128 token slots
+            // ---- end of the item: normaliser of each (head, query) column
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float v = l_part[g];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
+                for (int off = HG; off < 32; off <<= 1)
                     v += __shfl_xor_sync(0xffffffffu, v, off);
-                if (lane == 0)
-                    m->red2[warp][g] = v;
+                if (lane < HG)
+                    m->red2[warp][lane * G + g] = v;
             }
             bar_sync(kBarEpi, kEpiThreads);
-            float l[G];
+            float l[NV];
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-                l[g] = (m->red2[0][g] + m->red2[1][g]) + (m->red2[2][g] + m->red2[3][g]);
-            const int h0 = d.kvh * G;
-            if (!SPLIT || d.nparts == 1) {
-                T *out = reinterpret_cast<T *>(p.out) + ((size_t)d.s * p.num_heads + h0) * kD;
+            for (int n = 0; n < NV; ++n)
+                l[n] = (m->red2[0][n] + m->red2[1][n]) + (m->red2[2][n] + m->red2[3][n]);
+            const size_t head0 = (size_t)d.s * p.num_heads + (size_t)d.group * NV;
+            if (!SPLIT || (p.fused_merge && d.nparts == 1)) {
+                T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-                    out[g * kD + t] = Elem<T>::from(o_acc[g] / l[g]);
+                for (int n = 0; n < NV; ++n)
+                    out[n * kD + t] = Elem<T>::from(o_acc[n] / l[n]);
             } else {
-                const size_t row0 = ((size_t)d.s * p.num_heads + h0) * p.max_parts + d.part;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const size_t row = row0 + (size_t)g * p.max_parts;
-                    p.ws_o[row * kD + t] = o_acc[g];
-                    if (t == g) {
-                        p.ws_ml[row * 2] = m_run[g];
-                        p.ws_ml[row * 2 + 1] = l[g];
+                for (int n = 0; n < NV; ++n) {
+                    const size_t row = (head0 + n) * p.max_parts + d.part;
+                    p.ws_o[row * kD + t] = o_acc[n];
+                    if (t == n) {
+                        p.ws_ml[row * 2] = m_run[n];
+                        p.ws_ml[row * 2 + 1] = l[n];
                     }
                 }
+                if (!p.fused_merge)
+                    continue; // the reduce kernel merges the partitions
                 __threadfence();
                 bar_sync(kBarEpi, kEpiThreads);
                 if (t == 0) {
-                    const uint32_t old = atomicAdd(p.arrive + d.s * p.num_kv_heads + d.kvh, 1u);
+                    const uint32_t old = atomicAdd(p.arrive + d.s * p.num_groups + d.group, 1u);
                     m->bcast[0] = (old == (uint32_t)(d.nparts - 1)) ? 1 : 0;
                 }
                 bar_sync(kBarEpi, kEpiThreads);
                 if (m->bcast[0]) {
-                    // Last partition of (s, kv head): merge every partition.
+                    // Last partition of (s, group): merge every partition.  All
+                    // (m, l) pairs are fetched at once into shared memory, then
+                    // each thread sums its head_size row with independent loads.
                     __threadfence();
-                    T *out = reinterpret_cast<T *>(p.out) + ((size_t)d.s * p.num_heads + h0) * kD;
-                    for (int g = 0; g < G; ++g) {
-                        const size_t rg = ((size_t)d.s * p.num_heads + h0 + g) * p.max_parts;
+                    const int np = d.nparts; // <= kFusedMergeMax here
+                    for (int i = t; i < NV * np; i += kEpiThreads) {
+                        const size_t row = (head0 + i / np) * p.max_parts + i % np;
+                        m->ml[i][0] = __ldcg(p.ws_ml + row * 2);
+                        m->ml[i][1] = __ldcg(p.ws_ml + row * 2 + 1);
+                    }
+                    bar_sync(kBarEpi, kEpiThreads);
+                    T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) {
+                        const size_t rg = (head0 + n) * p.max_parts;
                         float M = -INFINITY;
-                        for (int q = 0; q < d.nparts; ++q)
-                            M = fmaxf(M, __ldcg(p.ws_ml + (rg + q) * 2));
+                        for (int q = 0; q < np; ++q)
+                            M = fmaxf(M, m->ml[n * np + q][0]);
                         float num = 0.f, den = 0.f;
-                        for (int q = 0; q < d.nparts; ++q) {
-                            const float w = ex2(__ldcg(p.ws_ml + (rg + q) * 2) - M);
-                            den = fmaf(w, __ldcg(p.ws_ml + (rg + q) * 2 + 1), den);
+#pragma unroll 4
+                        for (int q = 0; q < np; ++q) {
+                            const float w = ex2(m->ml[n * np + q][0] - M);
+                            den = fmaf(w, m->ml[n * np + q][1], den);
                             num = fmaf(w, __ldcg(p.ws_o + (rg + q) * kD + t), num);
                         }
-                        out[g * kD + t] = Elem<T>::from(num / den);
+                        out[n * kD + t] = Elem<T>::from(num / den);
                     }
+                    bar_sync(kBarEpi, kEpiThreads); // ml is reused by the next merge
                 }
             }
         }
@@ -586,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kQkWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -660,11 +756,11 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
         hdr[1] = carry_s * (uint32_t)Hkv;
 }
 
-template <typename T, int BS, int G, bool SPLIT>
+template <typename T, int BS, int G, int HG, bool SPLIT>
 cudaError_t launch_tc_one(const CUtensorMap &pool, const CUtensorMap &qmap, const TcParams &p,
                           dim3 grid, cudaStream_t stream)
 {
-    auto kern = decode_tc_kernel<T, BS, G, SPLIT>;
+    auto kern = decode_tc_kernel<T, BS, G, HG, SPLIT>;
     static unsigned long long done_mask = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -681,31 +777,45 @@ cudaError_t launch_tc_one(const CUtensorMap &pool, const CUtensorMap &qmap, cons
     return cudaGetLastError();
 }
 
-template <typename T, int G>
+template <typename T, int G, int HG>
 cudaError_t launch_tc_bs(int block_size, bool split, const CUtensorMap &pool,
                          const CUtensorMap &qmap, const TcParams &p, dim3 grid,
                          cudaStream_t stream)
 {
     if (block_size == 16)
-        return split ? launch_tc_one<T, 16, G, true>(pool, qmap, p, grid, stream)
-                     : launch_tc_one<T, 16, G, false>(pool, qmap, p, grid, stream);
+        return split ? launch_tc_one<T, 16, G, HG, true>(pool, qmap, p, grid, stream)
+                     : launch_tc_one<T, 16, G, HG, false>(pool, qmap, p, grid, stream);
     if (block_size == 32)
-        return split ? launch_tc_one<T, 32, G, true>(pool, qmap, p, grid, stream)
-                     : launch_tc_one<T, 32, G, false>(pool, qmap, p, grid, stream);
+        return split ? launch_tc_one<T, 32, G, HG, true>(pool, qmap, p, grid, stream)
+                     : launch_tc_one<T, 32, G, HG, false>(pool, qmap, p, grid, stream);
     return cudaErrorNotSupported;
 }
 
+// Kv heads per CTA for group size G: 16/G when num_kv_heads allows it, else 1.
+__host__ __device__ constexpr int heads_per_cta(int group, int num_kv_heads)
+{
+    return (num_kv_heads % (16 / group) == 0) ? 16 / group : 1;
+}
+
 template <typename T>
-cudaError_t launch_tc(int block_size, int group, bool split, const CUtensorMap &pool,
+cudaError_t launch_tc(int block_size, int group, int hg, bool split, const CUtensorMap &pool,
                       const CUtensorMap &qmap, const TcParams &p, dim3 grid, cudaStream_t stream)
 {
+#define PA_TC_CASE(Gv)                                                                        \
+    case Gv:                                                                                  \
+        return hg == 16 / Gv ? launch_tc_bs<T, Gv, 16 / Gv>(block_size, split, pool, qmap, p, \
+                                                             grid, stream)                    \
+                             : (hg == 1 ? launch_tc_bs<T, Gv, 1>(block_size, split, pool,      \
+                                                                 qmap, p, grid, stream)       \
+                                        : cudaErrorNotSupported);
     switch (group) {
-    case 1: return launch_tc_bs<T, 1>(block_size, split, pool, qmap, p, grid, stream);
-    case 2: return launch_tc_bs<T, 2>(block_size, split, pool, qmap, p, grid, stream);
-    case 4: return launch_tc_bs<T, 4>(block_size, split, pool, qmap, p, grid, stream);
-    case 8: return launch_tc_bs<T, 8>(block_size, split, pool, qmap, p, grid, stream);
+        PA_TC_CASE(1)
+        PA_TC_CASE(2)
+        PA_TC_CASE(4)
+        PA_TC_CASE(8)
     default: return cudaErrorNotSupported;
     }
+#undef PA_TC_CASE
 }
 
 } // namespace tc

@@ -69,14 +69,14 @@ cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int n
 namespace tc {
 struct TcParams;
 }
-// Tensor-core (tcgen05) decode kernels, head_size 128.  One-pass: grid
-// (Hkv, B), one (kv head, sequence) per CTA.  Split: persistent 1-D grid fed
-// by the work counter of the plan.
-cudaError_t launch_decode_tc_f16(int block_size, int group, bool split, const CUtensorMap &pool,
-                                 const CUtensorMap &qmap, const tc::TcParams &p, dim3 grid,
-                                 cudaStream_t stream);
-cudaError_t launch_decode_tc_bf16(int block_size, int group, bool split, const CUtensorMap &pool,
-                                  const CUtensorMap &qmap, const tc::TcParams &p, dim3 grid,
-                                  cudaStream_t stream);
+// Tensor-core (tcgen05) decode kernels, head_size 128, `hg` kv heads per
+// CTA.  One-pass: grid (Hkv/hg, B), one (head group, sequence) per CTA.
+// Split: persistent 1-D grid fed by the work counter of the plan.
+cudaError_t launch_decode_tc_f16(int block_size, int group, int hg, bool split,
+                                 const CUtensorMap &pool, const CUtensorMap &qmap,
+                                 const tc::TcParams &p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_decode_tc_bf16(int block_size, int group, int hg, bool split,
+                                  const CUtensorMap &pool, const CUtensorMap &qmap,
+                                  const tc::TcParams &p, dim3 grid, cudaStream_t stream);
 
 } // namespace pa
