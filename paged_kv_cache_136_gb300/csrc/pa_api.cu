@@ -391,20 +391,18 @@ static size_t splitk_parts(int max_seq_len, int partition_size)
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Split-K workspace: [header 256 B: work counter, item count]
-// [arrival counters, one per (sequence, head)] [unit list, one per
-// (sequence, partition)] [partial o, fp32 D per row] [partial (m, l)],
+// Split-K workspace: [header 256 B: work counter, item count] [unit list,
+// one per (sequence, partition)] [partial o, fp32 D per row] [partial (m, l)],
 // each region 256-byte aligned; rows = B * H * partitions.
 struct WsLayout {
-    size_t arrive, units, o, ml, total;
+    size_t units, o, ml, total;
 };
 
 static WsLayout ws_layout(int num_seqs, int num_heads, int head_size, size_t parts)
 {
     WsLayout w;
     const size_t rows = (size_t)num_seqs * num_heads * parts;
-    w.arrive = 256;
-    w.units = w.arrive + round_up((size_t)num_seqs * num_heads * 4, 256);
+    w.units = 256;
     w.o = w.units + round_up((size_t)num_seqs * parts * 4, 256);
     w.ml = w.o + round_up(rows * head_size * sizeof(float), 256);
     w.total = w.ml + round_up(rows * 2 * sizeof(float), 256);
@@ -470,16 +468,15 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
             !make_q_map(&qmap, q, dtype, num_seqs * num_heads, head_size, hg * group))
             return PA_ERR_CUDA;
         uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
-        uint32_t *arrive = reinterpret_cast<uint32_t *>(wsb + lay.arrive);
         uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
         if (dtype == PA_BF16)
             tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, arrive,
-                units, static_cast<__nv_bfloat16 *>(out), err);
+                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
+                static_cast<__nv_bfloat16 *>(out), err);
         else
             tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, arrive,
-                units, static_cast<__half *>(out), err);
+                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
+                static_cast<__half *>(out), err);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return PA_ERR_CUDA;
         tc::TcParams t = {};
@@ -488,7 +485,6 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         t.seq_lens = seq_lens;
         t.err = err;
         t.hdr = hdr;
-        t.arrive = arrive;
         t.units = units;
         t.ws_o = ws_o;
         t.ws_ml = ws_ml;
@@ -500,7 +496,6 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         t.part_tokens = partition_size;
         t.max_parts = (int)parts;
         t.len_cap = len_cap;
-        t.fused_merge = parts <= (size_t)tc::kFusedMergeMax;
         t.qscale = scale * kLog2e;
         const int sms = sm_count(&e);
         if (!sms)
@@ -511,10 +506,10 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         e = launch(block_size, group, hg, true, pmap, qmap, t, dim3(grid), s);
         if (e != cudaSuccess)
             return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
-        if (!t.fused_merge) {
-            // Many partitions per sequence: merge them with the parallel reduce.
+        if (parts > 1) {
+            // Merge the partitions of multi-partition sequences.
             ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
-                              len_cap};
+                              len_cap, 1};
             e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
         }
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -539,7 +534,8 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
     e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
     if (e != cudaSuccess)
         return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
-    ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size, len_cap};
+    ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size, len_cap,
+                      0};
     e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

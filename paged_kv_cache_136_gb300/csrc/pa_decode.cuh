@@ -418,6 +418,8 @@ __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
         out[d] = Elem<T>::from(0.f);
         return;
     }
+    if (np == 1 && p.skip_single)
+        return;
     // global max of m over the partitions
     float M = -INFINITY;
     for (int q = d; q < np; q += D)

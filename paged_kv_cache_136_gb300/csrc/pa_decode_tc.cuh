@@ -38,11 +38,11 @@
 // with the 128-byte swizzle (shared-memory matrix descriptors).
 //
 // Split-K ("PagedAttention 在 vLLM 中的实现分析", section 7.3): items are
-// (partition of P tokens, head group) pairs dealt dynamically to a persistent
-// grid through an atomic counter.  A sequence with one partition writes its
-// output directly; otherwise each partition writes its unnormalised (o, m, l)
-// to the workspace and the last partition to finish (an arrival counter per
-// (sequence, head group)) merges them with the log-sum-exp rescale.
+// (partition of P tokens, head group) pairs dealt dynamically, longest first,
+// to a persistent grid through an atomic counter.  A sequence with one
+// partition writes its output directly; otherwise each partition writes its
+// unnormalised (o, m, l) to the workspace and the reduce kernel that follows
+// merges them with the log-sum-exp rescale.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -80,7 +80,6 @@ constexpr int kOffP = kOffQ + kStages * kQBytes;
 constexpr int kOffMisc = kOffP + 2 * kPBytes;
 
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagStop = 4;
-constexpr int kFusedMergeMax = 8;         // partitions merged in-kernel by the last arriver
 
 struct StageDesc {
     int s, group, part, nvalid, flags, nparts, pad0, pad1;
@@ -90,7 +89,6 @@ struct Misc {
     StageDesc desc[kStages];
     float red[2][4][kNQ];  // per-stage max, double-buffered by stage parity
     float red2[4][kNQ];    // normaliser sums at item end
-    float ml[kNQ * kFusedMergeMax][2]; // (m, l) of every partition being merged
     int bcast[4];
     uint32_t tmem_base;
     uint32_t pad;
@@ -108,13 +106,11 @@ struct TcParams {
     unsigned int *err;
     // split-K workspace (null in one-pass mode)
     uint32_t *hdr;               // [0] work counter, [1] total items
-    uint32_t *arrive;            // [B * num_groups] arrival counters
     const uint32_t *units;       // (s << 16) | partition
     float *ws_o;                 // [B, H, max_parts, 128]
     float *ws_ml;                // [B, H, max_parts, 2]
     int num_heads, num_kv_heads, num_groups, num_blocks, max_blocks;
     int part_tokens, max_parts, len_cap;
-    int fused_merge;             // split: last partition merges (else a reduce kernel follows)
     float qscale;
 };
 
@@ -622,12 +618,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < NV; ++n)
                 l[n] = (m->red2[0][n] + m->red2[1][n]) + (m->red2[2][n] + m->red2[3][n]);
             const size_t head0 = (size_t)d.s * p.num_heads + (size_t)d.group * NV;
-            if (!SPLIT || (p.fused_merge && d.nparts == 1)) {
+            if (!SPLIT || d.nparts == 1) {
                 T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
 #pragma unroll
                 for (int n = 0; n < NV; ++n)
                     out[n * kD + t] = Elem<T>::from(o_acc[n] / l[n]);
             } else {
+                // Partial state of this partition; the reduce kernel that
+                // follows merges the partitions of the sequence.
 #pragma unroll
                 for (int n = 0; n < NV; ++n) {
                     const size_t row = (head0 + n) * p.max_parts + d.part;
@@ -636,45 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.ws_ml[row * 2] = m_run[n];
                         p.ws_ml[row * 2 + 1] = l[n];
                     }
-                }
-                if (!p.fused_merge)
-                    continue; // the reduce kernel merges the partitions
-                __threadfence();
-                bar_sync(kBarEpi, kEpiThreads);
-                if (t == 0) {
-                    const uint32_t old = atomicAdd(p.arrive + d.s * p.num_groups + d.group, 1u);
-                    m->bcast[0] = (old == (uint32_t)(d.nparts - 1)) ? 1 : 0;
-                }
-                bar_sync(kBarEpi, kEpiThreads);
-                if (m->bcast[0]) {
-                    // Last partition of (s, group): merge every partition.  All
-                    // (m, l) pairs are fetched at once into shared memory, then
-                    // each thread sums its head_size row with independent loads.
-                    __threadfence();
-                    const int np = d.nparts; // <= kFusedMergeMax here
-                    for (int i = t; i < NV * np; i += kEpiThreads) {
-                        const size_t row = (head0 + i / np) * p.max_parts + i % np;
-                        m->ml[i][0] = __ldcg(p.ws_ml + row * 2);
-                        m->ml[i][1] = __ldcg(p.ws_ml + row * 2 + 1);
-                    }
-                    bar_sync(kBarEpi, kEpiThreads);
-                    T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
-#pragma unroll
-                    for (int n = 0; n < NV; ++n) {
-                        const size_t rg = (head0 + n) * p.max_parts;
-                        float M = -INFINITY;
-                        for (int q = 0; q < np; ++q)
-                            M = fmaxf(M, m->ml[n * np + q][0]);
-                        float num = 0.f, den = 0.f;
-#pragma unroll 4
-                        for (int q = 0; q < np; ++q) {
-                            const float w = ex2(m->ml[n * np + q][0] - M);
-                            den = fmaf(w, m->ml[n * np + q][1], den);
-                            num = fmaf(w, __ldcg(p.ws_o + (rg + q) * kD + t), num);
-                        }
-                        out[n * kD + t] = Elem<T>::from(num / den);
-                    }
-                    bar_sync(kBarEpi, kEpiThreads); // ml is reused by the next merge
                 }
             }
         }
@@ -688,42 +647,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Split-K plan: zero the work and arrival counters, list every
-// (sequence, partition) unit in sequence order, count the work items
-// (units x kv heads), and write zero rows for empty sequences.  One CTA.
+// Split-K plan (one CTA): zero the work counter, write zero
+// rows for empty sequences, and list every (sequence, partition) unit
+// longest first -- all full partitions, then each sequence's last, partial
+// partition in descending size (a counting sort over kPlanBuckets size
+// buckets) -- so the dynamically claimed work ends with the shortest items.
+// The item count (units x head groups) goes to hdr[1].
+constexpr int kPlanBuckets = 256;
+
 template <typename T>
 __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_lens, int B, int H,
-                                                           int Hkv, int part_tokens, int len_cap,
-                                                           uint32_t *hdr, uint32_t *arrive,
-                                                           uint32_t *units, T *out,
-                                                           unsigned int *err)
+                                                           int num_groups, int part_tokens,
+                                                           int len_cap, uint32_t *hdr,
+                                                           uint32_t *units,
+                                                           T *out, unsigned int *err)
 {
     __shared__ uint32_t warp_tot[32];
+    __shared__ uint32_t bucket[kPlanBuckets];
     __shared__ uint32_t carry_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < B * Hkv; i += blockDim.x)
-        arrive[i] = 0;
+    const int nwarps = blockDim.x >> 5;
+    for (int i = tid; i < kPlanBuckets; i += blockDim.x)
+        bucket[i] = 0;
     if (tid == 0) {
         hdr[0] = 0;
         carry_s = 0;
     }
     __syncthreads();
+    auto seq_len = [&](int s) {
+        int L = seq_lens[s];
+        if (L < 0 || L > len_cap) {
+            atomicOr(err, PA_DEVERR_SEQ_LEN_);
+            L = L < 0 ? 0 : len_cap;
+        }
+        return L;
+    };
+    // Size bucket of a last partition of `last` tokens: larger first.
+    auto size_bucket = [&](int last) {
+        const int b = (int)(((long long)(last - 1) * kPlanBuckets) / part_tokens);
+        return kPlanBuckets - 1 - (b < kPlanBuckets - 1 ? b : kPlanBuckets - 1);
+    };
+    // Pass 1: full partitions in sequence order; histogram of the last ones.
     for (int c0 = 0; c0 < B; c0 += blockDim.x) {
         const int s = c0 + tid;
-        uint32_t n = 0;
+        uint32_t nfull = 0;
         if (s < B) {
-            int L = seq_lens[s];
-            if (L < 0 || L > len_cap) {
-                atomicOr(err, PA_DEVERR_SEQ_LEN_);
-                L = L < 0 ? 0 : len_cap;
-            }
-            n = (uint32_t)((L + part_tokens - 1) / part_tokens);
-            if (L == 0)
+            const int L = seq_len(s);
+            const int n = (L + part_tokens - 1) / part_tokens;
+            if (n > 0) {
+                nfull = (uint32_t)(n - 1);
+                atomicAdd(&bucket[size_bucket(L - (n - 1) * part_tokens)], 1u);
+            } else {
                 for (int i = 0; i < H * 128; ++i)
                     out[(size_t)s * H * 128 + i] = Elem<T>::from(0.f);
+            }
         }
-        // block exclusive scan of n
-        uint32_t v = n;
+        uint32_t v = nfull;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, v, off);
@@ -734,7 +713,7 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
             warp_tot[warp] = v;
         __syncthreads();
         if (warp == 0) {
-            uint32_t w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+            uint32_t w = lane < nwarps ? warp_tot[lane] : 0;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xffffffffu, w, off);
@@ -744,16 +723,34 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
             warp_tot[lane] = w; // inclusive prefix over warps
         }
         __syncthreads();
-        const uint32_t base = carry_s + (warp ? warp_tot[warp - 1] : 0) + v - n;
-        for (uint32_t q = 0; q < n; ++q)
+        const uint32_t base = carry_s + (warp ? warp_tot[warp - 1] : 0) + v - nfull;
+        for (uint32_t q = 0; q < nfull; ++q)
             units[base + q] = ((uint32_t)s << 16) | q;
         __syncthreads();
         if (tid == 0)
-            carry_s += warp_tot[(blockDim.x >> 5) - 1];
+            carry_s += warp_tot[nwarps - 1];
         __syncthreads();
     }
-    if (tid == 0)
-        hdr[1] = carry_s * (uint32_t)Hkv;
+    // Bucket start offsets after the full partitions (buckets in size order).
+    if (tid == 0) {
+        uint32_t acc = carry_s;
+        for (int b = 0; b < kPlanBuckets; ++b) {
+            const uint32_t c = bucket[b];
+            bucket[b] = acc;
+            acc += c;
+        }
+        hdr[1] = acc * (uint32_t)num_groups;
+    }
+    __syncthreads();
+    // Pass 2: place each last partition in its bucket.
+    for (int s = tid; s < B; s += blockDim.x) {
+        const int L = seq_len(s);
+        const int n = (L + part_tokens - 1) / part_tokens;
+        if (n > 0) {
+            const uint32_t pos = atomicAdd(&bucket[size_bucket(L - (n - 1) * part_tokens)], 1u);
+            units[pos] = ((uint32_t)s << 16) | (uint32_t)(n - 1);
+        }
+    }
 }
 
 template <typename T, int BS, int G, int HG, bool SPLIT>

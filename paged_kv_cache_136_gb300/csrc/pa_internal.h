@@ -37,6 +37,7 @@ struct ReduceParams {
     int max_parts;
     int part_tokens;
     int len_cap;
+    int skip_single; // rows of one-partition sequences are already final
 };
 
 // Key of a decode kernel instantiation.

@@ -48,13 +48,13 @@ def test_status_strings(pa):
 
 
 def _expected_ws(B, H, D, L, P):
-    """Header 256 B, then arrival counters (B*H), the unit list (B*parts) and
-    the partial o (fp32 D) and (m, l) per (sequence, head, partition), each
-    region rounded up to 256 bytes."""
+    """Header 256 B, then the unit list (B*parts) and the partial o (fp32 D)
+    and (m, l) per (sequence, head, partition), each region rounded up to 256
+    bytes."""
     r = lambda x: -(-x // 256) * 256
     parts = max(1, -(-L // P))
     rows = B * H * parts
-    return 256 + r(B * H * 4) + r(B * parts * 4) + r(rows * D * 4) + r(rows * 2 * 4)
+    return 256 + r(B * parts * 4) + r(rows * D * 4) + r(rows * 2 * 4)
 
 
 def test_workspace_size(pa):
