@@ -52,6 +52,7 @@ WORKLOAD_TEXT = {
     "tiny": "tiny: 4 seqs {1,17,33,64}, 4/4 heads, head_size 64, block_size 16, fp16",
 }
 DECODE_SOURCES = ["paged_kv_cache_136_gb300/csrc/pa_decode.cuh",
+                  "paged_kv_cache_136_gb300/csrc/pa_decode_tc.cuh",
                   "paged_kv_cache_136_gb300/csrc/pa_ptx.cuh"]
 
 
@@ -164,6 +165,18 @@ def decode_launch_bytes(w, split: bool, partition: int) -> int:
         parts = int(((L + partition - 1) // partition).sum().item())
         b += 2 * parts * w.num_heads * (w.head_size + 2) * 4
     return b
+
+
+def decode_launches(w, split: bool, partition: int) -> int:
+    """Kernels one decode call launches: one-pass = 1; split-K = plan +
+    decode + (reduce when a sequence can span several partitions) for the
+    tensor-core path (head_size 128), decode + reduce otherwise."""
+    if not split:
+        return 1
+    msl = int(w.seq_lens.max().item())
+    if w.head_size == 128:
+        return 2 + (1 if msl > partition else 0)
+    return 2
 
 
 def reshape_launch_bytes(w) -> int:
@@ -363,8 +376,9 @@ def run_ours(args) -> dict | None:
                    "parallelism": f"replicas x{world}", "seed": args.seed},
         "seqs_per_s": round(seqs_all / (ms_max / 1e3), 1),
         "pct_hbm_peak": round(100.0 * value / peaks["hbm_gbs"], 2),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode_splitk (partition+reduce)" if split
-                     else "pa_decode", "achieved": round(achieved, 2),
+        "roofline": {"bound": "hbm", "kernel": ("pa_decode_splitk call (plan, decode and reduce "
+                                                "kernels together)") if split else "pa_decode",
+                     "achieved": round(achieved, 2),
                      "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": recorded_traffic(args.config, "splitk" if split else "onepass"),
@@ -374,14 +388,72 @@ def run_ours(args) -> dict | None:
                     "algorithmic_bytes_per_launch": reshape_launch_bytes(w)},
         "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": K * (3 if split else 2),
+        "gpu_launches": K * (1 + decode_launches(w, split, P)),
         "clocks": clk,
         "device_error_flags": flags,
         "kernel_source": source_digest(),
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if world == 1 and args.workloads:
+        del w, ws, out, host, out_h
+        torch.cuda.empty_cache()
+        line["workloads"] = [other_workload(name, args, peaks["hbm_gbs"])
+                             for name in args.workloads.split(",") if name]
     return line
+
+
+def other_workload(name: str, args, peak_gbs: float) -> dict:
+    """Short device-resident measurement of another workload through the same
+    step (cache write + split-K decode), reported beside the main line."""
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    w = wl.make(name, device="cuda")
+    out = torch.empty_like(w.q)
+    msl = int(w.seq_lens.max().item())
+    P = args.partition
+    ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                                        msl, P), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                            w.block_size, msl, ws, P)
+
+    for _ in range(5):
+        step()
+    n = max(3, args.workload_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(n):
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        ev[i][0].record(stream)
+        pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                            w.block_size, msl, ws, P)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    kvb = kv_bytes(w)
+    res = {"name": name, "workload": WORKLOAD_TEXT[name], "decode": "pa_decode_splitk",
+           "partition_size": P, "steps": n, "kv_bytes_per_step": kvb,
+           "step_gbs": round(kvb / ms / 1e6, 2), "ms_per_step": round(ms, 5),
+           "decode_gbs": round(decode_launch_bytes(w, True, P) / dec_ms / 1e6, 2),
+           "decode_frac": round(decode_launch_bytes(w, True, P) / dec_ms / 1e6 / peak_gbs, 4),
+           "seqs_per_s": round(w.num_seqs / (ms / 1e3), 1)}
+    if name == "prefix":
+        ub = w.unique_kv_bytes()
+        res["unique_kv_bytes_per_step"] = ub
+        res["unique_step_gbs"] = round(ub / ms / 1e6, 2)
+    del w, ws, out
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -439,6 +511,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200,
                     help="steps in the end-to-end (host buffers) measurement")
+    ap.add_argument("--workloads", default="gqa8b,long,prefix,tiny",
+                    help="other workloads measured briefly beside the main line ('' for none)")
+    ap.add_argument("--workload-steps", type=int, default=50)
     return ap.parse_args(argv)
 
 
