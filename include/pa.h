@@ -118,7 +118,8 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache,
                     void *stream);
 
 /*
- * Bytes of workspace pa_decode_splitk needs for these sizes: partial states
+ * Bytes of workspace pa_decode_splitk needs for these sizes: a work-list
+ * header, one list entry per (sequence, partition), and the partial states
  * (running max, normaliser, unnormalised head_size-vector, fp32) for every
  * (sequence, query head, partition), partitions = ceil(max_seq_len /
  * partition_size).  Returns 0 for invalid sizes.
@@ -200,6 +201,15 @@ pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int blo
  * read fails.
  */
 pa_status pa_device_errors(unsigned int *flags, int clear);
+
+/*
+ * Self-test of the in-kernel failure detection: launches one thread that
+ * waits on a barrier phase nothing will complete.  The wait gives up after
+ * its time limit (about 2 s), the kernel sets PA_DEVERR_TIMEOUT in the device
+ * error word and returns; the CUDA context stays usable.  No counterpart on
+ * the pages (it checks the library's own bounded-wait rule).
+ */
+pa_status pa_selftest_wait_timeout(void *stream);
 
 /* Static, human-readable name of a status code. */
 const char *pa_status_string(pa_status status);

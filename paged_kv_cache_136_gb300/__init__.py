@@ -19,7 +19,7 @@ __all__ = [
     "PAError", "lib_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
     "pa_decode_splitk_workspace_size", "pa_decode_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "pa_validate_tables", "pa_validate_slots",
-    "pa_device_errors", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
+    "pa_device_errors", "pa_selftest_wait_timeout", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
 
@@ -57,6 +57,8 @@ _lib.pa_validate_slots.restype = _I
 _lib.pa_validate_slots.argtypes = [_P, _I, _I, _I]
 _lib.pa_device_errors.restype = _I
 _lib.pa_device_errors.argtypes = [ctypes.POINTER(_U), _I]
+_lib.pa_selftest_wait_timeout.restype = _I
+_lib.pa_selftest_wait_timeout.argtypes = [_P]
 _lib.pa_status_string.restype = ctypes.c_char_p
 _lib.pa_status_string.argtypes = [_I]
 _lib.pa_version.restype = _I
@@ -221,6 +223,12 @@ def pa_validate_slots(slot_mapping: torch.Tensor, block_size: int, num_blocks: i
     sm = slot_mapping.detach().to("cpu", torch.int64).contiguous()
     return _lib.pa_validate_slots(ctypes.c_void_p(sm.data_ptr()), int(sm.numel()), block_size,
                                   num_blocks)
+
+
+def pa_selftest_wait_timeout(stream=None) -> None:
+    """Run the bounded-wait self-test kernel (a wait nothing completes); it
+    sets DEVERR_TIMEOUT after ~2 s and returns."""
+    _check(_lib.pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
 
 
 def pa_device_errors(clear: bool = True) -> int:

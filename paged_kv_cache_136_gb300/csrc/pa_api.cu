@@ -218,6 +218,19 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier phase that
+// nothing completes.  The wait gives up after its time limit, the kernel sets
+// PA_DEVERR_TIMEOUT and returns.
+__global__ void wait_timeout_selftest_kernel(unsigned int *err)
+{
+    __shared__ uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait(&bar, 0))
+        atomicOr(err, PA_DEVERR_TIMEOUT);
+    mbar_arrive(&bar); // complete the phase so the barrier is left consistent
+}
+
 } // namespace pa
 
 using namespace pa;
@@ -580,6 +593,16 @@ pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int blo
             return PA_ERR_OUT_OF_RANGE;
     }
     return PA_OK;
+}
+
+pa_status pa_selftest_wait_timeout(void *stream)
+{
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_device_errors(unsigned int *flags, int clear)

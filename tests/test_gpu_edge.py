@@ -145,3 +145,29 @@ def test_deterministic_and_batch_invariant(pa, split):
     c = _decode(pa, ws, split, max_seq_len=int(w.seq_lens.max().item()))
     torch.cuda.synchronize()
     assert torch.equal(c.view(torch.int16), a[sub].view(torch.int16))
+
+
+def test_bounded_wait_times_out_and_context_survives(pa):
+    """A wait that nothing completes gives up, reports PA_DEVERR_TIMEOUT, and
+    the context keeps working."""
+    pa.pa_device_errors(clear=True)
+    pa.pa_selftest_wait_timeout()
+    assert pa.pa_device_errors(clear=True) & pa.DEVERR_TIMEOUT
+    w = wl.make("tiny", device="cuda", poison=True)
+    out = _decode(pa, w, False)
+    torch.cuda.synchronize()
+    check_attention(out, oracle_decode(w), what="after timeout self-test")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("P", [64, 192, 320])
+def test_tensor_core_one_head_per_cta_and_ragged_partitions(pa, P):
+    """3 kv heads cannot be grouped, so the tensor-core kernel runs one kv
+    head per CTA (128-token stages); partitions that are not a multiple of
+    the stage end in partial stages."""
+    w = wl.make("gqa8b", device="cuda", poison=True, lengths=[1, 100, 129, 700, 1031],
+                num_heads=12, num_kv_heads=3, seed=40 + P)
+    ref = oracle_decode(w)
+    check_attention(_decode(pa, w, True, partition_size=P), ref, what=f"Hkv=3 split P={P}")
+    check_attention(_decode(pa, w, False), ref, what="Hkv=3 one-pass")
+    assert pa.pa_device_errors(clear=True) == 0
