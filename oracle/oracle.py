@@ -103,6 +103,8 @@ class Oracle:
         lib.or_online_softmax.argtypes = [P, P, P, P, P, i32, i32, i32]
         lib.or_merge_partials.restype = i32
         lib.or_merge_partials.argtypes = [P, P, P, P, i32, i32]
+        lib.or_copy_blocks.restype = i32
+        lib.or_copy_blocks.argtypes = [P, P, i32, i32, i32, i32, i32]
         lib.or_check_tables.restype = i32
         lib.or_check_tables.argtypes = [P, P, i32, i32, i32, i32]
         self.lib = lib
@@ -197,6 +199,15 @@ class Oracle:
         out = np.empty(d, np.float64)
         _check(self.lib.or_merge_partials(_ptr(out), _ptr(m), _ptr(l), _ptr(o), parts, d))
         return out
+
+    def copy_blocks(self, cache, mapping):
+        """Return a copy of ``cache`` (uint16 [2, NB, bs, Hkv, D]) after copying
+        block src -> dst for each (src, dst) row of ``mapping`` in order."""
+        c = np.array(_u16(cache), copy=True)
+        _, nb, bs, hkv, d = c.shape
+        mp = np.ascontiguousarray(mapping, dtype=np.int64).reshape(-1, 2)
+        _check(self.lib.or_copy_blocks(_ptr(c), _ptr(mp), mp.shape[0], nb, bs, hkv, d))
+        return c
 
     def check_tables(self, block_tables, seq_lens, block_size: int, num_blocks: int) -> int:
         bt = np.ascontiguousarray(block_tables, dtype=np.int32)

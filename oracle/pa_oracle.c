@@ -481,6 +481,33 @@ int or_merge_partials(double *out, const double *m, const double *l, const doubl
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Copy-on-write block copy ("Paged attention", k4i.top, section            */
+/* "并行采样中的 copy-on-write": a new block receives a copy of the shared  */
+/* block before the writer's token goes into it).                           */
+/* ------------------------------------------------------------------------ */
+
+/* For each pair i, copy every key and value row of physical block
+ * mapping[2i] into physical block mapping[2i+1] of the pool
+ * [2, num_blocks, block_size, num_kv_heads, head_size].  Pairs are applied in
+ * order.  Ids outside [0, num_blocks) are an error. */
+int or_copy_blocks(uint16_t *cache, const int64_t *mapping, int num_pairs, int num_blocks,
+                   int block_size, int num_kv_heads, int head_size)
+{
+    const size_t block_elems = (size_t)block_size * num_kv_heads * head_size;
+    for (int i = 0; i < num_pairs; i++) {
+        int64_t src = mapping[2 * i], dst = mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return OR_ERR_BLOCK_ID;
+        for (int plane = 0; plane < 2; plane++) {
+            const size_t base = (size_t)plane * num_blocks * block_elems;
+            memmove(cache + base + (size_t)dst * block_elems,
+                    cache + base + (size_t)src * block_elems, block_elems * sizeof(uint16_t));
+        }
+    }
+    return OR_OK;
+}
+
 /* Host check of the caller preconditions the CUDA library documents:
  * 0 <= seq_lens[s] <= max_blocks_per_seq * block_size and every block id a
  * sequence uses lies in [0, num_blocks).  Returns OR_OK or an error code. */

@@ -38,6 +38,8 @@ MUTANTS = [
     ("ties_away_from_zero", "double n = nearbyint(a / quantum);", "double n = round(a / quantum);"),
     ("online_merge_skips_rescale", "l = c_old * l + c_new * lj;", "l = l + c_new * lj;"),
     ("partials_unweighted_denominator", "denom += exp(m[p] - M) * l[p];", "denom += l[p];"),
+    ("copy_wrong_plane", "const size_t base = (size_t)plane * num_blocks * block_elems;",
+     "const size_t base = 0;"),
     ("max_misses_first_score", "double m = a[0];\n    for (int t = 1; t < L; t++)",
      "double m = a[L - 1] - 50.0;\n    for (int t = 1; t < L; t++)"),
 ]

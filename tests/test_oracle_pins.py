@@ -466,3 +466,59 @@ def test_output_rounding_matches_numpy_half(orc):
     q, cache, bt, sl, NB, _ = _case(rng, [33, 64], 4, 4, 64, 16, FP16, contiguous=False)
     out = orc.decode(q, cache, bt, sl, 4, 16, 0.125, FP16)
     assert np.array_equal(orc.round_to(out, FP16), out.astype(np.float16).view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# Copy-on-write block copy
+# ---------------------------------------------------------------------------
+
+def test_copy_blocks_matches_array_assignment(orc):
+    rng = np.random.default_rng(30)
+    cache = _rand_bits(rng, (2, 12, 16, 3, 32), BF16)
+    mapping = np.array([[2, 9], [6, 11], [0, 4]], np.int64)
+    got = orc.copy_blocks(cache, mapping)
+    ref = cache.copy()
+    for src, dst in mapping:
+        ref[:, dst] = ref[:, src]
+    assert np.array_equal(got, ref)
+    untouched = [b for b in range(12) if b not in (9, 11, 4)]
+    assert np.array_equal(got[:, untouched], cache[:, untouched])
+
+
+def test_copy_on_write_keeps_the_other_candidates_unchanged(orc):
+    """The page's parallel-sampling example: prompt blocks 2 and 6 shared by
+    three candidates (ref count 3); candidate 2 must write into block 6, so
+    block 6 is copied to a fresh block 11, candidate 2's table is repointed
+    and the token written there.  Candidates 1 and 3 read what they read
+    before; candidate 2 reads the copy plus its token."""
+    rng = np.random.default_rng(31)
+    bs, hkv, d, NB = 16, 2, 64, 16
+    cache = _rand_bits(rng, (2, NB, bs, hkv, d), FP16)
+    q = _rand_bits(rng, (3, 4, d), FP16)
+    tables = np.array([[2, 6], [2, 6], [2, 6]], np.int32)
+    lens = np.array([26, 26, 26], np.int32)               # block 6 holds 10 tokens
+    before = orc.decode(q, cache, tables, lens, hkv, bs, 0.125, FP16)
+    cow = orc.copy_blocks(cache, np.array([[6, 11]], np.int64))
+    tables2 = tables.copy()
+    tables2[1, 1] = 11
+    new_k = _rand_bits(rng, (1, hkv, d), FP16)
+    new_v = _rand_bits(rng, (1, hkv, d), FP16)
+    slot = orc.slot_of_token(tables2[1], 26, bs)          # token 26 -> block 11, offset 10
+    assert slot == 11 * bs + 10
+    cow = orc.reshape_and_cache(new_k, new_v, cow, np.array([slot], np.int64), bs)
+    lens2 = np.array([26, 27, 26], np.int32)
+    after = orc.decode(q, cow, tables2, lens2, hkv, bs, 0.125, FP16)
+    assert np.array_equal(after[[0, 2]], before[[0, 2]])
+    # candidate 2 = its private copy of the prompt + the new token
+    private = cache.copy()
+    private[:, 11] = cache[:, 6]
+    private = orc.reshape_and_cache(new_k, new_v, private, np.array([slot], np.int64), bs)
+    assert np.array_equal(after[1], orc.decode(q, private, tables2, lens2, hkv, bs, 0.125,
+                                               FP16)[1])
+    assert not np.array_equal(after[1], before[1])
+
+
+def test_copy_blocks_rejects_bad_ids(orc):
+    cache = np.zeros((2, 4, 16, 1, 8), np.uint16)
+    with pytest.raises(OracleError):
+        orc.copy_blocks(cache, np.array([[0, 4]], np.int64))
