@@ -403,12 +403,54 @@ def run_ours(args) -> dict | None:
     return line
 
 
+def copy_blocks_workload(args, peak_gbs: float) -> dict:
+    """Copy-on-write block copies on the mha7b pool: a quarter of the pool's
+    blocks copied into another quarter per launch (disjoint sources and
+    destinations, shuffled), timed per launch with CUDA events.  Bytes per
+    pair: the K and V planes of one block read and written."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    w = wl.make("mha7b", device="cuda", seed=args.seed)
+    nb = w.num_blocks
+    n = nb // 4
+    ids = np.random.default_rng(args.seed).permutation(nb)
+    mapping = torch.from_numpy(np.stack([ids[:n], ids[n:2 * n]], 1).astype(np.int64)).cuda()
+    plane = w.block_size * w.num_kv_heads * w.head_size * w.kv_cache.element_size()
+    nbytes = n * 2 * 2 * plane + mapping.numel() * 8
+    stream = torch.cuda.current_stream()
+    for _ in range(5):
+        pa.pa_copy_blocks(w.kv_cache, mapping, w.block_size)
+    k = max(3, args.workload_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(k)]
+    torch.cuda.synchronize()
+    for i in range(k):
+        ev[i][0].record(stream)
+        pa.pa_copy_blocks(w.kv_cache, mapping, w.block_size)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    res = {"name": "copy_blocks", "call": "pa_copy_blocks",
+           "workload": f"{n} (src, dst) block pairs of the mha7b pool ({nb} blocks, "
+                       f"{plane} B per K or V block plane), disjoint, shuffled",
+           "launches": k, "bytes_per_launch": nbytes, "ms_per_launch": round(ms, 5),
+           "gbs": round(nbytes / ms / 1e6, 2),
+           "frac": round(nbytes / ms / 1e6 / peak_gbs, 4),
+           "device_error_flags": pa.pa_device_errors(clear=True)}
+    del w, mapping
+    torch.cuda.empty_cache()
+    return res
+
+
 def other_workload(name: str, args, peak_gbs: float) -> dict:
     """Short device-resident measurement of another workload through the same
     step (cache write + split-K decode), reported beside the main line."""
     import torch
     import paged_kv_cache_136_gb300 as pa
     import workload as wl
+    if name == "copy_blocks":
+        return copy_blocks_workload(args, peak_gbs)
     w = wl.make(name, device="cuda")
     out = torch.empty_like(w.q)
     msl = int(w.seq_lens.max().item())
@@ -511,7 +553,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200,
                     help="steps in the end-to-end (host buffers) measurement")
-    ap.add_argument("--workloads", default="gqa8b,long,prefix,tiny",
+    ap.add_argument("--workloads", default="gqa8b,long,prefix,tiny,copy_blocks",
                     help="other workloads measured briefly beside the main line ('' for none)")
     ap.add_argument("--workload-steps", type=int, default=50)
     return ap.parse_args(argv)

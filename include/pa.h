@@ -6,6 +6,7 @@
  *   pa_reshape_and_cache  scatter each new token's key/value into the pool
  *   pa_decode             one-pass paged decode attention
  *   pa_decode_splitk      partitioned decode attention + log-sum-exp reduce
+ *   pa_copy_blocks        copy whole blocks (the device half of copy-on-write)
  *
  * Data layout (all tensors contiguous, row-major, caller-owned):
  *
@@ -176,6 +177,36 @@ pa_status pa_decode_splitk_noalloc(void *out, const void *q, const void *kv_cach
                                    int block_size, int num_blocks, int max_blocks_per_seq,
                                    float scale, pa_dtype dtype, int max_seq_len,
                                    int partition_size, void *stream);
+
+/*
+ * Copy whole blocks of the pool, for copy-on-write (k4i.top "paged
+ * attention" explainer, section on copy-on-write in parallel sampling and its
+ * Figure 3; the ATB PagedAttention blog's Copy-on-Write section: when a
+ * sequence must write into a block it shares, a fresh block receives a copy of
+ * the shared block, the sequence's table is repointed to it, and the new token
+ * is written there).
+ *
+ *   kv_cache       the pool, updated in place: for each pair i, the key rows
+ *                  and the value rows of block block_mapping[2i] are copied
+ *                  into block block_mapping[2i+1].
+ *   block_mapping  int64 [num_pairs, 2] (src, dst), device memory.  No dst
+ *                  may repeat or also appear as a src in the same call (the
+ *                  pairs are copied concurrently); pa_validate_block_mapping
+ *                  checks this on a host copy.  Ids outside [0, num_blocks)
+ *                  are skipped and flagged (PA_DEVERR_BLOCK_ID).
+ * num_pairs == 0 is a no-op; num_pairs <= 65535.
+ */
+pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
+                         int num_blocks, int block_size, int num_kv_heads, int head_size,
+                         pa_dtype dtype, void *stream);
+
+/*
+ * Host-side check of a HOST copy of a block mapping for pa_copy_blocks: ids in
+ * [0, num_blocks), destinations distinct, no destination also a source.
+ * Returns PA_OK, PA_ERR_OUT_OF_RANGE, or PA_ERR_INVALID_ARG.  No CUDA call.
+ */
+pa_status pa_validate_block_mapping(const int64_t *block_mapping, int num_pairs,
+                                    int num_blocks);
 
 /*
  * Host-side check of the decode preconditions on HOST copies of the tables:

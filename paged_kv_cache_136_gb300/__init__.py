@@ -19,7 +19,8 @@ __all__ = [
     "PAError", "lib_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
     "pa_decode_splitk_workspace_size", "pa_decode_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "pa_validate_tables", "pa_validate_slots",
-    "pa_device_errors", "pa_selftest_wait_timeout", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
+    "pa_device_errors", "pa_selftest_wait_timeout", "pa_copy_blocks",
+    "pa_validate_block_mapping", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
 
@@ -57,6 +58,10 @@ _lib.pa_validate_slots.restype = _I
 _lib.pa_validate_slots.argtypes = [_P, _I, _I, _I]
 _lib.pa_device_errors.restype = _I
 _lib.pa_device_errors.argtypes = [ctypes.POINTER(_U), _I]
+_lib.pa_copy_blocks.restype = _I
+_lib.pa_copy_blocks.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _P]
+_lib.pa_validate_block_mapping.restype = _I
+_lib.pa_validate_block_mapping.argtypes = [_P, _I, _I]
 _lib.pa_selftest_wait_timeout.restype = _I
 _lib.pa_selftest_wait_timeout.argtypes = [_P]
 _lib.pa_status_string.restype = ctypes.c_char_p
@@ -223,6 +228,31 @@ def pa_validate_slots(slot_mapping: torch.Tensor, block_size: int, num_blocks: i
     sm = slot_mapping.detach().to("cpu", torch.int64).contiguous()
     return _lib.pa_validate_slots(ctypes.c_void_p(sm.data_ptr()), int(sm.numel()), block_size,
                                   num_blocks)
+
+
+def pa_copy_blocks(kv_cache: torch.Tensor, block_mapping: torch.Tensor, block_size: int,
+                   stream=None) -> None:
+    """Copy the K and V rows of block src into block dst for every (src, dst)
+    row of ``block_mapping`` (CUDA int64 [n, 2]), the device half of
+    copy-on-write."""
+    nb, hkv, d = _pool_dims(kv_cache, block_size)
+    if kv_cache.dtype not in _DTYPE:
+        raise ValueError("dtype must be float16 or bfloat16")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or \
+            block_mapping.shape[1] != 2 or not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be contiguous int64 [n, 2]")
+    n = int(block_mapping.shape[0])
+    if n == 0:
+        return
+    _check(_lib.pa_copy_blocks(_dev(kv_cache, "kv_cache"), _dev(block_mapping, "block_mapping"),
+                               n, nb, block_size, hkv, d, _DTYPE[kv_cache.dtype],
+                               _stream(stream)), "pa_copy_blocks")
+
+
+def pa_validate_block_mapping(block_mapping: torch.Tensor, num_blocks: int) -> int:
+    m = block_mapping.detach().to("cpu", torch.int64).contiguous()
+    return _lib.pa_validate_block_mapping(ctypes.c_void_p(m.data_ptr()), int(m.shape[0]),
+                                          num_blocks)
 
 
 def pa_selftest_wait_timeout(stream=None) -> None:

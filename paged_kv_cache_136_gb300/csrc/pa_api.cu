@@ -218,6 +218,33 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Copy-on-write block copy (k4i.top "paged attention" explainer, parallel
+// sampling copy-on-write section: a fresh block receives a copy of the shared
+// block before the writer's token goes into it).  Grid: x = chunks of a block plane, y = pair;
+// each thread moves 16-byte vectors of both planes.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4 *__restrict__ cache, const int64_t *__restrict__ mapping,
+                       int num_blocks, int64_t block_vecs, unsigned int *err)
+{
+    const int64_t src = mapping[2 * (int64_t)blockIdx.y];
+    const int64_t dst = mapping[2 * (int64_t)blockIdx.y + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            atomicOr(err, PA_DEVERR_BLOCK_ID);
+        return;
+    }
+    const int64_t plane = (int64_t)num_blocks * block_vecs;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < block_vecs;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 k = cache[src * block_vecs + i];
+        const uint4 v = cache[plane + src * block_vecs + i];
+        cache[dst * block_vecs + i] = k;
+        cache[plane + dst * block_vecs + i] = v;
+    }
+}
+
 // Self-test of the bounded waits: one thread waits on an mbarrier phase that
 // nothing completes.  The wait gives up after its time limit, the kernel sets
 // PA_DEVERR_TIMEOUT and returns.
@@ -592,6 +619,56 @@ pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int blo
         if (s >= cap || !seen.insert(s).second)
             return PA_ERR_OUT_OF_RANGE;
     }
+    return PA_OK;
+}
+
+pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
+                         int num_blocks, int block_size, int num_kv_heads, int head_size,
+                         pa_dtype dtype, void *stream)
+{
+    if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_FP16 && dtype != PA_BF16)
+        return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!kv_cache || !block_mapping || !aligned(kv_cache, 16) || !aligned(block_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)block_size * num_kv_heads * head_size * 2;
+    if (block_bytes % 16)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs > 65535)
+        return PA_ERR_UNSUPPORTED;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    const int64_t block_vecs = block_bytes / 16;
+    const int64_t per_cta = 256 * 4; // four vectors per thread and plane
+    const unsigned gx = (unsigned)((block_vecs + per_cta - 1) / per_cta);
+    copy_blocks_kernel<<<dim3(gx, num_pairs), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(kv_cache), block_mapping, num_blocks, block_vecs, err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_validate_block_mapping(const int64_t *block_mapping, int num_pairs,
+                                    int num_blocks)
+{
+    if (num_pairs < 0 || num_blocks <= 0 || (num_pairs > 0 && !block_mapping))
+        return PA_ERR_INVALID_ARG;
+    std::unordered_set<int64_t> dsts, srcs;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int64_t src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return PA_ERR_OUT_OF_RANGE;
+        if (!dsts.insert(dst).second)
+            return PA_ERR_OUT_OF_RANGE;
+        srcs.insert(src);
+    }
+    for (int64_t d : dsts)
+        if (srcs.count(d))
+            return PA_ERR_OUT_OF_RANGE;
     return PA_OK;
 }
 

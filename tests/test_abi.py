@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
               "pa_decode_splitk_workspace_size", "pa_validate_tables", "pa_validate_slots",
-              "pa_device_errors", "pa_status_string", "pa_version"):
+              "pa_device_errors", "pa_status_string", "pa_version", "pa_copy_blocks",
+              "pa_validate_block_mapping", "pa_selftest_wait_timeout"):
         assert n in names
 
 
@@ -167,3 +168,23 @@ def test_import_fails_loudly_without_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                        cwd=str(tmp_path))
     assert r.returncode != 0 and "ImportError" in r.stderr and "libpa.so" in r.stderr
+
+
+def test_validate_block_mapping(pa):
+    import torch
+    ok = torch.tensor([[2, 9], [6, 11]])
+    assert pa.pa_validate_block_mapping(ok, 12) == 0
+    assert pa.pa_validate_block_mapping(torch.tensor([[2, 9], [6, 9]]), 12) == 5   # dst twice
+    assert pa.pa_validate_block_mapping(torch.tensor([[2, 9], [9, 11]]), 12) == 5  # dst is a src
+    assert pa.pa_validate_block_mapping(torch.tensor([[2, 12]]), 12) == 5          # out of range
+    assert pa.pa_validate_block_mapping(torch.tensor([[3, 4], [3, 5]]), 12) == 0   # fork: src twice
+
+
+def test_copy_blocks_rejects_bad_arguments(pa):
+    lib = _raw(pa)
+    f = lib.pa_copy_blocks
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    assert f(FAKE, FAKE, 3, 10, 16, 2, 64, 7, None) == 2      # dtype
+    assert f(0, FAKE, 3, 10, 16, 2, 64, 0, None) == 1         # null pool
+    assert f(FAKE, FAKE, 0, 10, 16, 2, 64, 0, None) == 0      # nothing to copy

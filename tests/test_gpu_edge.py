@@ -171,3 +171,58 @@ def test_tensor_core_one_head_per_cta_and_ragged_partitions(pa, P):
     check_attention(_decode(pa, w, True, partition_size=P), ref, what=f"Hkv=3 split P={P}")
     check_attention(_decode(pa, w, False), ref, what="Hkv=3 one-pass")
     assert pa.pa_device_errors(clear=True) == 0
+
+
+# ---------------------------------------------------------------------------
+# Copy-on-write block copy
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["mha7b", "gqa8b"])
+def test_copy_blocks_bit_exact(pa, name):
+    from oracle.oracle import get
+    w = wl.make(name, device="cuda", poison=True, num_seqs=8, seed=50)
+    rng = np.random.default_rng(51)
+    ids = rng.permutation(w.num_blocks)
+    n = min(300, w.num_blocks // 2)
+    mapping = torch.from_numpy(np.stack([ids[:n], ids[n:2 * n]], 1).astype(np.int64)).cuda()
+    assert pa.pa_validate_block_mapping(mapping, w.num_blocks) == 0
+    ref = get().copy_blocks(wl.bits(w.kv_cache), mapping.cpu().numpy())
+    pa.pa_copy_blocks(w.kv_cache, mapping, w.block_size)
+    torch.cuda.synchronize()
+    assert np.array_equal(wl.bits(w.kv_cache), ref)
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_copy_blocks_bad_id_is_skipped_and_flagged(pa):
+    w = wl.make("tiny", device="cuda", seed=52)
+    before = w.kv_cache.clone()
+    mapping = torch.tensor([[w.num_blocks + 3, 0], [1, -1]], dtype=torch.int64, device="cuda")
+    pa.pa_copy_blocks(w.kv_cache, mapping, w.block_size)
+    assert pa.pa_device_errors(clear=True) & pa.DEVERR_BLOCK_ID
+    assert torch.equal(w.kv_cache.view(torch.int16), before.view(torch.int16))
+
+
+def test_copy_on_write_step_on_gpu(pa):
+    """Fork, copy, repoint, write, decode: the GPU matches the oracle and the
+    sequences that kept the shared block still read the original."""
+    w = wl.make("gqa8b", device="cuda", poison=True, lengths=[40, 40, 40], seed=53)
+    bs = w.block_size
+    shared = w.block_tables[0].clone()
+    tables = shared.repeat(3, 1).contiguous()            # three candidates share the prompt
+    w.q[2].copy_(w.q[0])                                 # candidates 0 and 2 stay identical
+    w.block_tables = tables
+    free = int(w.num_blocks - 1)                         # a block no table uses
+    used = set(tables.flatten().tolist())
+    while free in used:
+        free -= 1
+    last = int(tables[1, (40 - 1) // bs].item())
+    mapping = torch.tensor([[last, free]], dtype=torch.int64, device="cuda")
+    pa.pa_copy_blocks(w.kv_cache, mapping, bs)
+    tables[1, (40 - 1) // bs] = free
+    w.seq_lens = torch.tensor([40, 41, 40], dtype=torch.int32, device="cuda")
+    slot = torch.tensor([-1, free * bs + 40 % bs, -1], dtype=torch.int64, device="cuda")
+    pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, slot, bs)
+    out = _decode(pa, w, True, partition_size=64)
+    torch.cuda.synchronize()
+    check_attention(out, oracle_decode(w), what="copy-on-write step")
+    assert torch.equal(out[0].view(torch.int16), out[2].view(torch.int16))
