@@ -105,6 +105,11 @@ class Oracle:
         lib.or_merge_partials.argtypes = [P, P, P, P, i32, i32]
         lib.or_copy_blocks.restype = i32
         lib.or_copy_blocks.argtypes = [P, P, i32, i32, i32, i32, i32]
+        lib.or_prefill.restype = i32
+        lib.or_prefill.argtypes = [P, P, P, P, P, i64, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                   dbl, i32, i32, P, i64, i32]
+        lib.or_merge_attn_states.restype = i32
+        lib.or_merge_attn_states.argtypes = [P, P, P, P, P, P, i64, i32]
         lib.or_check_tables.restype = i32
         lib.or_check_tables.argtypes = [P, P, i32, i32, i32, i32]
         self.lib = lib
@@ -208,6 +213,57 @@ class Oracle:
         mp = np.ascontiguousarray(mapping, dtype=np.int64).reshape(-1, 2)
         _check(self.lib.or_copy_blocks(_ptr(c), _ptr(mp), mp.shape[0], nb, bs, hkv, d))
         return c
+
+    def prefill(self, q, cache, block_tables, seq_lens, query_start_loc, num_kv_heads: int,
+                block_size: int, scale: float, dtype: int, causal: bool = True, items=None,
+                nthreads: int | None = None, block_table_stride: int | None = None,
+                max_blocks_per_seq: int | None = None):
+        """fp64 attention of the packed query rows q [T, H, D] to each request's
+        paged keys; returns (out [T, H, D], lse [T, H]).  ``items`` (token * H +
+        head) limits the rows computed; the other rows are NaN.  The block table
+        may be a 1-D buffer read with an explicit row stride."""
+        qb = _u16(q)
+        cb = _u16(cache)
+        t, h, d = qb.shape
+        nb = cb.shape[1]
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        if block_table_stride is None:
+            block_table_stride = bt.shape[1]
+        if max_blocks_per_seq is None:
+            max_blocks_per_seq = block_table_stride
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+        assert qsl.size == sl.size + 1 and int(qsl[-1]) == t
+        out = np.full((t, h, d), np.nan, dtype=np.float64)
+        lse = np.full((t, h), np.nan, dtype=np.float64)
+        if items is not None:
+            it = np.ascontiguousarray(items, dtype=np.int64)
+            itp, nit = _ptr(it), it.size
+        else:
+            itp, nit = None, 0
+        if nthreads is None:
+            nthreads = os.cpu_count() or 1
+        _check(self.lib.or_prefill(_ptr(out), _ptr(lse), _ptr(qb), _ptr(cb), _ptr(bt),
+                                   int(block_table_stride), _ptr(sl), _ptr(qsl), sl.size, h,
+                                   num_kv_heads, d, block_size, nb, int(max_blocks_per_seq),
+                                   float(scale), 1 if causal else 0, dtype, itp, nit,
+                                   int(nthreads)))
+        return out, lse
+
+    def merge_attn_states(self, o_a, lse_a, o_b, lse_b):
+        """Merge two partial attention results given with their log-sum-exps:
+        o_x [..., D], lse_x [...]; returns (out, lse)."""
+        o_a = np.ascontiguousarray(o_a, dtype=np.float64)
+        o_b = np.ascontiguousarray(o_b, dtype=np.float64)
+        lse_a = np.ascontiguousarray(lse_a, dtype=np.float64)
+        lse_b = np.ascontiguousarray(lse_b, dtype=np.float64)
+        assert o_a.shape == o_b.shape and lse_a.shape == lse_b.shape == o_a.shape[:-1]
+        d = o_a.shape[-1]
+        out = np.empty_like(o_a)
+        lse = np.empty_like(lse_a)
+        _check(self.lib.or_merge_attn_states(_ptr(out), _ptr(lse), _ptr(o_a), _ptr(lse_a),
+                                             _ptr(o_b), _ptr(lse_b), lse_a.size, d))
+        return out, lse
 
     def check_tables(self, block_tables, seq_lens, block_size: int, num_blocks: int) -> int:
         bt = np.ascontiguousarray(block_tables, dtype=np.int32)

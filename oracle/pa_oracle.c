@@ -34,7 +34,8 @@
  *     grouped-query groups);
  *   - seq_lens[s] counts every cached token of sequence s, the newest included;
  *   - seq_lens[s] == 0 gives an all-zero output row;
- *   - scale is an explicit argument (the configs use 1/sqrt(head_size)).
+ *   - scale is an explicit argument (the configs use 1/sqrt(head_size));
+ *   - the prefill readings are listed above or_prefill.
  */
 #include <math.h>
 #include <pthread.h>
@@ -504,6 +505,247 @@ int or_copy_blocks(uint16_t *cache, const int64_t *mapping, int num_pairs, int n
             memmove(cache + base + (size_t)dst * block_elems,
                     cache + base + (size_t)src * block_elems, block_elems * sizeof(uint16_t));
         }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Prefill and chunked prefill over the paged cache (chen3feng vLLM          */
+/* analysis, section 6.2: the FlashAttention backend attends the batch's     */
+/* new query tokens, packed by query_start_loc, to the paged keys of each    */
+/* request with seqlen_k = seq_lens, the block table and causal masking;     */
+/* section 5.4 lists query_start_loc as each request's first query row).     */
+/* ------------------------------------------------------------------------ */
+
+/* Readings where the section is silent:
+ *   - the q_len = query_start_loc[r+1] - query_start_loc[r] query rows of
+ *     request r are its LAST q_len tokens: seq_lens[r] counts them and the
+ *     cache write has already put them in the pool, so query row i of the
+ *     request sits at position p = seq_lens[r] - q_len + i;
+ *   - causal: position p attends keys 0..p; not causal (the shared-prefix
+ *     pass of section 6.4): every key 0..seq_lens[r]-1;
+ *   - lse is the natural log of the softmax denominator,
+ *     log sum_t exp(scale * q . k_t). */
+typedef struct {
+    double *out;                   /* [num_tokens, num_heads, head_size] */
+    double *lse;                   /* [num_tokens, num_heads] or NULL */
+    const uint16_t *q;             /* [num_tokens, num_heads, head_size] */
+    const uint16_t *cache;         /* [2, num_blocks, block_size, num_kv_heads, head_size] */
+    const int32_t *block_tables;   /* row r at block_tables + r * block_table_stride */
+    int64_t block_table_stride;
+    const int32_t *seq_lens;       /* [num_reqs] */
+    const int32_t *query_start_loc; /* [num_reqs + 1] */
+    int num_reqs, num_heads, num_kv_heads, head_size, block_size, num_blocks,
+        max_blocks_per_seq, causal;
+    double scale;
+    int dtype;
+    const int64_t *items; /* (token * num_heads + head) indices, or NULL for all */
+    int64_t num_items;
+} or_prefill_args;
+
+/* One output row: query token tok, query head h. */
+static int or_prefill_row(const or_prefill_args *A, int64_t tok, int h, double *Kc,
+                          double *Vc, double *a)
+{
+    const int D = A->head_size;
+    const int kvh = h / (A->num_heads / A->num_kv_heads);
+    int r = -1;
+    for (int i = 0; i < A->num_reqs; i++)
+        if (A->query_start_loc[i] <= tok && tok < A->query_start_loc[i + 1]) {
+            r = i;
+            break;
+        }
+    if (r < 0)
+        return OR_ERR_ARG;
+    const int L = A->seq_lens[r];
+    const int q_len = A->query_start_loc[r + 1] - A->query_start_loc[r];
+    if (L < q_len || L > A->max_blocks_per_seq * A->block_size)
+        return OR_ERR_SEQ_LEN;
+    const int pos = L - q_len + (int)(tok - A->query_start_loc[r]);
+    const int n_keys = A->causal ? pos + 1 : L;
+    const int32_t *bt = A->block_tables + (size_t)r * A->block_table_stride;
+
+    /* 1. Gather keys and values 0..n_keys-1 into contiguous rows. */
+    for (int t = 0; t < n_keys; t++) {
+        int32_t phys, off;
+        or_translate(bt, t, A->block_size, &phys, &off);
+        if (phys < 0 || phys >= A->num_blocks)
+            return OR_ERR_BLOCK_ID;
+        for (int d = 0; d < D; d++) {
+            Kc[(size_t)t * D + d] = or_load(
+                A->cache, or_pool_index(0, phys, off, kvh, d, A->num_blocks, A->block_size,
+                                        A->num_kv_heads, D), A->dtype);
+            Vc[(size_t)t * D + d] = or_load(
+                A->cache, or_pool_index(1, phys, off, kvh, d, A->num_blocks, A->block_size,
+                                        A->num_kv_heads, D), A->dtype);
+        }
+    }
+
+    /* 2. Scores a_t = scale * q . k_t. */
+    const size_t qrow = ((size_t)tok * A->num_heads + h) * D;
+    for (int t = 0; t < n_keys; t++) {
+        double acc = 0.0;
+        for (int d = 0; d < D; d++)
+            acc += or_load(A->q, qrow + d, A->dtype) * Kc[(size_t)t * D + d];
+        a[t] = A->scale * acc;
+    }
+
+    /* 3. Softmax with its maximum m and denominator l. */
+    double m = a[0];
+    for (int t = 1; t < n_keys; t++)
+        if (a[t] > m)
+            m = a[t];
+    double l = 0.0;
+    for (int t = 0; t < n_keys; t++) {
+        a[t] = exp(a[t] - m);
+        l += a[t];
+    }
+
+    /* 4. out[d] = sum_t softmax_t v_t[d]; lse = m + log l. */
+    double *o = A->out + ((size_t)tok * A->num_heads + h) * D;
+    for (int d = 0; d < D; d++) {
+        double acc = 0.0;
+        for (int t = 0; t < n_keys; t++)
+            acc += a[t] * Vc[(size_t)t * D + d];
+        o[d] = acc / l;
+    }
+    if (A->lse)
+        A->lse[(size_t)tok * A->num_heads + h] = m + log(l);
+    return OR_OK;
+}
+
+typedef struct {
+    const or_prefill_args *A;
+    int tid, nthreads;
+    int status;
+} or_prefill_worker_t;
+
+static void *or_prefill_worker(void *p)
+{
+    or_prefill_worker_t *w = (or_prefill_worker_t *)p;
+    const or_prefill_args *A = w->A;
+    const int64_t num_tokens = A->query_start_loc[A->num_reqs];
+    const int64_t n = A->items ? A->num_items : num_tokens * A->num_heads;
+    size_t cap = (size_t)A->max_blocks_per_seq * A->block_size;
+    if (cap == 0)
+        cap = 1;
+    double *Kc = (double *)malloc(cap * A->head_size * sizeof(double));
+    double *Vc = (double *)malloc(cap * A->head_size * sizeof(double));
+    double *a = (double *)malloc(cap * sizeof(double));
+    w->status = OR_OK;
+    if (!Kc || !Vc || !a) {
+        w->status = OR_ERR_NOMEM;
+    } else {
+        for (int64_t i = w->tid; i < n; i += w->nthreads) {
+            int64_t item = A->items ? A->items[i] : i;
+            if (item < 0 || item >= num_tokens * A->num_heads) {
+                w->status = OR_ERR_ARG;
+                break;
+            }
+            int rc = or_prefill_row(A, item / A->num_heads, (int)(item % A->num_heads), Kc,
+                                    Vc, a);
+            if (rc != OR_OK) {
+                w->status = rc;
+                break;
+            }
+        }
+    }
+    free(Kc);
+    free(Vc);
+    free(a);
+    return NULL;
+}
+
+/* Attention of every packed query row (or only the listed items) to its
+ * request's paged keys.  out [num_tokens, num_heads, head_size] and lse
+ * [num_tokens, num_heads] (may be NULL) are double precision; rows not listed
+ * are left untouched.  num_tokens = query_start_loc[num_reqs]. */
+int or_prefill(double *out, double *lse, const uint16_t *q, const uint16_t *cache,
+               const int32_t *block_tables, int64_t block_table_stride,
+               const int32_t *seq_lens, const int32_t *query_start_loc, int num_reqs,
+               int num_heads, int num_kv_heads, int head_size, int block_size, int num_blocks,
+               int max_blocks_per_seq, double scale, int causal, int dtype,
+               const int64_t *items, int64_t num_items, int nthreads)
+{
+    if (num_reqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || block_table_stride < max_blocks_per_seq ||
+        (dtype != OR_FP16 && dtype != OR_BF16))
+        return OR_ERR_ARG;
+    if (query_start_loc[0] != 0)
+        return OR_ERR_ARG;
+    for (int r = 0; r < num_reqs; r++)
+        if (query_start_loc[r + 1] < query_start_loc[r])
+            return OR_ERR_ARG;
+    if (nthreads < 1)
+        nthreads = 1;
+    or_prefill_args A = {out, lse, q, cache, block_tables, block_table_stride, seq_lens,
+                         query_start_loc, num_reqs, num_heads, num_kv_heads, head_size,
+                         block_size, num_blocks, max_blocks_per_seq, causal ? 1 : 0, scale,
+                         dtype, items, num_items};
+    or_prefill_worker_t *w =
+        (or_prefill_worker_t *)calloc((size_t)nthreads, sizeof(or_prefill_worker_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!w || !th) {
+        free(w);
+        free(th);
+        return OR_ERR_NOMEM;
+    }
+    int started = 1;
+    for (int i = 0; i < nthreads; i++) {
+        w[i].A = &A;
+        w[i].tid = i;
+        w[i].nthreads = nthreads;
+    }
+    for (int i = 1; i < nthreads; i++) {
+        if (pthread_create(&th[i], NULL, or_prefill_worker, &w[i]) != 0)
+            break;
+        started = i + 1;
+    }
+    or_prefill_worker(&w[0]);
+    for (int i = 1; i < started; i++)
+        pthread_join(th[i], NULL);
+    /* Items of threads that never started are done here, one by one. */
+    for (int i = started; i < nthreads; i++)
+        or_prefill_worker(&w[i]);
+    int st = OR_OK;
+    for (int i = 0; i < nthreads; i++)
+        if (w[i].status != OR_OK)
+            st = w[i].status;
+    free(w);
+    free(th);
+    return st;
+}
+
+/* Merge of two attention results over disjoint key sets, each given with its
+ * log-sum-exp (chen3feng vLLM analysis, section 6.4: the shared-prefix pass
+ * and the per-request suffix pass are combined with the online-softmax
+ * correction).  With M = max(lse_a, lse_b), w_x = exp(lse_x - M):
+ *   out = (w_a o_a + w_b o_b) / (w_a + w_b),  lse = M + log(w_a + w_b).
+ * A part with lse = -inf is empty; two empty parts give out = 0,
+ * lse = -inf.  lse_out may be NULL. */
+int or_merge_attn_states(double *out, double *lse_out, const double *o_a,
+                         const double *lse_a, const double *o_b, const double *lse_b,
+                         int64_t rows, int D)
+{
+    if (rows < 0 || D <= 0)
+        return OR_ERR_ARG;
+    for (int64_t i = 0; i < rows; i++) {
+        const double la = lse_a[i], lb = lse_b[i];
+        double *o = out + (size_t)i * D;
+        if (isinf(la) && la < 0 && isinf(lb) && lb < 0) {
+            for (int d = 0; d < D; d++)
+                o[d] = 0.0;
+            if (lse_out)
+                lse_out[i] = -INFINITY;
+            continue;
+        }
+        const double M = la > lb ? la : lb;
+        const double wa = exp(la - M), wb = exp(lb - M);
+        for (int d = 0; d < D; d++)
+            o[d] = (wa * o_a[(size_t)i * D + d] + wb * o_b[(size_t)i * D + d]) / (wa + wb);
+        if (lse_out)
+            lse_out[i] = M + log(wa + wb);
     }
     return OR_OK;
 }

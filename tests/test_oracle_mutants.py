@@ -15,10 +15,14 @@ from oracle.oracle import SOURCE, compile_source
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-# (name, text in pa_oracle.c, replacement)
+# (name, text in pa_oracle.c, replacement[, which occurrence]).  Text that
+# occurs more than once (the decode and the prefill row routines state the
+# same softmax steps) names the occurrence to change: 0 = decode, 1 = prefill.
 MUTANTS = [
-    ("softmax_sign", "a[t] = exp(a[t] - m);", "a[t] = exp(m - a[t]);"),
-    ("scale_dropped", "a[t] = A->scale * acc;", "a[t] = acc;"),
+    ("softmax_sign", "a[t] = exp(a[t] - m);", "a[t] = exp(m - a[t]);", 0),
+    ("prefill_softmax_sign", "a[t] = exp(a[t] - m);", "a[t] = exp(m - a[t]);", 1),
+    ("scale_dropped", "a[t] = A->scale * acc;", "a[t] = acc;", 0),
+    ("prefill_scale_dropped", "a[t] = A->scale * acc;", "a[t] = acc;", 1),
     ("gqa_head_map", "const int kvh = h / G;", "const int kvh = h % A->num_kv_heads;"),
     ("query_row_uses_kv_head", "const size_t qrow = ((size_t)s * A->num_heads + h) * D;",
      "const size_t qrow = ((size_t)s * A->num_heads + kvh) * D;"),
@@ -33,24 +37,52 @@ MUTANTS = [
      "cache[or_pool_index(0, blk, off, h, d, num_blocks, block_size, num_kv_heads,"),
     ("normaliser_drops_term", "    for (int t = 0; t < L; t++) {\n        a[t] = exp(a[t] - m);\n        l += a[t];\n    }",
      "    for (int t = 0; t < L; t++) {\n        a[t] = exp(a[t] - m);\n        if (t) l += a[t];\n    }"),
-    ("no_normalisation", "o[d] = acc / l;", "o[d] = acc;"),
+    ("no_normalisation", "o[d] = acc / l;", "o[d] = acc;", 0),
+    ("prefill_no_normalisation", "o[d] = acc / l;", "o[d] = acc;", 1),
     ("half_subnormal_exponent", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     ("ties_away_from_zero", "double n = nearbyint(a / quantum);", "double n = round(a / quantum);"),
     ("online_merge_skips_rescale", "l = c_old * l + c_new * lj;", "l = l + c_new * lj;"),
     ("partials_unweighted_denominator", "denom += exp(m[p] - M) * l[p];", "denom += l[p];"),
     ("copy_wrong_plane", "const size_t base = (size_t)plane * num_blocks * block_elems;",
      "const size_t base = 0;"),
+    ("prefill_causal_off_by_one", "const int n_keys = A->causal ? pos + 1 : L;",
+     "const int n_keys = A->causal ? pos + 2 : L;"),
+    ("prefill_top_left_causal",
+     "const int pos = L - q_len + (int)(tok - A->query_start_loc[r]);",
+     "const int pos = (int)(tok - A->query_start_loc[r]);"),
+    ("prefill_ignores_query_start_loc",
+     "const int pos = L - q_len + (int)(tok - A->query_start_loc[r]);",
+     "const int pos = L - q_len + (int)tok;"),
+    ("prefill_lse_in_log2", "A->lse[(size_t)tok * A->num_heads + h] = m + log(l);",
+     "A->lse[(size_t)tok * A->num_heads + h] = m + log2(l);"),
+    ("prefill_query_head_for_kv_head", "const size_t qrow = ((size_t)tok * A->num_heads + h) * D;",
+     "const size_t qrow = ((size_t)tok * A->num_heads + kvh) * D;"),
+    ("merge_lse_drops_max", "lse_out[i] = M + log(wa + wb);", "lse_out[i] = log(wa + wb);"),
+    ("merge_unnormalised", "o[d] = (wa * o_a[(size_t)i * D + d] + wb * o_b[(size_t)i * D + d]) / (wa + wb);",
+     "o[d] = wa * o_a[(size_t)i * D + d] + wb * o_b[(size_t)i * D + d];"),
     ("max_misses_first_score", "double m = a[0];\n    for (int t = 1; t < L; t++)",
      "double m = a[L - 1] - 50.0;\n    for (int t = 1; t < L; t++)"),
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_planted_mistake_is_caught(tmp_path, name, old, new):
+def _plant(src: str, old: str, new: str, which):
+    if which is None:
+        assert src.count(old) == 1, "anchor text not found exactly once"
+        return src.replace(old, new)
+    assert src.count(old) == 2, "anchor text not found exactly twice"
+    at = -1
+    for _ in range(which + 1):
+        at = src.index(old, at + 1)
+    return src[:at] + new + src[at + len(old):]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, mutant):
+    name, old, new = mutant[:3]
+    which = mutant[3] if len(mutant) > 3 else None
     src = open(SOURCE).read()
-    assert src.count(old) == 1, f"mutant {name}: anchor text not found exactly once"
     mutant_c = tmp_path / f"{name}.c"
-    mutant_c.write_text(src.replace(old, new))
+    mutant_c.write_text(_plant(src, old, new, which))
     so = compile_source(str(mutant_c), str(tmp_path / f"lib{name}.so"))
     env = dict(os.environ, PA_ORACLE_SO=so)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",

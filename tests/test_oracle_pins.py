@@ -522,3 +522,193 @@ def test_copy_blocks_rejects_bad_ids(orc):
     cache = np.zeros((2, 4, 16, 1, 8), np.uint16)
     with pytest.raises(OracleError):
         orc.copy_blocks(cache, np.array([[0, 4]], np.int64))
+
+
+# ---------------------------------------------------------------------------
+# Prefill / chunked prefill and the merge of attention states
+# ---------------------------------------------------------------------------
+
+def _prefill_case(rng, q_lens, ctx_lens, H, Hkv, D, bs, dtype, extra_blocks=4):
+    """Scattered tables: the pool's blocks are dealt from a permutation."""
+    q_lens = np.asarray(q_lens, np.int64)
+    L = q_lens + np.asarray(ctx_lens, np.int64)
+    nblk = -(-L // bs)
+    R = len(q_lens)
+    NB = int(nblk.sum()) + extra_blocks
+    ids = rng.permutation(NB).astype(np.int32)
+    bt = np.full((R, int(nblk.max())), -1, np.int32)
+    c = 0
+    for r in range(R):
+        bt[r, :nblk[r]] = ids[c:c + nblk[r]]
+        c += int(nblk[r])
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    cache = _rand_bits(rng, (2, NB, bs, Hkv, D), dtype)
+    q = _rand_bits(rng, (int(qsl[-1]), H, D), dtype)
+    return q, cache, bt, L.astype(np.int32), qsl
+
+
+def _sdpa_prefill(orc, q, cache, bt, L, qsl, H, Hkv, D, bs, scale, dtype, causal=True):
+    """torch SDPA in fp64 with an explicit mask, keys gathered by numpy fancy
+    indexing of the 5-D pool; also the log-sum-exp of the masked scores."""
+    qd = torch.from_numpy(orc.widen(q, dtype))
+    kd = torch.from_numpy(orc.widen(cache[0], dtype))
+    vd = torch.from_numpy(orc.widen(cache[1], dtype))
+    T = q.shape[0]
+    out = np.zeros((T, H, D))
+    lse = np.zeros((T, H))
+    G = H // Hkv
+    for r in range(len(L)):
+        n, ql = int(L[r]), int(qsl[r + 1] - qsl[r])
+        if ql == 0:
+            continue
+        t = np.arange(n)
+        k = kd[bt[r, t // bs], t % bs].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        v = vd[bt[r, t // bs], t % bs].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qq = qd[qsl[r]:qsl[r + 1]].permute(1, 0, 2)                       # [H, ql, D]
+        pos = (n - ql) + np.arange(ql)
+        allowed = torch.from_numpy(t[None, :] <= pos[:, None]) if causal else \
+            torch.ones((ql, n), dtype=torch.bool)
+        o = torch.nn.functional.scaled_dot_product_attention(qq, k, v, attn_mask=allowed,
+                                                             scale=scale)
+        out[qsl[r]:qsl[r + 1]] = o.permute(1, 0, 2).numpy()
+        s = scale * (qq @ k.transpose(1, 2))
+        s = s.masked_fill(~allowed, float("-inf"))
+        lse[qsl[r]:qsl[r + 1]] = torch.logsumexp(s, dim=-1).T.numpy()
+    return out, lse
+
+
+PREFILL_CASES = [
+    # q_lens, ctx_lens, H, Hkv, D, bs, dtype
+    ([1, 20, 37], [0, 5, 0], 4, 2, 64, 16, FP16),
+    ([16, 3, 40], [16, 30, 1], 4, 4, 64, 16, BF16),
+    ([70, 1], [33, 64], 8, 1, 128, 32, BF16),
+]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("q_lens,ctx,H,Hkv,D,bs,dtype", PREFILL_CASES)
+def test_prefill_matches_masked_sdpa(orc, q_lens, ctx, H, Hkv, D, bs, dtype, causal):
+    rng = np.random.default_rng(sum(q_lens) * 7 + sum(ctx) + H)
+    q, cache, bt, L, qsl = _prefill_case(rng, q_lens, ctx, H, Hkv, D, bs, dtype)
+    scale = 1.0 / math.sqrt(D)
+    got, lse = orc.prefill(q, cache, bt, L, qsl, Hkv, bs, scale, dtype, causal=causal,
+                           nthreads=2)
+    ref, ref_lse = _sdpa_prefill(orc, q, cache, bt, L, qsl, H, Hkv, D, bs, scale, dtype,
+                                 causal)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_first_row_of_a_fresh_prompt_is_its_value(orc):
+    """A fresh prompt's first token sees only itself: its output is v_0."""
+    rng = np.random.default_rng(61)
+    q, cache, bt, L, qsl = _prefill_case(rng, [5, 9], [0, 0], 4, 2, 64, 16, BF16)
+    out, lse = orc.prefill(q, cache, bt, L, qsl, 2, 16, 0.125, BF16)
+    v = orc.widen(cache[1], BF16)
+    for r in range(2):
+        for h in range(4):
+            assert np.array_equal(out[qsl[r], h], v[bt[r, 0], 0, h // 2])
+            s = 0.125 * float(orc.widen(q[qsl[r], h], BF16) @ orc.widen(cache[0][bt[r, 0], 0, h // 2], BF16))
+            assert lse[qsl[r], h] == pytest.approx(s, abs=1e-12)
+
+
+def test_prefill_zero_query_gives_running_means(orc):
+    """q = 0 makes every allowed score equal: row i of a request averages the
+    values of positions 0..ctx+i (causal) and lse = log(ctx + i + 1)."""
+    rng = np.random.default_rng(62)
+    q, cache, bt, L, qsl = _prefill_case(rng, [12], [7], 2, 2, 64, 16, FP16)
+    q[:] = 0
+    out, lse = orc.prefill(q, cache, bt, L, qsl, 2, 16, 0.3, FP16)
+    v = orc.widen(cache[1], FP16)
+    rows = np.stack([v[bt[0, t // 16], t % 16] for t in range(19)])      # [19, Hkv, D]
+    for i in range(12):
+        n = 7 + i + 1
+        np.testing.assert_allclose(out[i], rows[:n].mean(axis=0), rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse[i], math.log(n), rtol=0, atol=1e-13)
+
+
+def test_prefill_with_one_query_row_equals_decode(orc):
+    """q_len = 1 is the decode step: the two routines, written apart, agree."""
+    rng = np.random.default_rng(63)
+    lens = [1, 17, 40, 129]
+    q, cache, bt, L, qsl = _prefill_case(rng, [1] * 4, [x - 1 for x in lens], 8, 2, 128, 16, BF16)
+    got, _ = orc.prefill(q, cache, bt, L, qsl, 2, 16, 0.09, BF16)
+    ref = orc.decode(q, cache, bt, L, 2, 16, 0.09, BF16)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_chunked_prefill_equals_one_pass(orc):
+    """Prefilling a prompt in two chunks (the first with seq_len = its own
+    end) gives the same rows as one pass over the whole prompt."""
+    rng = np.random.default_rng(64)
+    q, cache, bt, L, qsl = _prefill_case(rng, [45], [0], 4, 2, 64, 16, FP16)
+    whole, whole_lse = orc.prefill(q, cache, bt, L, qsl, 2, 16, 0.125, FP16)
+    a = 19
+    c1, l1 = orc.prefill(q[:a], cache, bt, [a], [0, a], 2, 16, 0.125, FP16)
+    c2, l2 = orc.prefill(q[a:], cache, bt, [45], [0, 45 - a], 2, 16, 0.125, FP16)
+    np.testing.assert_allclose(np.concatenate([c1, c2]), whole, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(np.concatenate([l1, l2]), whole_lse, rtol=1e-14, atol=0)
+
+
+def test_non_causal_last_row_equals_causal(orc):
+    rng = np.random.default_rng(65)
+    q, cache, bt, L, qsl = _prefill_case(rng, [10, 6], [3, 20], 4, 2, 64, 16, BF16)
+    c, cl = orc.prefill(q, cache, bt, L, qsl, 2, 16, 0.125, BF16, causal=True)
+    n, nl = orc.prefill(q, cache, bt, L, qsl, 2, 16, 0.125, BF16, causal=False)
+    last = qsl[1:] - 1
+    np.testing.assert_array_equal(c[last], n[last])
+    np.testing.assert_array_equal(cl[last], nl[last])
+    assert not np.allclose(c[0], n[0])
+
+
+def test_cascade_prefix_then_suffix_merge_equals_whole(orc):
+    """The shared-prefix split: a non-causal pass over the first P keys and a
+    causal pass over the rest, merged with their log-sum-exps, reproduce one
+    causal pass over all keys (output and lse)."""
+    rng = np.random.default_rng(66)
+    bs, P = 16, 32
+    q, cache, bt, L, qsl = _prefill_case(rng, [1, 5, 20], [60, 40, P], 4, 2, 64, bs, BF16)
+    whole, whole_lse = orc.prefill(q, cache, bt, L, qsl, 2, bs, 0.125, BF16)
+    pb = P // bs
+    # Each request's first P keys play the prefix: the prefix pass reads only
+    # them (every query row sees all of them); the suffix pass reads the rest,
+    # whose positions start at P.
+    pre, pre_lse = orc.prefill(q, cache, bt[:, :pb].copy(), np.full(3, P, np.int32),
+                               qsl, 2, bs, 0.125, BF16, causal=False)
+    suf, suf_lse = orc.prefill(q, cache, bt[:, pb:].copy(), L - P, qsl, 2, bs, 0.125, BF16)
+    got, got_lse = orc.merge_attn_states(pre, pre_lse, suf, suf_lse)
+    np.testing.assert_allclose(got, whole, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(got_lse, whole_lse, rtol=1e-13, atol=1e-13)
+
+
+def test_merge_attn_states_closed_forms(orc):
+    o_a = np.array([[1.0, 2.0], [3.0, -1.0], [0.5, 0.5], [7.0, 7.0]])
+    o_b = np.array([[3.0, 0.0], [9.0, 9.0], [-2.0, 4.0], [1.0, 1.0]])
+    inf = float("inf")
+    lse_a = np.array([0.7, 2.0, -inf, -inf])
+    lse_b = np.array([0.7, -inf, 5.0, -inf])
+    out, lse = orc.merge_attn_states(o_a, lse_a, o_b, lse_b)
+    np.testing.assert_allclose(out[0], [2.0, 1.0], rtol=1e-15)            # equal weights
+    assert lse[0] == pytest.approx(0.7 + math.log(2.0), abs=1e-15)
+    np.testing.assert_array_equal(out[1], o_a[1])                          # b empty
+    assert lse[1] == 2.0
+    np.testing.assert_array_equal(out[2], o_b[2])                          # a empty
+    assert lse[2] == 5.0
+    np.testing.assert_array_equal(out[3], [0.0, 0.0])                      # both empty
+    assert lse[3] == -inf
+    # weights e^1 : e^0 for lse (1 + c, c)
+    out, lse = orc.merge_attn_states(o_a[:1], np.array([4.0]), o_b[:1], np.array([3.0]))
+    w = math.e / (math.e + 1.0)
+    np.testing.assert_allclose(out[0], w * o_a[0] + (1 - w) * o_b[0], rtol=1e-14)
+    assert lse[0] == pytest.approx(3.0 + math.log(math.e + 1.0), abs=1e-14)
+
+
+def test_prefill_rejects_bad_metadata(orc):
+    rng = np.random.default_rng(67)
+    q, cache, bt, L, qsl = _prefill_case(rng, [4, 4], [0, 0], 2, 2, 64, 16, FP16)
+    with pytest.raises(OracleError):            # seq_len shorter than the query rows
+        orc.prefill(q, cache, bt, np.array([3, 4], np.int32), qsl, 2, 16, 0.1, FP16)
+    bad = bt.copy()
+    bad[1, 0] = cache.shape[1] + 5
+    with pytest.raises(OracleError):
+        orc.prefill(q, cache, bad, L, qsl, 2, 16, 0.1, FP16)

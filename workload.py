@@ -31,6 +31,20 @@ Workloads (seed = the config index unless given):
   [50, 500] tokens starting at a block boundary, 32 q / 8 kv heads,
   head_size 128, block_size 16, bf16.
 
+Prefill workloads (``make_prefill``; the pages give no prefill shapes, so these
+are a stated recipe): the batch's new query tokens are packed row after row
+and ``query_start_loc`` holds each request's first row.  Request r has
+``ctx_r`` tokens already cached and ``q_r`` new tokens, ``seq_len = ctx_r +
+q_r``; the new tokens' keys/values are written at positions ctx_r..seq_len-1
+by the cache-write step before the attention reads them.
+
+- ``prefill_tiny``: q_len {1, 20, 37, 130}, ctx {0, 5, 0, 70}, 4 q / 2 kv
+  heads, head_size 128, block_size 16, fp16.
+- ``prefill_mha7b``: 16 requests, q_len uniform on [256, 2048]; even requests
+  are fresh prompts (ctx 0), odd ones continue a chunked prefill with ctx
+  uniform on [0, 4096]; 32/32 heads, head_size 128, block_size 16, fp16.
+- ``prefill_gqa8b``: the same lengths recipe with 32 q / 8 kv heads, bf16.
+
 Q, K and V are N(0,1) draws rounded to the cache dtype.  With ``poison=True``
 every pool row that no sequence owns (unused blocks and the tail of each
 sequence's last block) holds NaN, so a read past a sequence's end shows up in
@@ -253,3 +267,136 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 
 ORACLE_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+# ---------------------------------------------------------------------------
+# Prefill / chunked-prefill workloads
+# ---------------------------------------------------------------------------
+
+PREFILL_NAMES = ("prefill_tiny", "prefill_mha7b", "prefill_gqa8b")
+
+PREFILL_SPECS = {
+    "prefill_tiny": Spec("prefill_tiny", 4, 4, 2, 128, 16, torch.float16),
+    "prefill_mha7b": Spec("prefill_mha7b", 16, 32, 32, 128, 16, torch.float16),
+    "prefill_gqa8b": Spec("prefill_gqa8b", 16, 32, 8, 128, 16, torch.bfloat16),
+}
+
+
+@dataclass
+class PrefillWorkload:
+    name: str
+    q: torch.Tensor                 # [T, H, D] packed new query tokens
+    kv_cache: torch.Tensor          # [2, NB, bs, Hkv, D]
+    block_tables: torch.Tensor      # [R, MB] int32, unused entries -1
+    seq_lens: torch.Tensor          # [R] int32, cached + new tokens
+    query_start_loc: torch.Tensor   # [R + 1] int32
+    key: torch.Tensor               # [T, Hkv, D] new tokens' keys
+    value: torch.Tensor             # [T, Hkv, D]
+    slot_mapping: torch.Tensor      # [T] int64
+    block_size: int
+    scale: float
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kv_cache.shape[1])
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.q.dtype
+
+    def q_lens(self) -> np.ndarray:
+        qsl = self.query_start_loc.cpu().numpy().astype(np.int64)
+        return qsl[1:] - qsl[:-1]
+
+    def causal_pairs(self) -> int:
+        """(query row, key) pairs a causal pass attends, per query head."""
+        L = self.seq_lens.cpu().numpy().astype(np.int64)
+        ql = self.q_lens()
+        ctx = L - ql
+        return int((ql * ctx + ql * (ql + 1) // 2).sum())
+
+
+def make_prefill(name: str, seed: int | None = None, device="cpu", poison: bool = False,
+                 q_lens=None, ctx_lens=None, **overrides) -> PrefillWorkload:
+    """Build one prefill workload; ``q_lens``/``ctx_lens``/spec fields may be
+    overridden to make smaller cases with the same structure."""
+    if seed is None:
+        seed = 101 + PREFILL_NAMES.index(name)
+    spec = PREFILL_SPECS[name]
+    spec = Spec(**{**spec.__dict__, **{k: v for k, v in overrides.items()
+                                       if k in spec.__dict__}})
+    rng = np.random.default_rng(seed)
+    if q_lens is not None:
+        ql = np.asarray(q_lens, dtype=np.int64)
+        cx = np.zeros_like(ql) if ctx_lens is None else np.asarray(ctx_lens, dtype=np.int64)
+    elif name == "prefill_tiny":
+        ql = np.array([1, 20, 37, 130], dtype=np.int64)
+        cx = np.array([0, 5, 0, 70], dtype=np.int64)
+    else:
+        R = spec.num_seqs
+        ql = rng.integers(256, 2048, size=R, endpoint=True)
+        cx = np.where(np.arange(R) % 2 == 1, rng.integers(0, 4096, size=R, endpoint=True), 0)
+    R = ql.size
+    L = ql + cx
+    H, Hkv, D, bs = spec.num_heads, spec.num_kv_heads, spec.head_size, spec.block_size
+    nblk = -(-L // bs)
+    MB = max(1, int(nblk.max()) if R else 1)
+    need = int(nblk.sum())
+    NB = max(1, need, int(math.ceil(spec.pool_factor * need)))
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((R, MB), -1, dtype=np.int32)
+    cursor = 0
+    for r in range(R):
+        k = int(nblk[r])
+        tables[r, :k] = perm[cursor:cursor + k]
+        cursor += k
+    qsl = np.zeros(R + 1, dtype=np.int64)
+    qsl[1:] = np.cumsum(ql)
+    T = int(qsl[-1])
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    q = _randn((T, H, D), gen, device, spec.dtype)
+    cache = torch.empty((2, NB, bs, Hkv, D), dtype=spec.dtype, device=device)
+    cache[0] = _randn((NB, bs, Hkv, D), gen, device, spec.dtype, chunk_rows=1 << 12)
+    cache[1] = _randn((NB, bs, Hkv, D), gen, device, spec.dtype, chunk_rows=1 << 12)
+    key = _randn((T, Hkv, D), gen, device, spec.dtype)
+    value = _randn((T, Hkv, D), gen, device, spec.dtype)
+    slots = np.empty(T, dtype=np.int64)
+    for r in range(R):
+        for i in range(int(ql[r])):
+            pos = int(cx[r]) + i
+            slots[qsl[r] + i] = int(tables[r, pos // bs]) * bs + pos % bs
+
+    if poison:
+        owned = np.zeros((NB, bs), dtype=bool)
+        for r in range(R):
+            for j in range(int(nblk[r])):
+                n = min(bs, int(L[r]) - j * bs)
+                owned[tables[r, j], :n] = True
+        mask = torch.from_numpy(~owned).to(device)
+        nan = torch.tensor(float("nan"), dtype=spec.dtype, device=device)
+        for plane in range(2):
+            cache[plane][mask] = nan
+
+    return PrefillWorkload(
+        name=name, q=q, kv_cache=cache,
+        block_tables=torch.from_numpy(tables).to(device),
+        seq_lens=torch.from_numpy(L.astype(np.int32)).to(device),
+        query_start_loc=torch.from_numpy(qsl.astype(np.int32)).to(device),
+        key=key, value=value, slot_mapping=torch.from_numpy(slots).to(device),
+        block_size=bs, scale=1.0 / math.sqrt(D), num_heads=H, num_kv_heads=Hkv,
+        head_size=D, meta={"seed": seed, "poison": poison},
+    )
