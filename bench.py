@@ -51,6 +51,13 @@ WORKLOAD_TEXT = {
               "32 q / 8 kv heads, head_size 128, block_size 16, bf16",
     "tiny": "tiny: 4 seqs {1,17,33,64}, 4/4 heads, head_size 64, block_size 16, fp16",
 }
+PREFILL_TEXT = {
+    "prefill_mha7b": "chunked prefill, MHA 7B-like: 16 requests, q_len U[256,2048], even ones "
+                     "fresh (ctx 0), odd ones ctx U[0,4096]; 32/32 heads, head_size 128, "
+                     "block_size 16, fp16, causal",
+    "prefill_gqa8b": "chunked prefill, GQA 8B-like: the same lengths, 32 q / 8 kv heads, "
+                     "head_size 128, block_size 16, bf16, causal",
+}
 DECODE_SOURCES = ["paged_kv_cache_136_gb300/csrc/pa_decode.cuh",
                   "paged_kv_cache_136_gb300/csrc/pa_decode_tc.cuh",
                   "paged_kv_cache_136_gb300/csrc/pa_ptx.cuh"]
@@ -210,8 +217,9 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 # ---------------------------------------------------------------------------
@@ -443,6 +451,56 @@ def copy_blocks_workload(args, peak_gbs: float) -> dict:
     return res
 
 
+def prefill_workload(name: str, args, peaks: dict) -> dict:
+    """Prefill step (cache write of the new tokens + causal prefill attention
+    over the paged pool), device-resident, timed per call with CUDA events.
+    Work per call: 4 * head_size flops per (query row, attended key, query
+    head) -- the QK^T and PV contractions -- over the causal pairs only."""
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    w = wl.make_prefill(name, device="cuda")
+    out = torch.empty_like(w.q)
+    mq = int(w.q_lens().max())
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pa.pa_prefill(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.query_start_loc,
+                      w.scale, w.block_size, mq)
+
+    for _ in range(5):
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        call()
+    k = max(3, args.workload_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k)]
+    torch.cuda.synchronize()
+    for i in range(k):
+        ev[i][0].record(stream)
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        ev[i][1].record(stream)
+        call()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    flops = 4 * w.head_size * w.num_heads * w.causal_pairs()
+    tf = flops / ms / 1e9
+    peak = peaks.get("bf16_tflops")
+    res = {"name": name, "call": "pa_prefill (causal)", "workload": PREFILL_TEXT[name],
+           "launches": k, "tokens": w.num_tokens, "flops_per_call": flops,
+           "ms_per_call": round(ms, 5), "tflops": round(tf, 2),
+           "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                        "peak_source": peaks["source"] + " bf16 dense (cuBLAS), burst; "
+                                       "fp16 has the same nominal rate"},
+           "ms_per_step": round(step_ms, 5),
+           "tokens_per_s": round(w.num_tokens / (step_ms / 1e3), 1),
+           "device_error_flags": pa.pa_device_errors(clear=True)}
+    del w, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def other_workload(name: str, args, peak_gbs: float) -> dict:
     """Short device-resident measurement of another workload through the same
     step (cache write + split-K decode), reported beside the main line."""
@@ -451,6 +509,8 @@ def other_workload(name: str, args, peak_gbs: float) -> dict:
     import workload as wl
     if name == "copy_blocks":
         return copy_blocks_workload(args, peak_gbs)
+    if name.startswith("prefill_"):
+        return prefill_workload(name, args, measured_peaks())
     w = wl.make(name, device="cuda")
     out = torch.empty_like(w.q)
     msl = int(w.seq_lens.max().item())
@@ -553,7 +613,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200,
                     help="steps in the end-to-end (host buffers) measurement")
-    ap.add_argument("--workloads", default="gqa8b,long,prefix,tiny,copy_blocks",
+    ap.add_argument("--workloads",
+                    default="gqa8b,long,prefix,tiny,copy_blocks,prefill_mha7b,prefill_gqa8b",
                     help="other workloads measured briefly beside the main line ('' for none)")
     ap.add_argument("--workload-steps", type=int, default=50)
     return ap.parse_args(argv)

@@ -7,6 +7,7 @@
  *   pa_decode             one-pass paged decode attention
  *   pa_decode_splitk      partitioned decode attention + log-sum-exp reduce
  *   pa_copy_blocks        copy whole blocks (the device half of copy-on-write)
+ *   pa_prefill            prefill / chunked prefill attention over the pool
  *
  * Data layout (all tensors contiguous, row-major, caller-owned):
  *
@@ -177,6 +178,48 @@ pa_status pa_decode_splitk_noalloc(void *out, const void *q, const void *kv_cach
                                    int block_size, int num_blocks, int max_blocks_per_seq,
                                    float scale, pa_dtype dtype, int max_seq_len,
                                    int partition_size, void *stream);
+
+/*
+ * Prefill / chunked prefill over the paged cache ("PagedAttention 在 vLLM 中的
+ * 实现分析", section 6.2: the FlashAttention backend attends the batch's new
+ * query tokens, packed by query_start_loc, to each request's paged keys with
+ * seqlen_k = seq_lens, the block table and causal masking; section 6.4: the
+ * shared-prefix pass of cascade attention is the same call without the
+ * causal mask).  On the tensor cores (tcgen05).
+ *
+ *   out              [num_tokens, num_heads, head_size], dtype; rows of tokens
+ *                    outside every request's range are left untouched.
+ *   lse              NULL, or float32 [num_tokens, num_heads]: the natural log
+ *                    of each row's softmax denominator, log sum_t exp(scale q.k_t).
+ *   q                [num_tokens, num_heads, head_size], dtype.  The q_len =
+ *                    query_start_loc[r+1] - query_start_loc[r] rows of request
+ *                    r are its last q_len tokens: row i sits at position
+ *                    seq_lens[r] - q_len + i, and its keys/values must already
+ *                    be in the pool (pa_reshape_and_cache first).
+ *   kv_cache         the pool [2, num_blocks, block_size, num_kv_heads, head_size].
+ *   block_tables     int32, row r at block_tables + r * block_table_stride,
+ *                    its first ceil(seq_lens[r] / block_size) entries used
+ *                    (max_blocks_per_seq <= block_table_stride entries per row).
+ *   seq_lens         int32 [num_reqs]: cached tokens of request r, the new
+ *                    ones included (q_len <= seq_len).
+ *   query_start_loc  int32 [num_reqs + 1], non-decreasing, from 0 to at most
+ *                    num_tokens.
+ *   max_query_len    an upper bound of every q_len (sets the grid).
+ *   causal           1: position p attends keys 0..p; 0: every key of the
+ *                    request.
+ * Query head h reads kv head h / (num_heads / num_kv_heads).  head_size 64
+ * or 128, block_size 16 or 32.  A request whose metadata breaks these rules
+ * (q_len < 0 or > max_query_len, seq_len < q_len or beyond its table,
+ * query_start_loc outside [0, num_tokens]) is skipped and flagged
+ * (PA_DEVERR_SEQ_LEN); block ids outside the pool read zeros and are flagged
+ * (PA_DEVERR_BLOCK_ID).
+ */
+pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
+                     const int32_t *block_tables, int64_t block_table_stride,
+                     const int32_t *seq_lens, const int32_t *query_start_loc, int num_reqs,
+                     int num_tokens, int max_query_len, int num_heads, int num_kv_heads,
+                     int head_size, int block_size, int num_blocks, int max_blocks_per_seq,
+                     float scale, int causal, pa_dtype dtype, void *stream);
 
 /*
  * Copy whole blocks of the pool, for copy-on-write (k4i.top "paged

@@ -19,7 +19,7 @@ __all__ = [
     "PAError", "lib_path", "pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
     "pa_decode_splitk_workspace_size", "pa_decode_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "pa_validate_tables", "pa_validate_slots",
-    "pa_device_errors", "pa_selftest_wait_timeout", "pa_copy_blocks",
+    "pa_device_errors", "pa_selftest_wait_timeout", "pa_copy_blocks", "pa_prefill",
     "pa_validate_block_mapping", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
@@ -58,6 +58,9 @@ _lib.pa_validate_slots.restype = _I
 _lib.pa_validate_slots.argtypes = [_P, _I, _I, _I]
 _lib.pa_device_errors.restype = _I
 _lib.pa_device_errors.argtypes = [ctypes.POINTER(_U), _I]
+_lib.pa_prefill.restype = _I
+_lib.pa_prefill.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                            _I, _F, _I, _I, _P]
 _lib.pa_copy_blocks.restype = _I
 _lib.pa_copy_blocks.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _P]
 _lib.pa_validate_block_mapping.restype = _I
@@ -228,6 +231,49 @@ def pa_validate_slots(slot_mapping: torch.Tensor, block_size: int, num_blocks: i
     sm = slot_mapping.detach().to("cpu", torch.int64).contiguous()
     return _lib.pa_validate_slots(ctypes.c_void_p(sm.data_ptr()), int(sm.numel()), block_size,
                                   num_blocks)
+
+
+def pa_prefill(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+               block_tables: torch.Tensor, seq_lens: torch.Tensor,
+               query_start_loc: torch.Tensor, scale: float, block_size: int,
+               max_query_len: int, causal: bool = True, lse: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """Prefill / chunked-prefill attention of the packed query rows q [T, H, D]
+    to each request's paged keys; writes and returns ``out``.  ``block_tables``
+    may be a column slice of a larger table (rows contiguous, any row stride).
+    ``lse`` (float32 [T, H]) receives the natural-log softmax denominators."""
+    nb, hkv, d = _pool_dims(kv_cache, block_size)
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
+        raise ValueError("q must be contiguous [num_tokens, H, head_size]")
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be contiguous and match q")
+    if q.dtype != kv_cache.dtype or q.dtype not in _DTYPE:
+        raise ValueError("q, kv_cache and out must share dtype float16 or bfloat16")
+    T, H = int(q.shape[0]), int(q.shape[1])
+    R = int(seq_lens.numel())
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != R or block_tables.stride(1) != 1 or \
+            block_tables.stride(0) < block_tables.shape[1]:
+        raise ValueError("block_tables must be int32 [R, max_blocks] with contiguous rows")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be contiguous int32 [R]")
+    if query_start_loc.dtype != torch.int32 or query_start_loc.numel() != R + 1 or \
+            not query_start_loc.is_contiguous():
+        raise ValueError("query_start_loc must be contiguous int32 [R + 1]")
+    lse_ptr = ctypes.c_void_p(0)
+    if lse is not None:
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (T, H) or not lse.is_contiguous():
+            raise ValueError("lse must be contiguous float32 [num_tokens, H]")
+        lse_ptr = _dev(lse, "lse")
+    if R == 0 or T == 0:
+        return out
+    _check(_lib.pa_prefill(_dev(out, "out"), lse_ptr, _dev(q, "q"), _dev(kv_cache, "kv_cache"),
+                           _dev(block_tables, "block_tables"), int(block_tables.stride(0)),
+                           _dev(seq_lens, "seq_lens"), _dev(query_start_loc, "query_start_loc"),
+                           R, T, int(max_query_len), H, hkv, d, block_size, nb,
+                           max(1, int(block_tables.shape[1])), float(scale),
+                           1 if causal else 0, _DTYPE[q.dtype], _stream(stream)), "pa_prefill")
+    return out
 
 
 def pa_copy_blocks(kv_cache: torch.Tensor, block_mapping: torch.Tensor, block_size: int,

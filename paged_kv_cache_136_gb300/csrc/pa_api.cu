@@ -113,6 +113,26 @@ static bool make_q_map(CUtensorMap *map, const void *q, int dtype, int rows, int
     return r == CUDA_SUCCESS;
 }
 
+// Packed query rows [T, H, D] as a 3-D tensor {D, H, T}; a box is 64
+// elements of one head for 128 consecutive tokens, with the 128-byte swizzle.
+static bool make_q_rows_map(CUtensorMap *map, const void *q, int dtype, int num_tokens,
+                            int num_heads, int head_size)
+{
+    cudaError_t err;
+    auto fn = encode_fn(&err);
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)head_size, (cuuint64_t)num_heads, (cuuint64_t)num_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)head_size * 2, (cuuint64_t)num_heads * head_size * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void *>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static int sm_count(cudaError_t *err)
 {
     static int count[64] = {0};
@@ -577,6 +597,68 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
     ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size, len_cap,
                       0};
     e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
+                     const int32_t *block_tables, int64_t block_table_stride,
+                     const int32_t *seq_lens, const int32_t *query_start_loc, int num_reqs,
+                     int num_tokens, int max_query_len, int num_heads, int num_kv_heads,
+                     int head_size, int block_size, int num_blocks, int max_blocks_per_seq,
+                     float scale, int causal, pa_dtype dtype, void *stream)
+{
+    if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
+        num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_size <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+        block_table_stride < max_blocks_per_seq || !isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if ((head_size != 64 && head_size != 128) || (block_size != 16 && block_size != 32) ||
+        (dtype != PA_FP16 && dtype != PA_BF16))
+        return PA_ERR_UNSUPPORTED;
+    if (num_reqs == 0 || num_tokens == 0 || max_query_len == 0)
+        return PA_OK;
+    if (!out || !q || !kv_cache || !block_tables || !seq_lens || !query_start_loc)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(lse, 4) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)num_blocks * block_size >= (int64_t)INT32_MAX ||
+        (int64_t)max_blocks_per_seq * block_size >= (int64_t)INT32_MAX ||
+        (int64_t)num_tokens + 512 >= (int64_t)INT32_MAX || num_heads > 65535 ||
+        num_reqs > 65535)
+        return PA_ERR_UNSUPPORTED;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    alignas(64) CUtensorMap pmap, qmap;
+    if (!make_pool_map(&pmap, kv_cache, dtype, num_blocks, block_size, num_kv_heads, head_size,
+                       1, block_size) ||
+        !make_q_rows_map(&qmap, q, dtype, num_tokens, num_heads, head_size))
+        return PA_ERR_CUDA;
+    PrefillParams p{};
+    p.out = out;
+    p.lse = lse;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.query_start_loc = query_start_loc;
+    p.err = err;
+    p.bt_stride = block_table_stride;
+    p.num_tokens = num_tokens;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_query_len = max_query_len;
+    p.causal = causal ? 1 : 0;
+    p.qscale = scale * kLog2e;
+    const dim3 grid((unsigned)((max_query_len + 255) / 256), (unsigned)num_heads,
+                    (unsigned)num_reqs);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = dtype == PA_BF16 ? launch_prefill_bf16(head_size, block_size, pmap, qmap, p, grid, st)
+                         : launch_prefill_f16(head_size, block_size, pmap, qmap, p, grid, st);
+    if (e == cudaErrorNotSupported)
+        return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

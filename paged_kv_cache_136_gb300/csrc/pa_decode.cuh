@@ -34,10 +34,6 @@
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
-#define PA_DEVERR_BLOCK_ID_ 0x1u
-#define PA_DEVERR_SEQ_LEN_ 0x2u
-#define PA_DEVERR_TIMEOUT_ 0x8u
-
 namespace pa {
 
 constexpr int kConsumerWarps = 4;

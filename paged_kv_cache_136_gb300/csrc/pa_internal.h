@@ -6,6 +6,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Bits of the sticky device error word (the same values as PA_DEVERR_* in
+// pa.h, which the kernels' translation units do not include).
+#define PA_DEVERR_BLOCK_ID_ 0x1u
+#define PA_DEVERR_SEQ_LEN_ 0x2u
+#define PA_DEVERR_TIMEOUT_ 0x8u
+
 namespace pa {
 
 // Kernel parameters of the decode kernels (one-pass and split-K partition).
@@ -79,5 +85,27 @@ cudaError_t launch_decode_tc_f16(int block_size, int group, int hg, bool split,
 cudaError_t launch_decode_tc_bf16(int block_size, int group, int hg, bool split,
                                   const CUtensorMap &pool, const CUtensorMap &qmap,
                                   const tc::TcParams &p, dim3 grid, cudaStream_t stream);
+
+// Parameters of the tensor-core prefill kernel.
+struct PrefillParams {
+    void *out;                      // [num_tokens, H, D]
+    float *lse;                     // [num_tokens, H] natural log, or null
+    const int32_t *block_tables;    // row r at block_tables + r * bt_stride
+    const int32_t *seq_lens;        // [R]
+    const int32_t *query_start_loc; // [R + 1]
+    unsigned int *err;
+    long long bt_stride;
+    int num_tokens, num_heads, num_kv_heads, num_blocks, max_blocks, max_query_len;
+    int causal;
+    float qscale;                   // scale * log2(e)
+};
+
+// Prefill over the paged cache on grid (ceil(max_query_len/256), H, R).
+cudaError_t launch_prefill_f16(int head_size, int block_size, const CUtensorMap &pool,
+                               const CUtensorMap &qmap, const PrefillParams &p, dim3 grid,
+                               cudaStream_t stream);
+cudaError_t launch_prefill_bf16(int head_size, int block_size, const CUtensorMap &pool,
+                                const CUtensorMap &qmap, const PrefillParams &p, dim3 grid,
+                                cudaStream_t stream);
 
 } // namespace pa

@@ -1,0 +1,515 @@
+// pa_prefill_tc.cuh -- prefill and chunked prefill over the paged KV cache on
+// the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// What it computes ("PagedAttention 在 vLLM 中的实现分析", section 6.2: the
+// batch's new query tokens, packed by query_start_loc, attend the paged keys
+// of their request with seqlen_k = seq_lens, through the block table, with
+// causal masking; section 6.4: the shared-prefix pass is the same attention
+// without the causal mask).  Query row i of request r sits at position
+// seq_len - q_len + i and attends keys 0..position (causal) or every key.
+//
+// A CTA owns 256 query rows of one (request, query head): two tiles of 128
+// rows, each with its own softmax warpgroup, so the tensor cores work on one
+// tile while the other tile's softmax runs.  Roles in a CTA of 320 threads:
+//
+//   warp 8 (producer)  TMA-loads the two query tiles once, then K and V tiles
+//                      of 128 keys into a ring of shared-memory slots, one
+//                      box {64 elements, 1 kv head, block_size rows} per lane
+//                      and block ("Paged attention", k4i.top, section "block
+//                      table": physical_block = block_table[t // block_size]).
+//   warp 9 (MMA)       owns all 512 TMEM columns and issues, per key tile k
+//                      and query tile t,
+//                        S_t = Q_t K_k^T          (M=128, N=128, K=head_size)
+//                        O_t (+)= P_t V_k         (M=128, N=head_size, K=128)
+//                      with P_t read from tensor memory (A operand) and V_k as
+//                      an MN-major shared-memory operand.
+//   warps 0-3 / 4-7    one query row per thread (TMEM lane): scale and mask
+//   (softmax, tile 0/1) the row's 128 scores, row max, base-2 exponentials,
+//                      write P over S as 16-bit values (bf16: a high part in
+//                      columns 0-63 and the rounded remainder in 64-127, so P
+//                      keeps ~16 significant bits), and at the end
+//                      out = O / l (and the log-sum-exp when asked).
+//
+// The running maximum is updated lazily: O and l are rescaled only when a key
+// tile raises a row's maximum by more than 2^8, so most tiles skip the rescale
+// and P stays below 2^8 (exact in fp16/bf16 range).  Every key row past
+// seq_len that a tile could hold is zeroed in shared memory before the values
+// MMA reads it, so stale or NaN bytes never reach O.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace pf {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTileM = 128;         // query rows per tile
+constexpr int kTileN = 128;         // keys per K/V tile
+constexpr int kRowsPerCta = 2 * kTileM;
+constexpr float kRescaleLog2 = 8.f; // lazy-rescale threshold, log2 units
+constexpr uint32_t kTmemCols = 512; // S0, S1, O0, O1: 128 columns each
+constexpr int kRegion = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+
+template <int D>
+struct Geo {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kTileBytes = kHalves * kRegion; // a Q, K or V tile
+    static constexpr int kSlots = D == 128 ? 4 : 8;      // K/V ring
+    static constexpr int kOffKV = 2 * kTileBytes;        // after the two Q tiles
+    static constexpr int kOffMisc = kOffKV + kSlots * kTileBytes;
+};
+
+struct Misc {
+    uint64_t q_full;
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+};
+
+template <int D>
+constexpr int smem_bytes()
+{
+    return 1024 + Geo<D>::kOffMisc + (int)sizeof(Misc);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b)
+{
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Warp-uniform bounded wait driven by lane 0.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane)
+{
+    bool ok = true;
+    if (lane == 0)
+        ok = mbar_wait(bar, parity);
+    return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+}
+
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap pool_map,
+                      const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
+{
+    using Gm = Geo<D>;
+    constexpr int NH = Gm::kHalves;
+    constexpr int TB = Gm::kTileBytes;
+    constexpr int S = Gm::kSlots;
+    constexpr int BPT = kTileN / BS; // pool blocks per key tile
+    static_assert(32 % BPT == 0 && BPT * NH <= 32, "key tile geometry");
+    constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    // bf16 keeps only 8 significant bits: P then travels as a high part plus
+    // the rounded remainder (two MMAs on the same V), fp16's 11 bits suffice.
+    constexpr bool kSplitP = kFmt == 1u;
+    constexpr uint32_t kIdescS = idesc_f16_f32(kFmt, 0, 0, kTileM, kTileN);
+    constexpr uint32_t kIdescO = idesc_f16_f32(kFmt, 0, 1, kTileM, D);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc *m = reinterpret_cast<Misc *>(smem + Gm::kOffMisc);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+255
+    const int r = blockIdx.z;
+    const int h = blockIdx.y;
+    const int qb = (int)gridDim.x - 1 - (int)blockIdx.x; // latest (heaviest) rows first
+    const int i0 = qb * kRowsPerCta;
+    const int q0 = __ldg(p.query_start_loc + r);
+    const int q1 = __ldg(p.query_start_loc + r + 1);
+    const int L = __ldg(p.seq_lens + r);
+    const int q_len = q1 - q0;
+    if (q0 < 0 || q1 > p.num_tokens || q_len < 0 || q_len > p.max_query_len || L < q_len ||
+        L > p.max_blocks * BS) {
+        if (tid == 0 && qb == 0 && h == 0)
+            atomicOr(p.err, PA_DEVERR_SEQ_LEN_);
+        return;
+    }
+    if (i0 >= q_len)
+        return;
+    const int ctx = L - q_len;
+    int nv[2], nt[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        nv[t] = min(max(q_len - (i0 + t * kTileM), 0), kTileM);
+        const int ext = p.causal ? min(L, ctx + i0 + t * kTileM + nv[t]) : L;
+        nt[t] = nv[t] > 0 ? (ext + kTileN - 1) / kTileN : 0;
+    }
+    const int n = max(nt[0], nt[1]); // key tiles loaded
+    const bool tail = n * kTileN > L; // the last key tile reaches past seq_len
+    const int fixer = nt[1] == n ? 1 : 0;
+
+    if (tid == 0) {
+        mbar_init(&m->q_full, 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&m->kv_full[i], 1);
+            mbar_init(&m->kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&m->s_full[i], 1);
+            mbar_init(&m->p_full[i], 4);
+            mbar_init(&m->o_done[i], 1);
+        }
+        mbar_init(&m->drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&m->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = m->tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ================================================================ producer
+        const int kvh = h / (p.num_heads / p.num_kv_heads);
+        if (lane == 0) {
+            prefetch_tensormap(&pool_map);
+            prefetch_tensormap(&q_map);
+            mbar_arrive_expect_tx(&m->q_full, (uint32_t)((nv[1] > 0 ? 2 : 1) * TB));
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (nv[t] > 0)
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf)
+                        tma_load_3d(smem + t * TB + hf * kRegion, &q_map, &m->q_full, hf * 64, h,
+                                    q0 + i0 + t * kTileM);
+        }
+        // Block-table entries of 64 blocks live in lane registers (this
+        // window and the next), refreshed every 32 blocks.
+        const int nblk_req = (L + BS - 1) / BS;
+        const int32_t *bt = p.block_tables + (size_t)r * (size_t)p.bt_stride;
+        int cb = 0;
+        int cur = lane < nblk_req ? __ldg(bt + lane) : -1;
+        int nxt = 32 + lane < nblk_req ? __ldg(bt + 32 + lane) : -1;
+        for (int g = 0; g < 2 * n; ++g) {
+            const int k = g >> 1, plane = g & 1, slot = g % S;
+            if (g >= S && !warp_wait(&m->kv_empty[slot], ((g / S) - 1) & 1, lane)) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+                break;
+            }
+            const int jt = k * BPT;
+            if (jt >= cb + 32) {
+                cb += 32;
+                cur = nxt;
+                nxt = cb + 32 + lane < nblk_req ? __ldg(bt + cb + 32 + lane) : -1;
+            }
+            const int nblk = min(BPT, nblk_req - jt);
+            if (lane == 0)
+                mbar_arrive_expect_tx(&m->kv_full[slot], (uint32_t)(nblk * BS * D * 2));
+            __syncwarp();
+            const int c = lane / NH, hf = lane % NH;
+            const int phys = __shfl_sync(0xffffffffu, cur, (jt + min(c, BPT - 1) - cb) & 31);
+            if (lane < nblk * NH) {
+                int row;
+                if (phys < 0 || phys >= p.num_blocks) {
+                    atomicOr(p.err, PA_DEVERR_BLOCK_ID_);
+                    row = p.num_blocks * BS; // past the extent: zero fill
+                } else {
+                    row = phys * BS;
+                }
+                tma_load_4d(smem + Gm::kOffKV + slot * TB + hf * kRegion + c * BS * 128,
+                            &pool_map, &m->kv_full[slot], hf * 64, kvh, row, plane);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ===================================================== MMA issuer
+        auto issue_qk = [&](int t, int slot) {
+            const uint32_t qa = smem_addr(smem + t * TB);
+            const uint32_t ka = smem_addr(smem + Gm::kOffKV + slot * TB);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
+                umma_f16(tmem + (uint32_t)(t * 128), smem_desc_sw128(qa + off, 16, 1024),
+                         smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&m->s_full[t]);
+        };
+        auto issue_pv = [&](int t, int slot, bool acc) {
+            const uint32_t va = smem_addr(smem + Gm::kOffKV + slot * TB);
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk) {
+                const uint64_t vd = smem_desc_sw128(va + kk * 2048, kRegion, 1024);
+                umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128), tmem + (uint32_t)(t * 128 + kk * 8),
+                                vd, kIdescO, (acc || kk > 0) ? 1u : 0u);
+                if (kSplitP) // the low parts of P, 64 columns further on
+                    umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128),
+                                    tmem + (uint32_t)(t * 128 + 64 + kk * 8), vd, kIdescO, 1u);
+            }
+        };
+        bool ok = warp_wait(&m->q_full, 0, lane) && warp_wait(&m->kv_full[0], 0, lane);
+        if (ok) {
+            tc_fence_after_sync();
+            if (lane == 0) {
+                for (int t = 0; t < 2; ++t)
+                    if (nt[t] > 0)
+                        issue_qk(t, 0);
+                umma_commit(&m->kv_empty[0]);
+            }
+            __syncwarp();
+        }
+        for (int k = 0; ok && k < n; ++k) {
+            const int gv = 2 * k + 1, sv = gv % S;
+            ok = warp_wait(&m->kv_full[sv], (gv / S) & 1, lane);
+            // The last tile's rows past seq_len are zeroed by one softmax
+            // warpgroup before it hands over its P; no values MMA of that
+            // tile may start earlier.
+            if (ok && tail && k == n - 1)
+                ok = warp_wait(&m->p_full[fixer], k & 1, lane);
+            bool next_ready = false;
+            const int gk = 2 * k + 2, sk = gk % S;
+            for (int t = 0; ok && t < 2; ++t) {
+                if (k >= nt[t])
+                    continue;
+                ok = warp_wait(&m->p_full[t], k & 1, lane);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                if (lane == 0)
+                    issue_pv(t, sv, k > 0);
+                if (k + 1 < nt[t]) {
+                    if (!next_ready) {
+                        ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
+                        if (!ok)
+                            break;
+                        tc_fence_after_sync();
+                        next_ready = true;
+                    }
+                    if (lane == 0)
+                        issue_qk(t, sk);
+                } else if (lane == 0) {
+                    umma_commit(&m->o_done[t]);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                umma_commit(&m->kv_empty[sv]);
+                if (next_ready)
+                    umma_commit(&m->kv_empty[sk]);
+            }
+            __syncwarp();
+        }
+        if (!ok && lane == 0)
+            atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+        // Drain: every MMA issued completes before TMEM is freed.
+        if (lane == 0)
+            umma_commit(&m->drain);
+        warp_wait(&m->drain, 0, lane);
+    } else {
+        // =========================================== softmax / epilogue (tiles 0, 1)
+        const int wg = warp >> 2;
+        const int row = tid & 127;
+        const uint32_t lane_base = (uint32_t)(((warp & 3) * 32) << 16);
+        const uint32_t s_addr = tmem + lane_base + (uint32_t)(wg * 128);
+        const uint32_t o_addr = tmem + lane_base + (uint32_t)(256 + wg * 128);
+        const int ntt = nt[wg];
+        if (ntt > 0) {
+            const int pos = ctx + i0 + wg * kTileM + row;
+            const int lim = p.causal ? min(L, pos + 1) : L;              // keys < lim
+            const int lim_lo = p.causal ? min(L, ctx + i0 + wg * kTileM + 1) : L;
+            const float qs = p.qscale;
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int k = 0; k < ntt; ++k) {
+                ok = warp_wait(&m->s_full[wg], k & 1, lane);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                // The row's 128 scores, as raw bits, then scaled in place.
+                uint32_t sv[kTileN];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32_nowait(s_addr + (uint32_t)(c * 32),
+                                     *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+                tmem_wait_ld();
+                float mx = -INFINITY;
+                if ((k + 1) * kTileN > lim_lo) {
+                    const int kl = lim - k * kTileN; // keys of this tile below the limit
+#pragma unroll
+                    for (int i = 0; i < kTileN; ++i) {
+                        const float x = i < kl ? __uint_as_float(sv[i]) * qs : -INFINITY;
+                        sv[i] = __float_as_uint(x);
+                        mx = fmaxf(mx, x);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTileN; ++i) {
+                        const float x = __uint_as_float(sv[i]) * qs;
+                        sv[i] = __float_as_uint(x);
+                        mx = fmaxf(mx, x);
+                    }
+                }
+                float alpha = 1.f;
+                bool need = false;
+                if (k == 0) {
+                    m_used = mx;
+                } else if (mx > m_used + kRescaleLog2) {
+                    alpha = ex2(m_used - mx);
+                    m_used = mx;
+                    l *= alpha;
+                    need = true;
+                }
+                const float mu = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16], lo[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2(__uint_as_float(sv[c * 32 + 2 * j]) - mu);
+                        const float p1 = ex2(__uint_as_float(sv[c * 32 + 2 * j + 1]) - mu);
+                        l += p0 + p1;
+                        pk[j] = pack2<T>(p0, p1);
+                        if (kSplitP) {
+                            const float h0 = __uint_as_float(pk[j] << 16);
+                            const float h1 = __uint_as_float(pk[j] & 0xFFFF0000u);
+                            lo[j] = pack2<T>(p0 - h0, p1 - h1);
+                        }
+                    }
+                    tmem_st16(s_addr + (uint32_t)(c * 16), pk);
+                    if (kSplitP)
+                        tmem_st16(s_addr + (uint32_t)(64 + c * 16), lo);
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    // O holds the values of key tiles 0..k-1 (their MMAs are
+                    // complete: S_k was committed after them).  Done after P
+                    // is written so the scores' registers are free.
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32_nowait(o_addr + (uint32_t)(c * 32), v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                        tmem_st32(o_addr + (uint32_t)(c * 32), v);
+                    }
+                }
+                tmem_wait_st();
+                if (tail && wg == fixer && k == n - 1) {
+                    // Zero the V rows of keys >= seq_len in the last tile.
+                    const int gv = 2 * k + 1;
+                    ok = warp_wait(&m->kv_full[gv % S], (gv / S) & 1, lane);
+                    if (ok && k * kTileN + row >= L) {
+                        uint8_t *vrow = smem + Gm::kOffKV + (gv % S) * TB + row * 128;
+#pragma unroll
+                        for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4 *>(vrow + hf * kRegion + c * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&m->p_full[wg]);
+                if (!ok)
+                    break;
+            }
+            if (ok)
+                ok = warp_wait(&m->o_done[wg], 0, lane);
+            if (!ok) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+            } else {
+                tc_fence_after_sync();
+                const bool valid = row < nv[wg];
+                const size_t tok = (size_t)(q0 + i0 + wg * kTileM + row);
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                T *o = reinterpret_cast<T *>(p.out) + (tok * p.num_heads + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32_nowait(o_addr + (uint32_t)(c * 32), v);
+                    tmem_wait_ld();
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = pack2<T>(__uint_as_float(v[2 * j]) * inv,
+                                        __uint_as_float(v[2 * j + 1]) * inv);
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    }
+                }
+                if (p.lse && valid)
+                    p.lse[tok * p.num_heads + h] =
+                        l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_one(const CUtensorMap &pool, const CUtensorMap &qmap, const PrefillParams &p,
+                       dim3 grid, cudaStream_t stream)
+{
+    auto kern = prefill_tc_kernel<T, D, BS>;
+    constexpr int kSmem = smem_bytes<D>();
+    static unsigned long long done_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess)
+            return e;
+        __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
+    }
+    kern<<<grid, kThreads, kSmem, stream>>>(pool, qmap, p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch(int head_size, int block_size, const CUtensorMap &pool, const CUtensorMap &qmap,
+                   const PrefillParams &p, dim3 grid, cudaStream_t stream)
+{
+    if (head_size == 128 && block_size == 16)
+        return launch_one<T, 128, 16>(pool, qmap, p, grid, stream);
+    if (head_size == 128 && block_size == 32)
+        return launch_one<T, 128, 32>(pool, qmap, p, grid, stream);
+    if (head_size == 64 && block_size == 16)
+        return launch_one<T, 64, 16>(pool, qmap, p, grid, stream);
+    if (head_size == 64 && block_size == 32)
+        return launch_one<T, 64, 32>(pool, qmap, p, grid, stream);
+    return cudaErrorNotSupported;
+}
+
+} // namespace pf
+} // namespace pa

@@ -28,6 +28,31 @@ def oracle_decode(w: Workload, items=None, cache_bits=None) -> np.ndarray:
                       w.num_kv_heads, w.block_size, w.scale, ORACLE_DTYPE[w.dtype], items=items)
 
 
+def oracle_prefill(w, items=None, cache_bits=None, causal=True, block_tables=None,
+                   seq_lens=None):
+    """fp64 (out, lse) of a prefill workload from the oracle."""
+    orc = get_oracle()
+    cb = cache_bits if cache_bits is not None else bits(w.kv_cache)
+    bt = (w.block_tables if block_tables is None else block_tables).cpu().numpy()
+    sl = (w.seq_lens if seq_lens is None else seq_lens).cpu().numpy()
+    return orc.prefill(bits(w.q), cb, bt, sl, w.query_start_loc.cpu().numpy(), w.num_kv_heads,
+                       w.block_size, w.scale, ORACLE_DTYPE[w.dtype], causal=causal,
+                       items=items)
+
+
+def check_lse(got: torch.Tensor, ref: np.ndarray, items=None, what: str = ""):
+    """Log-sum-exps agree to 1e-3 absolute (the scores are fp32 dot products
+    of 16-bit inputs; the log of the denominator is insensitive to P's
+    16-bit rounding)."""
+    g = got.detach().cpu().numpy().astype(np.float64).reshape(-1)
+    r = np.asarray(ref).reshape(-1)
+    if items is not None:
+        g, r = g[np.asarray(items)], r[np.asarray(items)]
+    assert np.isfinite(g).all() and np.isfinite(r).all(), f"{what}: non-finite lse"
+    err = np.abs(g - r)
+    assert (err <= 1e-3 + 1e-4 * np.abs(r)).all(), f"{what}: lse max err {err.max()}"
+
+
 def oracle_reshape(w: Workload, cache_bits=None) -> np.ndarray:
     orc = get_oracle()
     cb = cache_bits if cache_bits is not None else bits(w.kv_cache)

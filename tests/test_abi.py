@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     for n in ("pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
               "pa_decode_splitk_workspace_size", "pa_validate_tables", "pa_validate_slots",
               "pa_device_errors", "pa_status_string", "pa_version", "pa_copy_blocks",
-              "pa_validate_block_mapping", "pa_selftest_wait_timeout"):
+              "pa_validate_block_mapping", "pa_selftest_wait_timeout", "pa_prefill"):
         assert n in names
 
 
@@ -188,3 +188,29 @@ def test_copy_blocks_rejects_bad_arguments(pa):
     assert f(FAKE, FAKE, 3, 10, 16, 2, 64, 7, None) == 2      # dtype
     assert f(0, FAKE, 3, 10, 16, 2, 64, 0, None) == 1         # null pool
     assert f(FAKE, FAKE, 0, 10, 16, 2, 64, 0, None) == 0      # nothing to copy
+
+
+def test_prefill_rejects_bad_arguments(pa):
+    lib = _raw(pa)
+    f = lib.pa_prefill
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 2 +
+                  [ctypes.c_int] * 9 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p])
+    P = [FAKE, 0, FAKE, FAKE, FAKE, 8, FAKE, FAKE]
+    ok = dict(R=2, T=10, mq=8, H=4, Hkv=2, D=128, bs=16, NB=10, MB=8)
+
+    def call(P=P, scale=0.1, causal=1, dtype=0, **kw):
+        a = {**ok, **kw}
+        return f(*P, a["R"], a["T"], a["mq"], a["H"], a["Hkv"], a["D"], a["bs"], a["NB"],
+                 a["MB"], scale, causal, dtype, None)
+    assert call(D=96) == 2                                    # head_size
+    assert call(bs=8) == 2                                    # block_size
+    assert call(dtype=5) == 2
+    assert call(Hkv=3) == 1                                   # H % Hkv
+    assert call(MB=9) == 1                                    # stride < max blocks
+    assert call(scale=float("nan")) == 1
+    assert call(T=0) == 0                                     # nothing to do
+    assert call(R=0) == 0
+    assert call(P=[FAKE + 2] + P[1:]) == 1                    # misaligned out
+    assert call(P=[0] + P[1:]) == 1                           # null out
