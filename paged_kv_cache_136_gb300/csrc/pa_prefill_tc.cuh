@@ -339,30 +339,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                // The row's 128 scores, as raw bits, then scaled in place.
+                // The row's 128 raw scores (bits).
                 uint32_t sv[kTileN];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     tmem_ld32_nowait(s_addr + (uint32_t)(c * 32),
                                      *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
                 tmem_wait_ld();
-                float mx = -INFINITY;
+                // Row max over the raw scores (scale > 0 commutes with max),
+                // in 8 independent chains; masked keys become -inf.
+                float m8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    m8[j] = -INFINITY;
                 if ((k + 1) * kTileN > lim_lo) {
                     const int kl = lim - k * kTileN; // keys of this tile below the limit
 #pragma unroll
                     for (int i = 0; i < kTileN; ++i) {
-                        const float x = i < kl ? __uint_as_float(sv[i]) * qs : -INFINITY;
+                        const float x = i < kl ? __uint_as_float(sv[i]) : -INFINITY;
                         sv[i] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
+                        m8[i & 7] = fmaxf(m8[i & 7], x);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < kTileN; ++i) {
-                        const float x = __uint_as_float(sv[i]) * qs;
-                        sv[i] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
-                    }
+                    for (int i = 0; i < kTileN; ++i)
+                        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
                 }
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qs;
                 float alpha = 1.f;
                 bool need = false;
                 if (k == 0) {
@@ -373,15 +377,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= alpha;
                     need = true;
                 }
-                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                // p = 2^(S * scale*log2e - m): one FFMA and one ex2 per key;
+                // the row sum in 4 independent chains.
+                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16], lo[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2(__uint_as_float(sv[c * 32 + 2 * j]) - mu);
-                        const float p1 = ex2(__uint_as_float(sv[c * 32 + 2 * j + 1]) - mu);
-                        l += p0 + p1;
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j]), qs, nmu));
+                        const float p1 =
+                            ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j + 1]), qs, nmu));
+                        l4[j & 3] += p0 + p1;
                         pk[j] = pack2<T>(p0, p1);
                         if (kSplitP) {
                             const float h0 = __uint_as_float(pk[j] << 16);
@@ -393,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kSplitP)
                         tmem_st16(s_addr + (uint32_t)(64 + c * 16), lo);
                 }
+                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 if (__any_sync(0xffffffffu, need)) {
                     // O holds the values of key tiles 0..k-1 (their MMAs are
                     // complete: S_k was committed after them).  Done after P
