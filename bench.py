@@ -501,6 +501,61 @@ def prefill_workload(name: str, args, peaks: dict) -> dict:
     return res
 
 
+def cascade_workload(args, peak_gbs: float) -> dict:
+    """The shared-prefix workload through pa_cascade_decode (prefix attended
+    once for all sequences, suffixes split-K, merged), with the cache write,
+    timed like the other workloads.  Throughput is reported on the same
+    logical KV bytes as the plain decode (every sequence's full length), and
+    on the distinct bytes the cascade has to read."""
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    w = wl.make("prefix", device="cuda")
+    out = torch.empty_like(w.q)
+    msl = int(w.seq_lens.max().item())
+    pb = w.meta["shared_blocks"]
+    P = args.partition
+    n = pa.pa_cascade_decode_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                            w.block_tables.shape[1], pb, msl, w.block_size, P)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pa.pa_cascade_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                             w.block_size, pb, msl, ws, P)
+
+    for _ in range(5):
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        call()
+    k = max(3, args.workload_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k)]
+    torch.cuda.synchronize()
+    for i in range(k):
+        ev[i][0].record(stream)
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        ev[i][1].record(stream)
+        call()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    kvb = kv_bytes(w)
+    ub = w.unique_kv_bytes()
+    res = {"name": "prefix_cascade", "call": "pa_cascade_decode", "workload": WORKLOAD_TEXT["prefix"],
+           "prefix_blocks": pb, "partition_size": P, "steps": k,
+           "kv_bytes_per_step": kvb, "unique_kv_bytes_per_step": ub,
+           "ms_per_call": round(ms, 5), "ms_per_step": round(step_ms, 5),
+           "decode_gbs_logical": round(kvb / ms / 1e6, 2),
+           "decode_gbs_unique": round(ub / ms / 1e6, 2),
+           "unique_frac_of_peak": round(ub / ms / 1e6 / peak_gbs, 4),
+           "seqs_per_s": round(w.num_seqs / (step_ms / 1e3), 1),
+           "gpu_launches_per_call": 5 + (1 if msl - pb * w.block_size > P else 0),
+           "device_error_flags": pa.pa_device_errors(clear=True)}
+    del w, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def other_workload(name: str, args, peak_gbs: float) -> dict:
     """Short device-resident measurement of another workload through the same
     step (cache write + split-K decode), reported beside the main line."""
@@ -511,6 +566,8 @@ def other_workload(name: str, args, peak_gbs: float) -> dict:
         return copy_blocks_workload(args, peak_gbs)
     if name.startswith("prefill_"):
         return prefill_workload(name, args, measured_peaks())
+    if name == "prefix_cascade":
+        return cascade_workload(args, peak_gbs)
     w = wl.make(name, device="cuda")
     out = torch.empty_like(w.q)
     msl = int(w.seq_lens.max().item())
@@ -614,7 +671,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200,
                     help="steps in the end-to-end (host buffers) measurement")
     ap.add_argument("--workloads",
-                    default="gqa8b,long,prefix,tiny,copy_blocks,prefill_mha7b,prefill_gqa8b",
+                    default="gqa8b,long,prefix,prefix_cascade,tiny,copy_blocks,prefill_mha7b,"
+                            "prefill_gqa8b",
                     help="other workloads measured briefly beside the main line ('' for none)")
     ap.add_argument("--workload-steps", type=int, default=50)
     return ap.parse_args(argv)

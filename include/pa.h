@@ -8,6 +8,9 @@
  *   pa_decode_splitk      partitioned decode attention + log-sum-exp reduce
  *   pa_copy_blocks        copy whole blocks (the device half of copy-on-write)
  *   pa_prefill            prefill / chunked prefill attention over the pool
+ *   pa_decode_splitk_lse  split-K decode that also returns the log-sum-exps
+ *   pa_merge_attn_states  merge two partial attention results
+ *   pa_cascade_decode     decode for sequences sharing a prefix (cascade)
  *
  * Data layout (all tensors contiguous, row-major, caller-owned):
  *
@@ -81,6 +84,8 @@ typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEVERR_SEQ_LEN 0x2u  /* a seq_len outside its allowed range */
 #define PA_DEVERR_SLOT 0x4u     /* a slot >= num_blocks * block_size */
 #define PA_DEVERR_TIMEOUT 0x8u  /* a bounded in-kernel wait ran out */
+#define PA_DEVERR_PREFIX 0x10u  /* cascade: a table does not start with the shared
+                                   prefix blocks, or a seq_len is shorter than it */
 
 /*
  * Write new tokens into the pool ("PagedAttention 在 vLLM 中的实现分析",
@@ -178,6 +183,67 @@ pa_status pa_decode_splitk_noalloc(void *out, const void *q, const void *kv_cach
                                    int block_size, int num_blocks, int max_blocks_per_seq,
                                    float scale, pa_dtype dtype, int max_seq_len,
                                    int partition_size, void *stream);
+
+/*
+ * pa_decode_splitk that also writes each row's log-sum-exp: lse[s][h] =
+ * log sum_t exp(scale * q . k_t), natural log, float32 [num_seqs, num_heads]
+ * (-inf for an empty sequence).  The pieces of a cascade are merged with it
+ * (pa_merge_attn_states).  Arguments and errors as pa_decode_splitk; lse must
+ * be non-NULL and 4-byte aligned.
+ */
+pa_status pa_decode_splitk_lse(void *out, float *lse, const void *q, const void *kv_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                               int block_size, int num_blocks, int max_blocks_per_seq,
+                               float scale, pa_dtype dtype, int max_seq_len, int partition_size,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Merge two attention results over disjoint key sets ("PagedAttention 在 vLLM
+ * 中的实现分析", section 6.4, merge_attn_states: the online-softmax
+ * correction).  Per row (token, head), with M = max(lse_a, lse_b) and
+ * w_x = exp(lse_x - M):
+ *   out = (w_a o_a + w_b o_b) / (w_a + w_b),  out_lse = M + log(w_a + w_b).
+ * A row whose lse is -inf is an empty part; two empty parts give 0 and -inf.
+ *   out, o_a, o_b   [num_tokens, num_heads, head_size], dtype, 16-byte aligned
+ *                   (out may alias o_a or o_b).
+ *   lse_a, lse_b    float32 [num_tokens, num_heads]; out_lse the same or NULL.
+ * head_size 64 or 128.
+ */
+pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const float *lse_a,
+                               const void *o_b, const float *lse_b, int num_tokens,
+                               int num_heads, int head_size, pa_dtype dtype, void *stream);
+
+/*
+ * Workspace bytes of pa_cascade_decode for these sizes (0 on bad sizes).
+ */
+size_t pa_cascade_decode_workspace_size(int num_seqs, int num_heads, int head_size,
+                                        int max_blocks_per_seq, int prefix_blocks,
+                                        int max_seq_len, int block_size, int partition_size);
+
+/*
+ * Cascade decode attention for sequences that share a prefix ("PagedAttention
+ * 在 vLLM 中的实现分析", section 6.4: the common prefix is attended once,
+ * without the causal mask, for all requests; each request's own suffix
+ * separately; merge_attn_states combines them).  The result equals
+ * pa_decode over the full tables.
+ *
+ * The first prefix_blocks entries of every block_tables row must be the same
+ * physical blocks (row 0's), and every seq_len >= prefix_blocks * block_size;
+ * a table or length that breaks this is flagged (PA_DEVERR_PREFIX) and its
+ * output is not defined.  Steps, all on the given stream: a setup kernel
+ * (suffix lengths and tables), one prefill pass of the B queries over the
+ * prefix (tensor cores), a split-K decode of the suffixes with log-sum-exp,
+ * and the merge.  prefix_blocks == 0 is plain pa_decode_splitk.  Other
+ * arguments, layouts and errors as pa_decode_splitk; the workspace must hold
+ * pa_cascade_decode_workspace_size bytes, 256-byte aligned.
+ */
+pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                            int num_heads, int num_kv_heads, int head_size, int block_size,
+                            int num_blocks, int max_blocks_per_seq, int prefix_blocks,
+                            float scale, pa_dtype dtype, int max_seq_len, int partition_size,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Prefill / chunked prefill over the paged cache ("PagedAttention 在 vLLM 中的

@@ -20,6 +20,8 @@ __all__ = [
     "pa_decode_splitk_workspace_size", "pa_decode_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "pa_validate_tables", "pa_validate_slots",
     "pa_device_errors", "pa_selftest_wait_timeout", "pa_copy_blocks", "pa_prefill",
+    "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
+    "pa_cascade_decode_workspace_size",
     "pa_validate_block_mapping", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
@@ -29,6 +31,7 @@ DEVERR_BLOCK_ID = 0x1
 DEVERR_SEQ_LEN = 0x2
 DEVERR_SLOT = 0x4
 DEVERR_TIMEOUT = 0x8
+DEVERR_PREFIX = 0x10
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
 
@@ -58,6 +61,16 @@ _lib.pa_validate_slots.restype = _I
 _lib.pa_validate_slots.argtypes = [_P, _I, _I, _I]
 _lib.pa_device_errors.restype = _I
 _lib.pa_device_errors.argtypes = [ctypes.POINTER(_U), _I]
+_lib.pa_decode_splitk_lse.restype = _I
+_lib.pa_decode_splitk_lse.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                      _I, _I, _I, _P, _SZ, _P]
+_lib.pa_merge_attn_states.restype = _I
+_lib.pa_merge_attn_states.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]
+_lib.pa_cascade_decode_workspace_size.restype = _SZ
+_lib.pa_cascade_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I]
+_lib.pa_cascade_decode.restype = _I
+_lib.pa_cascade_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                   _I, _I, _P, _SZ, _P]
 _lib.pa_prefill.restype = _I
 _lib.pa_prefill.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                             _I, _F, _I, _I, _P]
@@ -192,6 +205,79 @@ def pa_decode_splitk(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
                                  int(max_seq_len), int(partition_size),
                                  _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
            "pa_decode_splitk")
+    return out
+
+
+def _lse_arg(lse, rows: int, cols: int, name: str = "lse"):
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (rows, cols) or not lse.is_contiguous():
+        raise ValueError(f"{name} must be contiguous float32 [{rows}, {cols}]")
+    return _dev(lse, name)
+
+
+def pa_decode_splitk_lse(out: torch.Tensor, lse: torch.Tensor, q: torch.Tensor,
+                         kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                         seq_lens: torch.Tensor, scale: float, block_size: int,
+                         max_seq_len: int, workspace: torch.Tensor, partition_size: int = 512,
+                         stream=None) -> torch.Tensor:
+    """pa_decode_splitk that also writes the natural-log softmax denominators
+    into ``lse`` (float32 [B, H])."""
+    B, H, hkv, d, nb, mb = _decode_common(out, q, kv_cache, block_tables, seq_lens, block_size)
+    lp = _lse_arg(lse, B, H)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_splitk_lse(_dev(out, "out"), lp, _dev(q, "q"),
+                                     _dev(kv_cache, "kv_cache"), _dev(block_tables, "block_tables"),
+                                     _dev(seq_lens, "seq_lens"), B, H, hkv, d, block_size, nb, mb,
+                                     float(scale), _DTYPE[q.dtype], int(max_seq_len),
+                                     int(partition_size), _dev(workspace, "workspace"), ws_bytes,
+                                     _stream(stream)), "pa_decode_splitk_lse")
+    return out
+
+
+def pa_merge_attn_states(out: torch.Tensor, o_a: torch.Tensor, lse_a: torch.Tensor,
+                         o_b: torch.Tensor, lse_b: torch.Tensor,
+                         out_lse: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Merge two partial attention results [T, H, D] given with their
+    log-sum-exps [T, H]; writes and returns ``out``."""
+    for name, t in (("out", out), ("o_a", o_a), ("o_b", o_b)):
+        if t.dim() != 3 or t.shape != o_a.shape or t.dtype != o_a.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [T, H, D] like o_a")
+    if o_a.dtype not in _DTYPE:
+        raise ValueError("dtype must be float16 or bfloat16")
+    T, H, D = (int(x) for x in o_a.shape)
+    la, lb = _lse_arg(lse_a, T, H, "lse_a"), _lse_arg(lse_b, T, H, "lse_b")
+    lo = _lse_arg(out_lse, T, H, "out_lse") if out_lse is not None else ctypes.c_void_p(0)
+    if T == 0:
+        return out
+    _check(_lib.pa_merge_attn_states(_dev(out, "out"), lo, _dev(o_a, "o_a"), la,
+                                     _dev(o_b, "o_b"), lb, T, H, D, _DTYPE[o_a.dtype],
+                                     _stream(stream)), "pa_merge_attn_states")
+    return out
+
+
+def pa_cascade_decode_workspace_size(num_seqs: int, num_heads: int, head_size: int,
+                                     max_blocks_per_seq: int, prefix_blocks: int,
+                                     max_seq_len: int, block_size: int,
+                                     partition_size: int = 512) -> int:
+    return int(_lib.pa_cascade_decode_workspace_size(num_seqs, num_heads, head_size,
+                                                     max_blocks_per_seq, prefix_blocks,
+                                                     max_seq_len, block_size, partition_size))
+
+
+def pa_cascade_decode(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      block_size: int, prefix_blocks: int, max_seq_len: int,
+                      workspace: torch.Tensor, partition_size: int = 512,
+                      stream=None) -> torch.Tensor:
+    """Decode attention for sequences whose tables share their first
+    ``prefix_blocks`` blocks (cascade: prefix once, suffixes, merge)."""
+    B, H, hkv, d, nb, mb = _decode_common(out, q, kv_cache, block_tables, seq_lens, block_size)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pa_cascade_decode(_dev(out, "out"), _dev(q, "q"), _dev(kv_cache, "kv_cache"),
+                                  _dev(block_tables, "block_tables"), _dev(seq_lens, "seq_lens"),
+                                  B, H, hkv, d, block_size, nb, mb, int(prefix_blocks),
+                                  float(scale), _DTYPE[q.dtype], int(max_seq_len),
+                                  int(partition_size), _dev(workspace, "workspace"), ws_bytes,
+                                  _stream(stream)), "pa_cascade_decode")
     return out
 
 

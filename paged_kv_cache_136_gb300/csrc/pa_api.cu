@@ -478,19 +478,22 @@ size_t pa_decode_splitk_workspace_size(int num_seqs, int num_heads, int head_siz
     return ws_layout(num_seqs, num_heads, head_size, splitk_parts(max_seq_len, partition_size)).total;
 }
 
-pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
-                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
-                           int num_heads, int num_kv_heads, int head_size, int block_size,
-                           int num_blocks, int max_blocks_per_seq, float scale, pa_dtype dtype,
-                           int max_seq_len, int partition_size, void *workspace,
-                           size_t workspace_bytes, void *stream)
+} // extern "C"
+
+static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const void *kv_cache,
+                                    const int32_t *block_tables, const int32_t *seq_lens,
+                                    int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                    int block_size, int num_blocks, int max_blocks_per_seq,
+                                    float scale, pa_dtype dtype, int max_seq_len,
+                                    int partition_size, void *workspace, size_t workspace_bytes,
+                                    void *stream)
 {
     pa_status st = check_decode_args(out, q, kv_cache, block_tables, seq_lens, num_seqs,
                                      num_heads, num_kv_heads, head_size, block_size, num_blocks,
                                      max_blocks_per_seq, scale, dtype);
     if (st != PA_OK)
         return st;
-    if (max_seq_len < 0 || partition_size <= 0 || partition_size % kTok != 0)
+    if (max_seq_len < 0 || partition_size <= 0 || partition_size % kTok != 0 || !aligned(lse, 4))
         return PA_ERR_INVALID_ARG;
     if (num_seqs == 0)
         return PA_OK;
@@ -532,11 +535,11 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         if (dtype == PA_BF16)
             tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
                 seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
-                static_cast<__nv_bfloat16 *>(out), err);
+                static_cast<__nv_bfloat16 *>(out), lse, err);
         else
             tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
                 seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
-                static_cast<__half *>(out), err);
+                static_cast<__half *>(out), lse, err);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return PA_ERR_CUDA;
         tc::TcParams t = {};
@@ -557,6 +560,7 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         t.max_parts = (int)parts;
         t.len_cap = len_cap;
         t.qscale = scale * kLog2e;
+        t.lse = lse;
         const int sms = sm_count(&e);
         if (!sms)
             return PA_ERR_CUDA;
@@ -569,7 +573,7 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
         if (parts > 1) {
             // Merge the partitions of multi-partition sequences.
             ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
-                              len_cap, 1};
+                              len_cap, 1, lse};
             e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
         }
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -590,14 +594,125 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
     p.max_parts = (int)parts;
     p.len_cap = len_cap;
     p.qscale = scale * kLog2e;
+    p.lse = lse;
     DecodeKey key = {(int)dtype, head_size, block_size, group, true};
     e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
     if (e != cudaSuccess)
         return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
     ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size, len_cap,
-                      0};
+                      0, lse};
     e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Merge of attention states and cascade (shared-prefix) decode
+// ("PagedAttention 在 vLLM 中的实现分析", section 6.4: the shared prefix is
+// attended once without the causal mask, each request's own suffix
+// separately, and the two results are combined with the online-softmax
+// correction -- merge_attn_states).
+// ---------------------------------------------------------------------------
+
+// out = (w_a o_a + w_b o_b) / (w_a + w_b), w_x = exp(lse_x - max), lse =
+// max + log(w_a + w_b); a part with lse = -inf is empty, two empty parts give
+// 0 and -inf.  One thread per 8 elements (16 bytes) of a row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    merge_attn_states_kernel(T *__restrict__ out, float *__restrict__ out_lse,
+                             const T *__restrict__ o_a, const float *__restrict__ lse_a,
+                             const T *__restrict__ o_b, const float *__restrict__ lse_b,
+                             int64_t rows, int head_size)
+{
+    const int vpr = head_size / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t row = idx / vpr;
+    if (row >= rows)
+        return;
+    const int v = (int)(idx - row * vpr);
+    const float la = lse_a[row], lb = lse_b[row];
+    const size_t off = (size_t)row * head_size + (size_t)v * 8;
+    uint4 res = make_uint4(0, 0, 0, 0);
+    float lse = -INFINITY;
+    if (!(la == -INFINITY && lb == -INFINITY)) {
+        const float M = fmaxf(la, lb);
+        const float wa = __expf(la - M), wb = __expf(lb - M);
+        const float inv = 1.f / (wa + wb);
+        const uint4 ua = *reinterpret_cast<const uint4 *>(o_a + off);
+        const uint4 ub = *reinterpret_cast<const uint4 *>(o_b + off);
+        const T *ea = reinterpret_cast<const T *>(&ua);
+        const T *eb = reinterpret_cast<const T *>(&ub);
+        T *er = reinterpret_cast<T *>(&res);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            er[i] = Elem<T>::from((wa * Elem<T>::one(ea[i]) + wb * Elem<T>::one(eb[i])) * inv);
+        lse = M + __logf(wa + wb);
+    }
+    *reinterpret_cast<uint4 *>(out + off) = res;
+    if (out_lse && v == 0)
+        out_lse[row] = lse;
+}
+
+// Cascade setup, one CTA per sequence: the prefix pass's request metadata
+// (query_start_loc = {0, B}, seq_len = prefix tokens), each sequence's suffix
+// length and suffix block table (its entries after the prefix blocks), and a
+// check that every table starts with row 0's prefix blocks.
+__global__ void cascade_setup_kernel(const int32_t *__restrict__ block_tables,
+                                     const int32_t *__restrict__ seq_lens, int num_seqs,
+                                     int max_blocks, int prefix_blocks, int block_size,
+                                     int suffix_cols, int32_t *__restrict__ hdr,
+                                     int32_t *__restrict__ suffix_lens,
+                                     int32_t *__restrict__ suffix_tables, unsigned int *err)
+{
+    const int s = blockIdx.x;
+    const int P = prefix_blocks * block_size;
+    const int32_t *row = block_tables + (size_t)s * max_blocks;
+    if (s == 0 && threadIdx.x == 0) {
+        hdr[0] = 0;
+        hdr[1] = num_seqs;
+        hdr[2] = P;
+    }
+    if (threadIdx.x == 0) {
+        const int L = seq_lens[s];
+        if (L < P)
+            atomicOr(err, PA_DEVERR_PREFIX);
+        suffix_lens[s] = L < P ? 0 : L - P;
+    }
+    for (int j = threadIdx.x; j < suffix_cols; j += blockDim.x)
+        suffix_tables[(size_t)s * suffix_cols + j] =
+            prefix_blocks + j < max_blocks ? row[prefix_blocks + j] : -1;
+    for (int j = threadIdx.x; j < prefix_blocks; j += blockDim.x)
+        if (row[j] != block_tables[j])
+            atomicOr(err, PA_DEVERR_PREFIX);
+}
+
+extern "C" {
+
+pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int num_heads, int num_kv_heads, int head_size, int block_size,
+                           int num_blocks, int max_blocks_per_seq, float scale, pa_dtype dtype,
+                           int max_seq_len, int partition_size, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    return decode_splitk_impl(out, nullptr, q, kv_cache, block_tables, seq_lens, num_seqs,
+                              num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                              max_blocks_per_seq, scale, dtype, max_seq_len, partition_size,
+                              workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_splitk_lse(void *out, float *lse, const void *q, const void *kv_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                               int block_size, int num_blocks, int max_blocks_per_seq,
+                               float scale, pa_dtype dtype, int max_seq_len, int partition_size,
+                               void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!lse && num_seqs > 0)
+        return PA_ERR_INVALID_ARG;
+    return decode_splitk_impl(out, lse, q, kv_cache, block_tables, seq_lens, num_seqs,
+                              num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                              max_blocks_per_seq, scale, dtype, max_seq_len, partition_size,
+                              workspace, workspace_bytes, stream);
 }
 
 pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
@@ -660,6 +775,139 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
     if (e == cudaErrorNotSupported)
         return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const float *lse_a,
+                               const void *o_b, const float *lse_b, int num_tokens,
+                               int num_heads, int head_size, pa_dtype dtype, void *stream)
+{
+    if (num_tokens < 0 || num_heads <= 0 || head_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if ((head_size != 64 && head_size != 128) || (dtype != PA_FP16 && dtype != PA_BF16))
+        return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!out || !o_a || !o_b || !lse_a || !lse_b || !aligned(out, 16) || !aligned(o_a, 16) ||
+        !aligned(o_b, 16) || !aligned(lse_a, 4) || !aligned(lse_b, 4) || !aligned(out_lse, 4))
+        return PA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)num_tokens * num_heads;
+    const int64_t threads = rows * (head_size / 8);
+    const unsigned grid = (unsigned)((threads + 255) / 256);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == PA_BF16)
+        merge_attn_states_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            static_cast<__nv_bfloat16 *>(out), out_lse, static_cast<const __nv_bfloat16 *>(o_a),
+            lse_a, static_cast<const __nv_bfloat16 *>(o_b), lse_b, rows, head_size);
+    else
+        merge_attn_states_kernel<__half><<<grid, 256, 0, st>>>(
+            static_cast<__half *>(out), out_lse, static_cast<const __half *>(o_a), lse_a,
+            static_cast<const __half *>(o_b), lse_b, rows, head_size);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Cascade workspace: [256 B header: query_start_loc {0, B}, prefix seq_len]
+// [suffix lengths] [suffix tables] [prefix output, dtype] [prefix lse]
+// [suffix output, dtype] [suffix lse] [split-K workspace], 256-byte aligned.
+struct CascadeLayout {
+    size_t sl, bt, o_pre, lse_pre, o_suf, lse_suf, ws, ws_bytes, total;
+    int suffix_cols;
+};
+
+static CascadeLayout cascade_layout(int num_seqs, int num_heads, int head_size,
+                                    int max_blocks_per_seq, int prefix_blocks,
+                                    int max_suffix_len, int partition_size)
+{
+    CascadeLayout c;
+    const size_t rows = (size_t)num_seqs * num_heads;
+    c.suffix_cols = max_blocks_per_seq - prefix_blocks > 0 ? max_blocks_per_seq - prefix_blocks : 1;
+    c.sl = 256;
+    c.bt = c.sl + round_up((size_t)num_seqs * 4, 256);
+    c.o_pre = c.bt + round_up((size_t)num_seqs * c.suffix_cols * 4, 256);
+    c.lse_pre = c.o_pre + round_up(rows * head_size * 2, 256);
+    c.o_suf = c.lse_pre + round_up(rows * 4, 256);
+    c.lse_suf = c.o_suf + round_up(rows * head_size * 2, 256);
+    c.ws = c.lse_suf + round_up(rows * 4, 256);
+    c.ws_bytes = ws_layout(num_seqs, num_heads, head_size,
+                           splitk_parts(max_suffix_len, partition_size)).total;
+    c.total = c.ws + c.ws_bytes;
+    return c;
+}
+
+size_t pa_cascade_decode_workspace_size(int num_seqs, int num_heads, int head_size,
+                                        int max_blocks_per_seq, int prefix_blocks,
+                                        int max_seq_len, int block_size, int partition_size)
+{
+    if (num_seqs < 0 || num_heads <= 0 || head_size <= 0 || max_blocks_per_seq <= 0 ||
+        prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq || max_seq_len < 0 ||
+        block_size <= 0 || partition_size <= 0)
+        return 0;
+    const int suffix = max_seq_len - prefix_blocks * block_size;
+    return cascade_layout(num_seqs, num_heads, head_size, max_blocks_per_seq, prefix_blocks,
+                          suffix > 0 ? suffix : 0, partition_size).total;
+}
+
+pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                            int num_heads, int num_kv_heads, int head_size, int block_size,
+                            int num_blocks, int max_blocks_per_seq, int prefix_blocks,
+                            float scale, pa_dtype dtype, int max_seq_len, int partition_size,
+                            void *workspace, size_t workspace_bytes, void *stream)
+{
+    pa_status st = check_decode_args(out, q, kv_cache, block_tables, seq_lens, num_seqs,
+                                     num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                                     max_blocks_per_seq, scale, dtype);
+    if (st != PA_OK)
+        return st;
+    if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq || max_seq_len < 0 ||
+        partition_size <= 0 || partition_size % kTok != 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (prefix_blocks == 0)
+        return decode_splitk_impl(out, nullptr, q, kv_cache, block_tables, seq_lens, num_seqs,
+                                  num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                                  max_blocks_per_seq, scale, dtype, max_seq_len, partition_size,
+                                  workspace, workspace_bytes, stream);
+    const int P = prefix_blocks * block_size;
+    const int max_suffix = max_seq_len > P ? max_seq_len - P : 0;
+    const CascadeLayout c = cascade_layout(num_seqs, num_heads, head_size, max_blocks_per_seq,
+                                           prefix_blocks, max_suffix, partition_size);
+    if (!workspace || workspace_bytes < c.total || !aligned(workspace, 256))
+        return PA_ERR_WORKSPACE;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    char *w = static_cast<char *>(workspace);
+    int32_t *hdr = reinterpret_cast<int32_t *>(w);
+    int32_t *sl_suf = reinterpret_cast<int32_t *>(w + c.sl);
+    int32_t *bt_suf = reinterpret_cast<int32_t *>(w + c.bt);
+    void *o_pre = w + c.o_pre;
+    float *lse_pre = reinterpret_cast<float *>(w + c.lse_pre);
+    void *o_suf = w + c.o_suf;
+    float *lse_suf = reinterpret_cast<float *>(w + c.lse_suf);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cascade_setup_kernel<<<num_seqs, 128, 0, s>>>(block_tables, seq_lens, num_seqs,
+                                                  max_blocks_per_seq, prefix_blocks, block_size,
+                                                  c.suffix_cols, hdr, sl_suf, bt_suf, err);
+    if (cudaGetLastError() != cudaSuccess)
+        return PA_ERR_CUDA;
+    // 1. Every query against the shared prefix, no causal mask: one request
+    //    whose B query rows are the B sequences' queries.
+    st = pa_prefill(o_pre, lse_pre, q, kv_cache, block_tables, max_blocks_per_seq, hdr + 2, hdr, 1,
+                    num_seqs, num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                    num_blocks, prefix_blocks, scale, 0, dtype, stream);
+    if (st != PA_OK)
+        return st;
+    // 2. Each sequence's own suffix.
+    st = decode_splitk_impl(o_suf, lse_suf, q, kv_cache, bt_suf, sl_suf, num_seqs, num_heads,
+                            num_kv_heads, head_size, block_size, num_blocks, c.suffix_cols, scale,
+                            dtype, max_suffix, partition_size, w + c.ws, c.ws_bytes, stream);
+    if (st != PA_OK)
+        return st;
+    // 3. Merge the two.
+    return pa_merge_attn_states(out, nullptr, o_pre, lse_pre, o_suf, lse_suf, num_seqs, num_heads,
+                                head_size, dtype, stream);
 }
 
 pa_status pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,

@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + kvh * G) * D;
         for (int i = tid; i < G * D; i += kThreads)
             out[i] = Elem<T>::from(0.f);
+        if (p.lse && tid < G)
+            p.lse[(size_t)s * p.num_heads + kvh * G + tid] = -INFINITY;
         return;
     }
 
@@ -372,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             l += lbuf[j * G + g];
         }
         const int h = kvh * G + g;
-        if (SPLIT) {
-            float mg = m_run[0];
+        float mg = m_run[0];
 #pragma unroll
-            for (int gg = 1; gg < G; ++gg)
-                if (gg == g)
-                    mg = m_run[gg];
+        for (int gg = 1; gg < G; ++gg)
+            if (gg == g)
+                mg = m_run[gg];
+        if (SPLIT) {
             const size_t row = ((size_t)s * p.num_heads + h) * p.max_parts + part;
             p.ws_o[row * D + d] = acc;
             if (d == 0) {
@@ -387,6 +389,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else {
             T *out = reinterpret_cast<T *>(p.out);
             out[((size_t)s * p.num_heads + h) * D + d] = Elem<T>::from(acc / l);
+            // m is in log2 units of the scaled score.
+            if (p.lse && d == 0)
+                p.lse[(size_t)s * p.num_heads + h] = (mg + __log2f(l)) * 0.69314718055994531f;
         }
     }
 }
@@ -412,6 +417,8 @@ __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
     T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + h) * D;
     if (np == 0) {
         out[d] = Elem<T>::from(0.f);
+        if (p.lse && d == 0)
+            p.lse[(size_t)s * p.num_heads + h] = -INFINITY;
         return;
     }
     if (np == 1 && p.skip_single)
@@ -448,6 +455,8 @@ __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
             num = fmaf(w_s[q], p.ws_o[(row0 + q0 + q) * D + d], num);
     }
     out[d] = Elem<T>::from(num / den);
+    if (p.lse && d == 0)
+        p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
 }
 
 // Launch helper shared by the instantiation units.

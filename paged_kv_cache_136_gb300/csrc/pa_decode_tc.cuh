@@ -112,6 +112,7 @@ struct TcParams {
     int num_heads, num_kv_heads, num_groups, num_blocks, max_blocks;
     int part_tokens, max_parts, len_cap;
     float qscale;
+    float *lse;                  // [B, H] natural-log softmax denominators, or null
 };
 
 template <typename T>
@@ -302,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              ((size_t)s * p.num_heads + group * NV) * kD;
                     for (int i = lane; i < NV * kD; i += 32)
                         out[i] = Elem<T>::from(0.f);
+                    if (p.lse && lane < NV)
+                        p.lse[(size_t)s * p.num_heads + group * NV + lane] = -INFINITY;
                 }
             }
             if (!have)
@@ -623,6 +626,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int n = 0; n < NV; ++n)
                     out[n * kD + t] = Elem<T>::from(o_acc[n] / l[n]);
+                if (p.lse) {
+#pragma unroll
+                    for (int n = 0; n < NV; ++n)
+                        if (t == n)
+                            p.lse[head0 + n] = (m_run[n] + __log2f(l[n])) * 0.69314718055994531f;
+                }
             } else {
                 // Partial state of this partition; the reduce kernel that
                 // follows merges the partitions of the sequence.
@@ -660,7 +669,8 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
                                                            int num_groups, int part_tokens,
                                                            int len_cap, uint32_t *hdr,
                                                            uint32_t *units,
-                                                           T *out, unsigned int *err)
+                                                           T *out, float *lse,
+                                                           unsigned int *err)
 {
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t bucket[kPlanBuckets];
@@ -700,6 +710,9 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
             } else {
                 for (int i = 0; i < H * 128; ++i)
                     out[(size_t)s * H * 128 + i] = Elem<T>::from(0.f);
+                if (lse)
+                    for (int h = 0; h < H; ++h)
+                        lse[(size_t)s * H + h] = -INFINITY;
             }
         }
         uint32_t v = nfull;

@@ -31,6 +31,7 @@ struct DecodeParams {
     int max_parts;               // split-K: partitions reserved per (seq, head)
     int len_cap;                 // largest seq_len the tables (and workspace) allow
     float qscale;                // scale * log2(e)
+    float *lse;                  // [B, H] natural-log softmax denominators, or null
 };
 
 // Parameters of the split-K log-sum-exp reduce.
@@ -44,6 +45,7 @@ struct ReduceParams {
     int part_tokens;
     int len_cap;
     int skip_single; // rows of one-partition sequences are already final
+    float *lse;      // [B, H] natural-log softmax denominators, or null
 };
 
 // Key of a decode kernel instantiation.

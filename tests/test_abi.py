@@ -31,7 +31,9 @@ def test_header_declares_the_entry_points():
     for n in ("pa_reshape_and_cache", "pa_decode", "pa_decode_splitk",
               "pa_decode_splitk_workspace_size", "pa_validate_tables", "pa_validate_slots",
               "pa_device_errors", "pa_status_string", "pa_version", "pa_copy_blocks",
-              "pa_validate_block_mapping", "pa_selftest_wait_timeout", "pa_prefill"):
+              "pa_validate_block_mapping", "pa_selftest_wait_timeout", "pa_prefill",
+              "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
+              "pa_cascade_decode_workspace_size"):
         assert n in names
 
 
@@ -214,3 +216,29 @@ def test_prefill_rejects_bad_arguments(pa):
     assert call(R=0) == 0
     assert call(P=[FAKE + 2] + P[1:]) == 1                    # misaligned out
     assert call(P=[0] + P[1:]) == 1                           # null out
+
+
+def test_cascade_workspace_size_covers_its_parts(pa):
+    B, H, D, MB, pb, bs, P = 128, 32, 128, 157, 125, 16, 512
+    n = pa.pa_cascade_decode_workspace_size(B, H, D, MB, pb, 2500, bs, P)
+    split = pa.pa_decode_splitk_workspace_size(B, H, D, 2500 - pb * bs, P)
+    parts = B * H * D * 2 * 2 + B * H * 4 * 2 + B * 4 + B * (MB - pb) * 4
+    assert n >= split + parts and n % 256 == 0
+    assert pa.pa_cascade_decode_workspace_size(B, H, D, MB, MB + 1, 2500, bs, P) == 0
+
+
+def test_merge_and_cascade_reject_bad_arguments(pa):
+    lib = _raw(pa)
+    f = lib.pa_merge_attn_states
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 4, 2, 96, 0, None) == 2     # head_size
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 9, None) == 2    # dtype
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 0, None) == 0    # nothing to do
+    assert f(FAKE + 8, 0, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 0, None) == 1
+    g = lib.pa_decode_splitk_lse
+    g.restype = ctypes.c_int
+    g.argtypes = ([ctypes.c_void_p] * 6 + [ctypes.c_int] * 7 + [ctypes.c_float] +
+                  [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
+    assert g(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, 128, 16, 8, 4, 0.1, 0, 64, 512, FAKE,
+             1 << 20, None) == 1                                           # lse missing
