@@ -110,6 +110,20 @@ class Oracle:
                                    dbl, i32, i32, P, i64, i32]
         lib.or_merge_attn_states.restype = i32
         lib.or_merge_attn_states.argtypes = [P, P, P, P, P, P, i64, i32]
+        lib.or_fp8e4m3_to_double.restype = dbl
+        lib.or_fp8e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.or_double_to_fp8e4m3.restype = ctypes.c_uint8
+        lib.or_double_to_fp8e4m3.argtypes = [dbl]
+        lib.or_fp8_widen.restype = None
+        lib.or_fp8_widen.argtypes = [P, P, i64]
+        lib.or_fp8_quantize.restype = None
+        lib.or_fp8_quantize.argtypes = [P, P, i64, ctypes.c_float]
+        lib.or_reshape_and_cache_fp8.restype = i32
+        lib.or_reshape_and_cache_fp8.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i64, i64,
+                                                 i32, ctypes.c_float, ctypes.c_float]
+        lib.or_decode_fp8.restype = i32
+        lib.or_decode_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, dbl,
+                                      i32, dbl, dbl, P, i64]
         lib.or_check_tables.restype = i32
         lib.or_check_tables.argtypes = [P, P, i32, i32, i32, i32]
         self.lib = lib
@@ -264,6 +278,61 @@ class Oracle:
         _check(self.lib.or_merge_attn_states(_ptr(out), _ptr(lse), _ptr(o_a), _ptr(lse_a),
                                              _ptr(o_b), _ptr(lse_b), lse_a.size, d))
         return out, lse
+
+    # -- FP8 (e4m3) KV cache ----------------------------------------------------
+    def fp8_widen(self, codes) -> np.ndarray:
+        """e4m3 codes (uint8) -> float64 values."""
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.or_fp8_widen(_ptr(c), _ptr(out), c.size)
+        return out
+
+    def fp8_quantize(self, x, scale: float) -> np.ndarray:
+        """float32 values -> e4m3 codes of fp32(x / scale)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(x.shape, dtype=np.uint8)
+        self.lib.or_fp8_quantize(_ptr(x), _ptr(out), x.size, float(scale))
+        return out
+
+    def fp8_encode(self, x: float) -> int:
+        return int(self.lib.or_double_to_fp8e4m3(float(x)))
+
+    def reshape_and_cache_fp8(self, key, value, cache, slot_mapping, block_size: int,
+                              src_dtype: int, k_scale: float, v_scale: float):
+        """Copy of the uint8 pool ``cache`` [2, NB, bs, Hkv, D] with the new
+        tokens quantised and written."""
+        c = np.array(np.ascontiguousarray(cache, dtype=np.uint8), copy=True)
+        _, nb, bs, hkv, d = c.shape
+        assert bs == block_size
+        k = _u16(key)
+        v = _u16(value)
+        t = k.shape[0]
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        _check(self.lib.or_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(c), _ptr(sm), t, hkv, d,
+                                                 bs, nb, int(np.prod(k.shape[1:])),
+                                                 int(np.prod(v.shape[1:])), src_dtype,
+                                                 float(k_scale), float(v_scale)))
+        return c
+
+    def decode_fp8(self, q, cache, block_tables, seq_lens, num_kv_heads: int, block_size: int,
+                   scale: float, q_dtype: int, k_scale: float, v_scale: float, items=None):
+        """fp64 decode output [B, H, D] over a uint8 e4m3 pool."""
+        qb = _u16(q)
+        cb = np.ascontiguousarray(cache, dtype=np.uint8)
+        b, h, d = qb.shape
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        out = np.full((b, h, d), np.nan, dtype=np.float64)
+        if items is not None:
+            it = np.ascontiguousarray(items, dtype=np.int32)
+            itp, nit = _ptr(it), it.size
+        else:
+            itp, nit = None, 0
+        _check(self.lib.or_decode_fp8(_ptr(out), _ptr(qb), _ptr(cb), _ptr(bt), _ptr(sl), b, h,
+                                      num_kv_heads, d, block_size, cb.shape[1], bt.shape[1],
+                                      float(scale), q_dtype, float(k_scale), float(v_scale),
+                                      itp, nit))
+        return out
 
     def check_tables(self, block_tables, seq_lens, block_size: int, num_blocks: int) -> int:
         bt = np.ascontiguousarray(block_tables, dtype=np.int32)

@@ -750,6 +750,199 @@ int or_merge_attn_states(double *out, double *lse_out, const double *o_a,
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 KV cache ("PagedAttention 在 vLLM 中的实现分析", section 6.3: the    */
+/* cache write converts K/V to FP8 with k_scale / v_scale when the cache    */
+/* dtype is FP8; section 8 lists FP8 KV-cache quantisation).                */
+/* ------------------------------------------------------------------------ */
+
+/* Readings where the pages are silent:
+ *   - the FP8 format is e4m3 (1 sign, 4 exponent bits with bias 7, 3 fraction
+ *     bits, no infinities; exponent 15 with fraction 7 is NaN, so the largest
+ *     finite magnitude is 1.75 * 2^8 = 448);
+ *   - k_scale and v_scale are one float each: the cache stores x / scale and
+ *     a read gives stored * scale;
+ *   - the quotient x / scale is a float32 division (the precision the CUDA
+ *     kernel decides the code in), then rounded to e4m3, nearest with ties to
+ *     even, magnitudes above 448 saturating to 448, NaN staying NaN. */
+
+double or_fp8e4m3_to_double(uint8_t b)
+{
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);           /* subnormal: m/8 * 2^-6 */
+    else
+        v = ldexp(8.0 + m, e - 10);         /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+uint8_t or_double_to_fp8e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7E;                 /* saturate to 448 */
+    /* quantum of the binade holding a: 2^(e-3) for a in [2^e, 2^(e+1)),
+     * e >= -6; the subnormal range [0, 2^-6) has quantum 2^-9 */
+    int e;
+    frexp(a, &e);                           /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                 /* a in [2^e, 2^(e+1)) */
+    if (a == 0.0 || e < -6)
+        e = -6;
+    const double quantum = ldexp(1.0, e - 3);
+    double n = nearbyint(a / quantum);      /* ties to even (default mode) */
+    double r = n * quantum;
+    if (r > 448.0)
+        r = 448.0;
+    /* encode r exactly */
+    if (r < ldexp(1.0, -6))
+        return sign | (uint8_t)(r / ldexp(1.0, -9));
+    int er;
+    double f = frexp(r, &er);               /* r = f * 2^er, f in [0.5, 1) */
+    const int exp_field = er - 1 + 7;
+    const int frac = (int)((f * 2.0 - 1.0) * 8.0);
+    return sign | (uint8_t)(exp_field << 3) | (uint8_t)frac;
+}
+
+void or_fp8_widen(const uint8_t *bits, double *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        x[i] = or_fp8e4m3_to_double(bits[i]);
+}
+
+/* Quantise float32 values: code = e4m3(fp32(x / scale)). */
+void or_fp8_quantize(const float *x, uint8_t *bits, int64_t n, float scale)
+{
+    for (int64_t i = 0; i < n; i++) {
+        const float qv = x[i] / scale;
+        bits[i] = or_double_to_fp8e4m3((double)qv);
+    }
+}
+
+/* The cache write with an FP8 pool: token i with slot_mapping[i] >= 0 gets
+ * key[i] / k_scale and value[i] / v_scale, each quantised as above, at
+ * (slot / block_size, slot % block_size) of the pool
+ * [2, num_blocks, block_size, num_kv_heads, head_size] (uint8 codes). */
+int or_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value, uint8_t *cache,
+                             const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_size, int block_size, int num_blocks, int64_t key_stride,
+                             int64_t value_stride, int src_dtype, float k_scale, float v_scale)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return OR_ERR_ARG;
+    for (int i = 0; i < num_tokens; i++) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        if (slot >= (int64_t)num_blocks * block_size)
+            return OR_ERR_SLOT;
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; h++)
+            for (int d = 0; d < head_size; d++) {
+                const size_t src = (size_t)h * head_size + d;
+                const float kx = (float)or_load(key, (size_t)i * key_stride + src, src_dtype);
+                const float vx = (float)or_load(value, (size_t)i * value_stride + src, src_dtype);
+                cache[or_pool_index(0, blk, off, h, d, num_blocks, block_size, num_kv_heads,
+                                    head_size)] = or_double_to_fp8e4m3((double)(kx / k_scale));
+                cache[or_pool_index(1, blk, off, h, d, num_blocks, block_size, num_kv_heads,
+                                    head_size)] = or_double_to_fp8e4m3((double)(vx / v_scale));
+            }
+    }
+    return OR_OK;
+}
+
+/* Decode attention over an FP8 pool: keys k_scale * e4m3(K), values
+ * v_scale * e4m3(V); otherwise the definition of or_decode (two passes in
+ * fp64).  One output row per (sequence, query head), or only the items. */
+int or_decode_fp8(double *out, const uint16_t *q, const uint8_t *cache,
+                  const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                  int num_heads, int num_kv_heads, int head_size, int block_size,
+                  int num_blocks, int max_blocks_per_seq, double scale, int q_dtype,
+                  double k_scale, double v_scale, const int32_t *items, int64_t num_items)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return OR_ERR_ARG;
+    const int D = head_size, G = num_heads / num_kv_heads;
+    const size_t cap = (size_t)max_blocks_per_seq * block_size;
+    double *Kc = (double *)malloc((cap ? cap : 1) * D * sizeof(double));
+    double *Vc = (double *)malloc((cap ? cap : 1) * D * sizeof(double));
+    double *a = (double *)malloc((cap ? cap : 1) * sizeof(double));
+    int status = OR_OK;
+    if (!Kc || !Vc || !a) {
+        status = OR_ERR_NOMEM;
+        goto done;
+    }
+    const int64_t n = items ? num_items : (int64_t)num_seqs * num_heads;
+    for (int64_t it = 0; it < n; it++) {
+        const int64_t item = items ? items[it] : it;
+        const int s = (int)(item / num_heads), h = (int)(item % num_heads);
+        const int kvh = h / G;
+        double *o = out + ((size_t)s * num_heads + h) * D;
+        const int L = seq_lens[s];
+        if (L < 0 || (size_t)L > cap) {
+            status = OR_ERR_SEQ_LEN;
+            goto done;
+        }
+        if (L == 0) {
+            for (int d = 0; d < D; d++)
+                o[d] = 0.0;
+            continue;
+        }
+        const int32_t *bt = block_tables + (size_t)s * max_blocks_per_seq;
+        for (int t = 0; t < L; t++) {
+            int32_t phys, off;
+            or_translate(bt, t, block_size, &phys, &off);
+            if (phys < 0 || phys >= num_blocks) {
+                status = OR_ERR_BLOCK_ID;
+                goto done;
+            }
+            for (int d = 0; d < D; d++) {
+                Kc[(size_t)t * D + d] = k_scale * or_fp8e4m3_to_double(cache[or_pool_index(
+                                            0, phys, off, kvh, d, num_blocks, block_size,
+                                            num_kv_heads, D)]);
+                Vc[(size_t)t * D + d] = v_scale * or_fp8e4m3_to_double(cache[or_pool_index(
+                                            1, phys, off, kvh, d, num_blocks, block_size,
+                                            num_kv_heads, D)]);
+            }
+        }
+        const size_t qrow = ((size_t)s * num_heads + h) * D;
+        for (int t = 0; t < L; t++) {
+            double acc = 0.0;
+            for (int d = 0; d < D; d++)
+                acc += or_load(q, qrow + d, q_dtype) * Kc[(size_t)t * D + d];
+            a[t] = scale * acc;
+        }
+        double m = a[0];
+        for (int t = 1; t < L; t++)
+            if (a[t] > m)
+                m = a[t];
+        double l = 0.0;
+        for (int t = 0; t < L; t++) {
+            a[t] = exp(a[t] - m);
+            l += a[t];
+        }
+        for (int d = 0; d < D; d++) {
+            double acc = 0.0;
+            for (int t = 0; t < L; t++)
+                acc += a[t] * Vc[(size_t)t * D + d];
+            o[d] = acc / l;
+        }
+    }
+done:
+    free(Kc);
+    free(Vc);
+    free(a);
+    return status;
+}
+
 /* Host check of the caller preconditions the CUDA library documents:
  * 0 <= seq_lens[s] <= max_blocks_per_seq * block_size and every block id a
  * sequence uses lies in [0, num_blocks).  Returns OR_OK or an error code. */

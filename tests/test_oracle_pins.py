@@ -712,3 +712,135 @@ def test_prefill_rejects_bad_metadata(orc):
     bad[1, 0] = cache.shape[1] + 5
     with pytest.raises(OracleError):
         orc.prefill(q, cache, bad, L, qsl, 2, 16, 0.1, FP16)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache
+# ---------------------------------------------------------------------------
+
+ALL_FP8 = np.arange(256, dtype=np.uint8)
+
+
+def _torch_fp8_values(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_fp8_decode_matches_torch(orc):
+    got = orc.fp8_widen(ALL_FP8)
+    ref = _torch_fp8_values(ALL_FP8)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.nanmax(got) == 448.0 and np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def test_fp8_every_finite_code_round_trips(orc):
+    vals = orc.fp8_widen(ALL_FP8)
+    for c in ALL_FP8:
+        if not np.isnan(vals[c]):
+            assert orc.fp8_encode(vals[c]) == c
+
+
+def test_fp8_encode_is_nearest_even_by_brute_force(orc):
+    vals = orc.fp8_widen(ALL_FP8)
+    fin = ~np.isnan(vals)
+    codes, cv = ALL_FP8[fin], vals[fin]
+    rng = np.random.default_rng(81)
+    xs = np.concatenate([rng.uniform(-460, 460, 3000), rng.normal(0, 0.01, 2000),
+                         (cv[:-1] + np.roll(cv, -1)[:-1]) / 2])       # include midpoints
+    for x in xs:
+        got = orc.fp8_encode(x)
+        if abs(x) >= 448:
+            assert got == (0xFE if x < 0 else 0x7E)
+            continue
+        d = np.abs(cv - x)
+        best = np.nonzero(d == d.min())[0]
+        cand = [c for c in codes[best]]
+        if len(cand) > 1:                     # a tie: the even code (fraction LSB 0)
+            cand = [c for c in cand if (c & 1) == 0]
+        if x == 0:
+            cand = [0x80 if np.signbit(x) else 0x00]
+        assert got in cand, (x, got, cand)
+
+
+def test_fp8_encode_matches_torch_in_range(orc):
+    rng = np.random.default_rng(82)
+    x = np.concatenate([rng.normal(0, 3, 20000), rng.uniform(-440, 440, 5000)]).astype(np.float32)
+    got = orc.fp8_quantize(x, 1.0)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_saturates_and_keeps_nan(orc):
+    assert orc.fp8_encode(449.0) == 0x7E and orc.fp8_encode(1e30) == 0x7E
+    assert orc.fp8_encode(-464.0) == 0xFE
+    assert orc.fp8_encode(float("nan")) & 0x7F == 0x7F
+    # below half the smallest subnormal (2^-10) rounds to zero
+    assert orc.fp8_encode(2.0 ** -11) == 0x00 and orc.fp8_encode(-(2.0 ** -11)) == 0x80
+
+
+def test_reshape_fp8_matches_torch_quantisation(orc):
+    rng = np.random.default_rng(83)
+    NB, bs, Hkv, D, T = 6, 16, 2, 64, 9
+    key = _rand_bits(rng, (T, Hkv, D), BF16)
+    value = _rand_bits(rng, (T, Hkv, D), BF16)
+    cache = rng.integers(0, 256, size=(2, NB, bs, Hkv, D), dtype=np.uint8)
+    slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+    slots[3] = -1
+    ks, vs = 0.037, 0.11
+    got = orc.reshape_and_cache_fp8(key, value, cache, slots, bs, BF16, ks, vs)
+    ref = cache.copy()
+    flat = ref.reshape(2, NB * bs, Hkv, D)
+    kf = torch.from_numpy(orc.widen(key, BF16).astype(np.float32))
+    vf = torch.from_numpy(orc.widen(value, BF16).astype(np.float32))
+    kq = (kf / torch.tensor(ks, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    vq = (vf / torch.tensor(vs, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for i, sl in enumerate(slots):
+        if sl >= 0:
+            flat[0, sl] = kq[i]
+            flat[1, sl] = vq[i]
+    assert np.array_equal(got, ref)
+
+
+def _fp8_case(rng, lens, H, Hkv, D, bs, q_dtype):
+    q, cache16, bt, sl, NB, starts = _case(rng, lens, H, Hkv, D, bs, q_dtype)
+    x = rng.normal(0, 2, size=(2, NB, bs, Hkv, D)).astype(np.float32)
+    cache8 = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return q, cache8, bt, sl, NB, starts
+
+
+@pytest.mark.parametrize("lens,H,Hkv,bs", [([1, 17, 40], 4, 4, 16), ([100, 33], 8, 2, 32)])
+def test_decode_fp8_matches_sdpa(orc, lens, H, Hkv, bs):
+    rng = np.random.default_rng(84 + H)
+    D = 128
+    q, cache8, bt, sl, NB, starts = _fp8_case(rng, lens, H, Hkv, D, bs, FP16)
+    ks, vs = 0.3, 0.7
+    got = orc.decode_fp8(q, cache8, bt, sl, Hkv, bs, 1 / math.sqrt(D), FP16, ks, vs)
+    # SDPA on torch's own dequantisation of the same pool
+    kd = torch.from_numpy(_torch_fp8_values(cache8[0]).reshape(-1, Hkv, D) * ks)
+    vd = torch.from_numpy(_torch_fp8_values(cache8[1]).reshape(-1, Hkv, D) * vs)
+    qd = torch.from_numpy(orc.widen(q, FP16))
+    G = H // Hkv
+    for s in range(len(lens)):
+        L = int(sl[s])
+        k = kd[starts[s] * bs: starts[s] * bs + L].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        v = vd[starts[s] * bs: starts[s] * bs + L].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(qd[s][:, None, :], k, v,
+                                                             scale=1 / math.sqrt(D))
+        np.testing.assert_allclose(got[s], o[:, 0, :].numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_decode_fp8_equals_decode_on_the_dequantised_pool(orc):
+    """With power-of-two scales every dequantised value is exact in fp16:
+    the FP8 decode equals the fp16 decode of the dequantised pool."""
+    rng = np.random.default_rng(85)
+    lens = [5, 70, 129]
+    q, cache8, bt, sl, NB, starts = _fp8_case(rng, lens, 4, 2, 128, 16, FP16)
+    ks, vs = 0.25, 2.0
+    got = orc.decode_fp8(q, cache8, bt, sl, 2, 16, 0.1, FP16, ks, vs)
+    deq = np.stack([orc.fp8_widen(cache8[0]) * ks, orc.fp8_widen(cache8[1]) * vs])
+    cache16 = deq.astype(np.float16).view(np.uint16)
+    assert np.array_equal(cache16.view(np.float16).astype(np.float64), deq)
+    ref = orc.decode(q, cache16, bt, sl, 2, 16, 0.1, FP16)
+    np.testing.assert_allclose(got, ref, rtol=1e-14, atol=1e-15)

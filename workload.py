@@ -45,6 +45,12 @@ by the cache-write step before the attention reads them.
   uniform on [0, 4096]; 32/32 heads, head_size 128, block_size 16, fp16.
 - ``prefill_gqa8b``: the same lengths recipe with 32 q / 8 kv heads, bf16.
 
+FP8 pools (``make_fp8``): the same structure, tables, queries and new tokens
+as the named decode workload, with the pool drawn as e4m3 codes of N(0, 2)
+values (torch's float8_e4m3fn conversion of the draws) and the per-tensor
+scales k_scale = v_scale = 0.5, so the dequantised keys and values are about
+N(0, 1).  The poison code is 0x7F (NaN).
+
 Q, K and V are N(0,1) draws rounded to the cache dtype.  With ``poison=True``
 every pool row that no sequence owns (unused blocks and the tail of each
 sequence's last block) holds NaN, so a read past a sequence's end shows up in
@@ -400,3 +406,29 @@ def make_prefill(name: str, seed: int | None = None, device="cpu", poison: bool 
         block_size=bs, scale=1.0 / math.sqrt(D), num_heads=H, num_kv_heads=Hkv,
         head_size=D, meta={"seed": seed, "poison": poison},
     )
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) pools
+# ---------------------------------------------------------------------------
+
+def make_fp8(name: str, seed: int | None = None, device="cpu", poison: bool = False,
+             k_scale: float = 0.5, v_scale: float = 0.5, **kw) -> Workload:
+    """The decode workload ``name`` with its pool replaced by e4m3 codes
+    (uint8 [2, NB, bs, Hkv, D]); meta holds k_scale and v_scale."""
+    w = make(name, seed=seed, device=device, poison=poison, **kw)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1000 + int(w.meta["seed"]))
+    shape = tuple(w.kv_cache.shape)
+    pool = torch.empty(shape, dtype=torch.uint8, device=device)
+    for plane in range(2):
+        for i in range(0, shape[1], 1 << 12):
+            j = min(shape[1], i + (1 << 12))
+            x = torch.randn((j - i,) + shape[2:], generator=gen, device=device) * 2.0
+            pool[plane, i:j] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    if poison:
+        nan16 = torch.isnan(w.kv_cache)
+        pool[nan16] = 0x7F
+    w.kv_cache = pool
+    w.meta = {**w.meta, "k_scale": float(k_scale), "v_scale": float(v_scale), "fp8": True}
+    return w
