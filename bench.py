@@ -556,6 +556,60 @@ def cascade_workload(args, peak_gbs: float) -> dict:
     return res
 
 
+def fp8_workload(name: str, args, peak_gbs: float) -> dict:
+    """A decode workload with an FP8 (e4m3) pool: quantising cache write of the
+    new tokens + split-K decode over the FP8 pool.  KV bytes are the e4m3
+    codes read (one byte per element)."""
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    base = name[len("fp8_"):]
+    w = wl.make_fp8(base, device="cuda")
+    ks, vs = w.meta["k_scale"], w.meta["v_scale"]
+    out = torch.empty_like(w.q)
+    msl = int(w.seq_lens.max().item())
+    P = args.partition
+    ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                                        msl, P), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def write():
+        pa.pa_reshape_and_cache_fp8(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size,
+                                    ks, vs)
+
+    def call():
+        pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                                w.block_size, ks, vs, msl, ws, P)
+
+    for _ in range(5):
+        write()
+        call()
+    k = max(3, args.workload_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k)]
+    torch.cuda.synchronize()
+    for i in range(k):
+        ev[i][0].record(stream)
+        write()
+        ev[i][1].record(stream)
+        call()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    kvb = kv_bytes(w)
+    res = {"name": name, "call": "pa_decode_splitk_fp8", "workload": WORKLOAD_TEXT[base] +
+           "; FP8 e4m3 pool (k_scale = v_scale = 0.5)", "partition_size": P, "steps": k,
+           "kv_bytes_per_step": kvb, "ms_per_call": round(ms, 5), "ms_per_step": round(step_ms, 5),
+           "decode_gbs": round(kvb / ms / 1e6, 2), "decode_frac": round(kvb / ms / 1e6 / peak_gbs, 4),
+           "step_gbs": round(kvb / step_ms / 1e6, 2),
+           "seqs_per_s": round(w.num_seqs / (step_ms / 1e3), 1),
+           "device_error_flags": pa.pa_device_errors(clear=True)}
+    del w, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def other_workload(name: str, args, peak_gbs: float) -> dict:
     """Short device-resident measurement of another workload through the same
     step (cache write + split-K decode), reported beside the main line."""
@@ -568,6 +622,8 @@ def other_workload(name: str, args, peak_gbs: float) -> dict:
         return prefill_workload(name, args, measured_peaks())
     if name == "prefix_cascade":
         return cascade_workload(args, peak_gbs)
+    if name.startswith("fp8_"):
+        return fp8_workload(name, args, peak_gbs)
     w = wl.make(name, device="cuda")
     out = torch.empty_like(w.q)
     msl = int(w.seq_lens.max().item())
@@ -672,7 +728,7 @@ def parse_args(argv=None):
                     help="steps in the end-to-end (host buffers) measurement")
     ap.add_argument("--workloads",
                     default="gqa8b,long,prefix,prefix_cascade,tiny,copy_blocks,prefill_mha7b,"
-                            "prefill_gqa8b",
+                            "prefill_gqa8b,fp8_mha7b,fp8_gqa8b",
                     help="other workloads measured briefly beside the main line ('' for none)")
     ap.add_argument("--workload-steps", type=int, default=50)
     return ap.parse_args(argv)

@@ -11,6 +11,7 @@
  *   pa_decode_splitk_lse  split-K decode that also returns the log-sum-exps
  *   pa_merge_attn_states  merge two partial attention results
  *   pa_cascade_decode     decode for sequences sharing a prefix (cascade)
+ *   pa_*_fp8              the cache write and decode with an FP8 (e4m3) pool
  *
  * Data layout (all tensors contiguous, row-major, caller-owned):
  *
@@ -183,6 +184,42 @@ pa_status pa_decode_splitk_noalloc(void *out, const void *q, const void *kv_cach
                                    int block_size, int num_blocks, int max_blocks_per_seq,
                                    float scale, pa_dtype dtype, int max_seq_len,
                                    int partition_size, void *stream);
+
+/*
+ * FP8 KV cache ("PagedAttention 在 vLLM 中的实现分析", section 6.3: with an
+ * FP8 cache dtype the cache write converts K/V using k_scale / v_scale).  The
+ * pool is uint8 [2, num_blocks, block_size, num_kv_heads, head_size] of e4m3
+ * codes (1 sign, 4 exponent bits with bias 7, 3 fraction bits; 0x7F/0xFF are
+ * NaN; largest magnitude 448).  head_size 128.
+ *
+ * pa_reshape_and_cache_fp8: for token i with slot_mapping[i] >= 0 the codes
+ *   e4m3(fp32(key[i][..] / k_scale)) and e4m3(fp32(value[i][..] / v_scale))
+ *   go to pool row `slot`, rounded to nearest (ties to even), magnitudes
+ *   above 448 saturating to 448.  key/value are src_dtype rows as in
+ *   pa_reshape_and_cache (strides multiples of 8 elements); k_scale and
+ *   v_scale are positive finite floats.  Slots past the pool are skipped and
+ *   flagged (PA_DEVERR_SLOT).
+ * pa_decode_fp8 / pa_decode_splitk_fp8: pa_decode / pa_decode_splitk over
+ *   keys k_scale * e4m3(K) and values v_scale * e4m3(V); q and out are
+ *   `dtype`; the split-K workspace is the same size as pa_decode_splitk's.
+ */
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
+                                   const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_size, int block_size, int num_blocks,
+                                   int64_t key_stride, int64_t value_stride, pa_dtype src_dtype,
+                                   float k_scale, float v_scale, void *stream);
+pa_status pa_decode_fp8(void *out, const void *q, const void *kv_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int num_heads, int num_kv_heads, int head_size, int block_size,
+                        int num_blocks, int max_blocks_per_seq, float scale, float k_scale,
+                        float v_scale, pa_dtype dtype, void *stream);
+pa_status pa_decode_splitk_fp8(void *out, const void *q, const void *kv_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                               int block_size, int num_blocks, int max_blocks_per_seq,
+                               float scale, float k_scale, float v_scale, pa_dtype dtype,
+                               int max_seq_len, int partition_size, void *workspace,
+                               size_t workspace_bytes, void *stream);
 
 /*
  * pa_decode_splitk that also writes each row's log-sum-exp: lse[s][h] =

@@ -21,7 +21,8 @@ __all__ = [
     "pa_validate_tables", "pa_validate_slots",
     "pa_device_errors", "pa_selftest_wait_timeout", "pa_copy_blocks", "pa_prefill",
     "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
-    "pa_cascade_decode_workspace_size",
+    "pa_cascade_decode_workspace_size", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+    "pa_decode_splitk_fp8",
     "pa_validate_block_mapping", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
@@ -71,6 +72,15 @@ _lib.pa_cascade_decode_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I
 _lib.pa_cascade_decode.restype = _I
 _lib.pa_cascade_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                    _I, _I, _P, _SZ, _P]
+_lib.pa_reshape_and_cache_fp8.restype = _I
+_lib.pa_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I64, _I, _F,
+                                          _F, _P]
+_lib.pa_decode_fp8.restype = _I
+_lib.pa_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I,
+                               _P]
+_lib.pa_decode_splitk_fp8.restype = _I
+_lib.pa_decode_splitk_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F,
+                                      _F, _I, _I, _I, _P, _SZ, _P]
 _lib.pa_prefill.restype = _I
 _lib.pa_prefill.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                             _I, _F, _I, _I, _P]
@@ -359,6 +369,87 @@ def pa_prefill(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
                            R, T, int(max_query_len), H, hkv, d, block_size, nb,
                            max(1, int(block_tables.shape[1])), float(scale),
                            1 if causal else 0, _DTYPE[q.dtype], _stream(stream)), "pa_prefill")
+    return out
+
+
+def _fp8_pool(kv_cache: torch.Tensor, block_size: int):
+    if kv_cache.dtype != torch.uint8:
+        raise ValueError("an FP8 pool is a uint8 tensor of e4m3 codes")
+    return _pool_dims(kv_cache, block_size)
+
+
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, kv_cache: torch.Tensor,
+                             slot_mapping: torch.Tensor, block_size: int, k_scale: float,
+                             v_scale: float, stream=None) -> None:
+    """Quantise new tokens' K/V ([T, Hkv, D] fp16/bf16) to e4m3 with the
+    per-tensor scales and scatter them into the uint8 pool."""
+    nb, hkv, d = _fp8_pool(kv_cache, block_size)
+    T = int(key.shape[0])
+    for name, t in (("key", key), ("value", value)):
+        if t.dtype not in _DTYPE or t.dtype != key.dtype or t.shape[0] != T:
+            raise ValueError(f"{name} must be fp16/bf16 [T, ...] like key")
+        if t.dim() != 3 or t.shape[1] != hkv or t.shape[2] != d or t.stride(2) != 1 or \
+                t.stride(1) != d:
+            raise ValueError(f"{name} must be [T, num_kv_heads, head_size] with contiguous rows")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64 [T]")
+    if T == 0:
+        return
+    _check(_lib.pa_reshape_and_cache_fp8(_dev(key, "key"), _dev(value, "value"),
+                                         _dev(kv_cache, "kv_cache"),
+                                         _dev(slot_mapping, "slot_mapping"), T, hkv, d,
+                                         block_size, nb, key.stride(0), value.stride(0),
+                                         _DTYPE[key.dtype], float(k_scale), float(v_scale),
+                                         _stream(stream)), "pa_reshape_and_cache_fp8")
+
+
+def _fp8_decode_common(out, q, kv_cache, block_tables, seq_lens, block_size):
+    nb, hkv, d = _fp8_pool(kv_cache, block_size)
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous() or q.dtype not in _DTYPE:
+        raise ValueError("q must be contiguous fp16/bf16 [B, H, head_size]")
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be contiguous and match q")
+    B, H = int(q.shape[0]), int(q.shape[1])
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != B or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be contiguous int32 [B, max_blocks_per_seq]")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != B or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be contiguous int32 [B]")
+    return B, H, hkv, d, nb, int(block_tables.shape[1])
+
+
+def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                  block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                  block_size: int, k_scale: float, v_scale: float,
+                  stream=None) -> torch.Tensor:
+    """One-pass paged decode over an FP8 (e4m3) pool."""
+    B, H, hkv, d, nb, mb = _fp8_decode_common(out, q, kv_cache, block_tables, seq_lens,
+                                              block_size)
+    _check(_lib.pa_decode_fp8(_dev(out, "out"), _dev(q, "q"), _dev(kv_cache, "kv_cache"),
+                              _dev(block_tables, "block_tables"), _dev(seq_lens, "seq_lens"),
+                              B, H, hkv, d, block_size, nb, mb, float(scale), float(k_scale),
+                              float(v_scale), _DTYPE[q.dtype], _stream(stream)), "pa_decode_fp8")
+    return out
+
+
+def pa_decode_splitk_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
+                         block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                         block_size: int, k_scale: float, v_scale: float, max_seq_len: int,
+                         workspace: torch.Tensor, partition_size: int = 512,
+                         stream=None) -> torch.Tensor:
+    """Split-K paged decode over an FP8 (e4m3) pool (workspace as for
+    pa_decode_splitk)."""
+    B, H, hkv, d, nb, mb = _fp8_decode_common(out, q, kv_cache, block_tables, seq_lens,
+                                              block_size)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_splitk_fp8(_dev(out, "out"), _dev(q, "q"), _dev(kv_cache, "kv_cache"),
+                                     _dev(block_tables, "block_tables"),
+                                     _dev(seq_lens, "seq_lens"), B, H, hkv, d, block_size, nb, mb,
+                                     float(scale), float(k_scale), float(v_scale),
+                                     _DTYPE[q.dtype], int(max_seq_len), int(partition_size),
+                                     _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
+           "pa_decode_splitk_fp8")
     return out
 
 

@@ -33,6 +33,8 @@ UNITS = [
     ("pa_decode_bf16_d64", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=1", "-DPA_INST_D=64"]),
     ("pa_decode_bf16_d128", "pa_decode_inst.cu", ["-DPA_INST_DTYPE=1", "-DPA_INST_D=128"]),
     ("pa_prefill_f16", "pa_prefill_inst.cu", ["-DPA_INST_DTYPE=0"]),
+    ("pa_decode_fp8_f16", "pa_decode_fp8_inst.cu", ["-DPA_INST_DTYPE=0"]),
+    ("pa_decode_fp8_bf16", "pa_decode_fp8_inst.cu", ["-DPA_INST_DTYPE=1"]),
     ("pa_prefill_bf16", "pa_prefill_inst.cu", ["-DPA_INST_DTYPE=1"]),
 ]
 

@@ -113,6 +113,27 @@ static bool make_q_map(CUtensorMap *map, const void *q, int dtype, int rows, int
     return r == CUDA_SUCCESS;
 }
 
+// FP8 pool as a 4-D byte tensor {D, Hkv, NB*bs, 2}; a box is one kv head's
+// 128-byte rows of `box_rows` tokens, with the 128-byte swizzle.
+static bool make_pool_map_fp8(CUtensorMap *map, const void *cache, int num_blocks,
+                              int block_size, int num_kv_heads, int head_size, int box_rows)
+{
+    cudaError_t err;
+    auto fn = encode_fn(&err);
+    if (!fn)
+        return false;
+    cuuint64_t dims[4] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads,
+                          (cuuint64_t)num_blocks * block_size, 2};
+    cuuint64_t strides[3] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads * head_size,
+                             (cuuint64_t)num_blocks * block_size * num_kv_heads * head_size};
+    cuuint32_t box[4] = {(cuuint32_t)head_size, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(cache), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Packed query rows [T, H, D] as a 3-D tensor {D, H, T}; a box is 64
 // elements of one head for 128 consecutive tokens, with the 128-byte swizzle.
 static bool make_q_rows_map(CUtensorMap *map, const void *q, int dtype, int num_tokens,
@@ -775,6 +796,143 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
     if (e == cudaErrorNotSupported)
         return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
+                                   const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_size, int block_size, int num_blocks,
+                                   int64_t key_stride, int64_t value_stride, pa_dtype src_dtype,
+                                   float k_scale, float v_scale, void *stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || !(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) ||
+        !isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (head_size != 128 || (src_dtype != PA_FP16 && src_dtype != PA_BF16))
+        return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return PA_OK;
+    const int row = num_kv_heads * head_size;
+    if (!key || !value || !kv_cache || !slot_mapping || key_stride < row || value_stride < row ||
+        key_stride % 8 || value_stride % 8 || !aligned(key, 16) || !aligned(value, 16) ||
+        !aligned(kv_cache, 16) || !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > 65535)
+        return PA_ERR_UNSUPPORTED;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    const int64_t plane = (int64_t)num_blocks * block_size * row;
+    auto launch = src_dtype == PA_BF16 ? launch_reshape_fp8_bf16 : launch_reshape_fp8_f16;
+    e = launch(key, value, kv_cache, slot_mapping, num_tokens, row, key_stride, value_stride,
+               plane, block_size, (int64_t)num_blocks * block_size, k_scale, v_scale, err,
+               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
+                                 const int32_t *block_tables, const int32_t *seq_lens,
+                                 int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                 int block_size, int num_blocks, int max_blocks_per_seq,
+                                 float scale, float k_scale, float v_scale, pa_dtype dtype,
+                                 bool split, int max_seq_len, int partition_size,
+                                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    pa_status st = check_decode_args(out, q, kv_cache, block_tables, seq_lens, num_seqs,
+                                     num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                                     max_blocks_per_seq, scale, dtype);
+    if (st != PA_OK)
+        return st;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (head_size != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (split && (max_seq_len < 0 || partition_size <= 0 || partition_size % kTok != 0))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PA_OK;
+    cudaError_t e;
+    unsigned int *err = device_error_word(&e);
+    if (!err)
+        return PA_ERR_CUDA;
+    alignas(64) CUtensorMap tmap;
+    if (!make_pool_map_fp8(&tmap, kv_cache, num_blocks, block_size, num_kv_heads, head_size,
+                           block_size))
+        return PA_ERR_CUDA;
+    const int group = num_heads / num_kv_heads;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto launch = dtype == PA_BF16 ? launch_decode_fp8_bf16 : launch_decode_fp8_f16;
+    DecodeParams p = {};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.err = err;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.qscale = scale * k_scale * kLog2e;
+    if (!split) {
+        p.part_tokens = 0;
+        p.max_parts = 1;
+        p.len_cap = max_blocks_per_seq * block_size;
+        e = launch(block_size, group, false, tmap, p, v_scale, dim3(num_kv_heads, num_seqs, 1), s);
+        return e == cudaSuccess ? PA_OK
+                                : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
+    }
+    const size_t parts = splitk_parts(max_seq_len, partition_size);
+    if (parts > 65535)
+        return PA_ERR_UNSUPPORTED;
+    const size_t need = pa_decode_splitk_workspace_size(num_seqs, num_heads, head_size,
+                                                        max_seq_len, partition_size);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return PA_ERR_WORKSPACE;
+    const WsLayout lay = ws_layout(num_seqs, num_heads, head_size, parts);
+    char *wsb = static_cast<char *>(workspace);
+    float *ws_o = reinterpret_cast<float *>(wsb + lay.o);
+    float *ws_ml = reinterpret_cast<float *>(wsb + lay.ml);
+    const int64_t cap_tab = (int64_t)max_blocks_per_seq * block_size;
+    const int64_t cap_ws = (int64_t)parts * partition_size;
+    p.ws_o = ws_o;
+    p.ws_ml = ws_ml;
+    p.part_tokens = partition_size;
+    p.max_parts = (int)parts;
+    p.len_cap = (int)(cap_tab < cap_ws ? cap_tab : cap_ws);
+    e = launch(block_size, group, true, tmap, p, v_scale,
+               dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
+    if (e != cudaSuccess)
+        return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
+    ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
+                      p.len_cap, 0, nullptr};
+    e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_fp8(void *out, const void *q, const void *kv_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int num_heads, int num_kv_heads, int head_size, int block_size,
+                        int num_blocks, int max_blocks_per_seq, float scale, float k_scale,
+                        float v_scale, pa_dtype dtype, void *stream)
+{
+    return decode_fp8_impl(out, q, kv_cache, block_tables, seq_lens, num_seqs, num_heads,
+                           num_kv_heads, head_size, block_size, num_blocks, max_blocks_per_seq,
+                           scale, k_scale, v_scale, dtype, false, 0, 0, nullptr, 0, stream);
+}
+
+pa_status pa_decode_splitk_fp8(void *out, const void *q, const void *kv_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                               int block_size, int num_blocks, int max_blocks_per_seq,
+                               float scale, float k_scale, float v_scale, pa_dtype dtype,
+                               int max_seq_len, int partition_size, void *workspace,
+                               size_t workspace_bytes, void *stream)
+{
+    return decode_fp8_impl(out, q, kv_cache, block_tables, seq_lens, num_seqs, num_heads,
+                           num_kv_heads, head_size, block_size, num_blocks, max_blocks_per_seq,
+                           scale, k_scale, v_scale, dtype, true, max_seq_len, partition_size,
+                           workspace, workspace_bytes, stream);
 }
 
 pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const float *lse_a,

@@ -10,6 +10,7 @@
 // pa.h, which the kernels' translation units do not include).
 #define PA_DEVERR_BLOCK_ID_ 0x1u
 #define PA_DEVERR_SEQ_LEN_ 0x2u
+#define PA_DEVERR_SLOT_ 0x4u
 #define PA_DEVERR_TIMEOUT_ 0x8u
 
 namespace pa {
@@ -87,6 +88,26 @@ cudaError_t launch_decode_tc_f16(int block_size, int group, int hg, bool split,
 cudaError_t launch_decode_tc_bf16(int block_size, int group, int hg, bool split,
                                   const CUtensorMap &pool, const CUtensorMap &qmap,
                                   const tc::TcParams &p, dim3 grid, cudaStream_t stream);
+
+// FP8 (e4m3) pool, head_size 128: decode on grid (Hkv, B[, parts]) and the
+// cache write on grid (ceil(Hkv*128/8/256), T).
+cudaError_t launch_decode_fp8_f16(int block_size, int group, bool split, const CUtensorMap &tmap,
+                                  const DecodeParams &p, float v_scale, dim3 grid,
+                                  cudaStream_t stream);
+cudaError_t launch_decode_fp8_bf16(int block_size, int group, bool split, const CUtensorMap &tmap,
+                                   const DecodeParams &p, float v_scale, dim3 grid,
+                                   cudaStream_t stream);
+cudaError_t launch_reshape_fp8_f16(const void *key, const void *value, void *cache,
+                                   const int64_t *slots, int num_tokens, int row_elems,
+                                   int64_t key_stride, int64_t value_stride, int64_t plane_elems,
+                                   int block_size, int64_t num_slots, float k_scale,
+                                   float v_scale, unsigned int *err, cudaStream_t stream);
+cudaError_t launch_reshape_fp8_bf16(const void *key, const void *value, void *cache,
+                                    const int64_t *slots, int num_tokens, int row_elems,
+                                    int64_t key_stride, int64_t value_stride,
+                                    int64_t plane_elems, int block_size, int64_t num_slots,
+                                    float k_scale, float v_scale, unsigned int *err,
+                                    cudaStream_t stream);
 
 // Parameters of the tensor-core prefill kernel.
 struct PrefillParams {

@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
               "pa_device_errors", "pa_status_string", "pa_version", "pa_copy_blocks",
               "pa_validate_block_mapping", "pa_selftest_wait_timeout", "pa_prefill",
               "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
-              "pa_cascade_decode_workspace_size"):
+              "pa_cascade_decode_workspace_size", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+              "pa_decode_splitk_fp8"):
         assert n in names
 
 
@@ -242,3 +243,21 @@ def test_merge_and_cascade_reject_bad_arguments(pa):
                   [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
     assert g(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, 128, 16, 8, 4, 0.1, 0, 64, 512, FAKE,
              1 << 20, None) == 1                                           # lse missing
+
+
+def test_fp8_calls_reject_bad_arguments(pa):
+    lib = _raw(pa)
+    f = lib.pa_reshape_and_cache_fp8
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [ctypes.c_int64] * 2 +
+                  [ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p])
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, 128, 128, 0, 1.0, 1.0, None) == 2   # D 64
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 8, 256, 256, 0, 0.0, 1.0, None) == 1  # scale
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 8, 256, 256, 0, 1.0, -1.0, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, 256, 256, 0, 1.0, 1.0, None) == 0
+    g = lib.pa_decode_fp8
+    g.restype = ctypes.c_int
+    g.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 + [ctypes.c_float] * 3 +
+                  [ctypes.c_int, ctypes.c_void_p])
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 64, 16, 8, 4, 0.1, 1.0, 1.0, 0, None) == 2
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 128, 16, 8, 4, 0.1, 0.0, 1.0, 0, None) == 1
