@@ -663,14 +663,63 @@ __global__ void __launch_bounds__(256)
         const T *ea = reinterpret_cast<const T *>(&ua);
         const T *eb = reinterpret_cast<const T *>(&ub);
         T *er = reinterpret_cast<T *>(&res);
+        // An empty part (weight 0) is not read: its rows may hold anything.
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            er[i] = Elem<T>::from((wa * Elem<T>::one(ea[i]) + wb * Elem<T>::one(eb[i])) * inv);
+        for (int i = 0; i < 8; ++i) {
+            const float xa = wa > 0.f ? wa * Elem<T>::one(ea[i]) : 0.f;
+            const float xb = wb > 0.f ? wb * Elem<T>::one(eb[i]) : 0.f;
+            er[i] = Elem<T>::from((xa + xb) * inv);
+        }
         lse = M + __logf(wa + wb);
     }
     *reinterpret_cast<uint4 *>(out + off) = res;
     if (out_lse && v == 0)
         out_lse[row] = lse;
+}
+
+// N-way merge of parts [nparts][rows][head_size] with log-sum-exps
+// [nparts][rows]: out = sum_i w_i o_i / sum_i w_i, w_i = exp(lse_i - max).
+// Parts with lse = -inf carry no weight and are not read; a row whose parts
+// are all empty is zero.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    merge_parts_kernel(T *__restrict__ out, const T *__restrict__ parts,
+                       const float *__restrict__ lse_parts, int nparts, int64_t rows,
+                       int head_size)
+{
+    const int vpr = head_size / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t row = idx / vpr;
+    if (row >= rows)
+        return;
+    const int v = (int)(idx - row * vpr);
+    float M = -INFINITY;
+    for (int i = 0; i < nparts; ++i)
+        M = fmaxf(M, lse_parts[(size_t)i * rows + row]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float den = 0.f;
+    if (M != -INFINITY) {
+        for (int i = 0; i < nparts; ++i) {
+            const float li = lse_parts[(size_t)i * rows + row];
+            if (li == -INFINITY)
+                continue;
+            const float w = __expf(li - M);
+            den += w;
+            const uint4 u = *reinterpret_cast<const uint4 *>(
+                parts + ((size_t)i * rows + row) * head_size + (size_t)v * 8);
+            const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                acc[j] = fmaf(w, Elem<T>::one(e[j]), acc[j]);
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    uint4 res;
+    T *er = reinterpret_cast<T *>(&res);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        er[j] = Elem<T>::from(acc[j] * inv);
+    *reinterpret_cast<uint4 *>(out + (size_t)row * head_size + (size_t)v * 8) = res;
 }
 
 // Cascade setup, one CTA per sequence: the prefix pass's request metadata
@@ -736,12 +785,19 @@ pa_status pa_decode_splitk_lse(void *out, float *lse, const void *q, const void 
                               workspace, workspace_bytes, stream);
 }
 
-pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
-                     const int32_t *block_tables, int64_t block_table_stride,
-                     const int32_t *seq_lens, const int32_t *query_start_loc, int num_reqs,
-                     int num_tokens, int max_query_len, int num_heads, int num_kv_heads,
-                     int head_size, int block_size, int num_blocks, int max_blocks_per_seq,
-                     float scale, int causal, pa_dtype dtype, void *stream)
+} // extern "C"
+
+// Prefill launch; key_split > 1 (non-causal only) gives every CTA a chunk of
+// chunk_tiles key tiles and writes part c of out / lse at c * part_stride /
+// c * lse_part_stride elements.
+static pa_status prefill_impl(void *out, float *lse, const void *q, const void *kv_cache,
+                              const int32_t *block_tables, int64_t block_table_stride,
+                              const int32_t *seq_lens, const int32_t *query_start_loc,
+                              int num_reqs, int num_tokens, int max_query_len, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int num_blocks,
+                              int max_blocks_per_seq, float scale, int causal, pa_dtype dtype,
+                              int key_split, int chunk_tiles, int64_t part_stride,
+                              int64_t lse_part_stride, void *stream)
 {
     if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
         num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_size <= 0 ||
@@ -788,7 +844,13 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
     p.max_query_len = max_query_len;
     p.causal = causal ? 1 : 0;
     p.qscale = scale * kLog2e;
-    const dim3 grid((unsigned)((max_query_len + 255) / 256), (unsigned)num_heads,
+    if (key_split < 1 || (key_split > 1 && (causal || chunk_tiles < 1)))
+        return PA_ERR_INVALID_ARG;
+    p.key_split = key_split;
+    p.chunk_tiles = key_split > 1 ? chunk_tiles : 1;
+    p.part_stride = part_stride;
+    p.lse_part_stride = lse_part_stride;
+    const dim3 grid((unsigned)((max_query_len + 255) / 256 * key_split), (unsigned)num_heads,
                     (unsigned)num_reqs);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = dtype == PA_BF16 ? launch_prefill_bf16(head_size, block_size, pmap, qmap, p, grid, st)
@@ -796,6 +858,21 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
     if (e == cudaErrorNotSupported)
         return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" {
+
+pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
+                     const int32_t *block_tables, int64_t block_table_stride,
+                     const int32_t *seq_lens, const int32_t *query_start_loc, int num_reqs,
+                     int num_tokens, int max_query_len, int num_heads, int num_kv_heads,
+                     int head_size, int block_size, int num_blocks, int max_blocks_per_seq,
+                     float scale, int causal, pa_dtype dtype, void *stream)
+{
+    return prefill_impl(out, lse, q, kv_cache, block_tables, block_table_stride, seq_lens,
+                        query_start_loc, num_reqs, num_tokens, max_query_len, num_heads,
+                        num_kv_heads, head_size, block_size, num_blocks, max_blocks_per_seq,
+                        scale, causal, dtype, 1, 1, 0, 0, stream);
 }
 
 pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
@@ -964,27 +1041,30 @@ pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const
 }
 
 // Cascade workspace: [256 B header: query_start_loc {0, B}, prefix seq_len]
-// [suffix lengths] [suffix tables] [prefix output, dtype] [prefix lse]
-// [suffix output, dtype] [suffix lse] [split-K workspace], 256-byte aligned.
+// [suffix lengths] [suffix tables] [parts: prefix key chunks then the suffix,
+// dtype] [their lse] [split-K workspace], 256-byte aligned.  The prefix pass
+// is split over at most kMaxPrefixSplits key chunks.
+constexpr int kMaxPrefixSplits = 16;
+
 struct CascadeLayout {
-    size_t sl, bt, o_pre, lse_pre, o_suf, lse_suf, ws, ws_bytes, total;
-    int suffix_cols;
+    size_t sl, bt, parts, lse, ws, ws_bytes, total;
+    int suffix_cols, max_parts;
 };
 
 static CascadeLayout cascade_layout(int num_seqs, int num_heads, int head_size,
-                                    int max_blocks_per_seq, int prefix_blocks,
+                                    int max_blocks_per_seq, int prefix_blocks, int block_size,
                                     int max_suffix_len, int partition_size)
 {
     CascadeLayout c;
     const size_t rows = (size_t)num_seqs * num_heads;
+    const int prefix_tiles = (prefix_blocks * block_size + 127) / 128;
+    c.max_parts = (prefix_tiles < kMaxPrefixSplits ? prefix_tiles : kMaxPrefixSplits) + 1;
     c.suffix_cols = max_blocks_per_seq - prefix_blocks > 0 ? max_blocks_per_seq - prefix_blocks : 1;
     c.sl = 256;
     c.bt = c.sl + round_up((size_t)num_seqs * 4, 256);
-    c.o_pre = c.bt + round_up((size_t)num_seqs * c.suffix_cols * 4, 256);
-    c.lse_pre = c.o_pre + round_up(rows * head_size * 2, 256);
-    c.o_suf = c.lse_pre + round_up(rows * 4, 256);
-    c.lse_suf = c.o_suf + round_up(rows * head_size * 2, 256);
-    c.ws = c.lse_suf + round_up(rows * 4, 256);
+    c.parts = c.bt + round_up((size_t)num_seqs * c.suffix_cols * 4, 256);
+    c.lse = c.parts + round_up((size_t)c.max_parts * rows * head_size * 2, 256);
+    c.ws = c.lse + round_up((size_t)c.max_parts * rows * 4, 256);
     c.ws_bytes = ws_layout(num_seqs, num_heads, head_size,
                            splitk_parts(max_suffix_len, partition_size)).total;
     c.total = c.ws + c.ws_bytes;
@@ -1001,7 +1081,7 @@ size_t pa_cascade_decode_workspace_size(int num_seqs, int num_heads, int head_si
         return 0;
     const int suffix = max_seq_len - prefix_blocks * block_size;
     return cascade_layout(num_seqs, num_heads, head_size, max_blocks_per_seq, prefix_blocks,
-                          suffix > 0 ? suffix : 0, partition_size).total;
+                          block_size, suffix > 0 ? suffix : 0, partition_size).total;
 }
 
 pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
@@ -1029,7 +1109,7 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     const int P = prefix_blocks * block_size;
     const int max_suffix = max_seq_len > P ? max_seq_len - P : 0;
     const CascadeLayout c = cascade_layout(num_seqs, num_heads, head_size, max_blocks_per_seq,
-                                           prefix_blocks, max_suffix, partition_size);
+                                           prefix_blocks, block_size, max_suffix, partition_size);
     if (!workspace || workspace_bytes < c.total || !aligned(workspace, 256))
         return PA_ERR_WORKSPACE;
     cudaError_t e;
@@ -1040,32 +1120,54 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     int32_t *hdr = reinterpret_cast<int32_t *>(w);
     int32_t *sl_suf = reinterpret_cast<int32_t *>(w + c.sl);
     int32_t *bt_suf = reinterpret_cast<int32_t *>(w + c.bt);
-    void *o_pre = w + c.o_pre;
-    float *lse_pre = reinterpret_cast<float *>(w + c.lse_pre);
-    void *o_suf = w + c.o_suf;
-    float *lse_suf = reinterpret_cast<float *>(w + c.lse_suf);
+    const size_t rows = (size_t)num_seqs * num_heads;
+    char *parts = w + c.parts;
+    float *lse_parts = reinterpret_cast<float *>(w + c.lse);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Key chunks of the prefix pass: enough CTAs for two waves of the SMs.
+    const int sms = sm_count(&e);
+    if (!sms)
+        return PA_ERR_CUDA;
+    const int prefix_tiles = (P + 127) / 128;
+    const int ctas_per_chunk = ((num_seqs + 255) / 256) * num_heads;
+    int nsplit = (2 * sms + ctas_per_chunk - 1) / ctas_per_chunk;
+    nsplit = nsplit < 1 ? 1 : (nsplit > c.max_parts - 1 ? c.max_parts - 1 : nsplit);
+    const int chunk_tiles = (prefix_tiles + nsplit - 1) / nsplit;
+    nsplit = (prefix_tiles + chunk_tiles - 1) / chunk_tiles;
     cascade_setup_kernel<<<num_seqs, 128, 0, s>>>(block_tables, seq_lens, num_seqs,
                                                   max_blocks_per_seq, prefix_blocks, block_size,
                                                   c.suffix_cols, hdr, sl_suf, bt_suf, err);
     if (cudaGetLastError() != cudaSuccess)
         return PA_ERR_CUDA;
     // 1. Every query against the shared prefix, no causal mask: one request
-    //    whose B query rows are the B sequences' queries.
-    st = pa_prefill(o_pre, lse_pre, q, kv_cache, block_tables, max_blocks_per_seq, hdr + 2, hdr, 1,
-                    num_seqs, num_seqs, num_heads, num_kv_heads, head_size, block_size,
-                    num_blocks, prefix_blocks, scale, 0, dtype, stream);
+    //    whose B query rows are the B sequences' queries, split over nsplit
+    //    key chunks (parts 0 .. nsplit-1).
+    const int64_t part_elems = (int64_t)rows * head_size;
+    st = prefill_impl(parts, lse_parts, q, kv_cache, block_tables, max_blocks_per_seq, hdr + 2,
+                      hdr, 1, num_seqs, num_seqs, num_heads, num_kv_heads, head_size,
+                      block_size, num_blocks, prefix_blocks, scale, 0, dtype, nsplit,
+                      chunk_tiles, part_elems, (int64_t)rows, stream);
     if (st != PA_OK)
         return st;
-    // 2. Each sequence's own suffix.
-    st = decode_splitk_impl(o_suf, lse_suf, q, kv_cache, bt_suf, sl_suf, num_seqs, num_heads,
-                            num_kv_heads, head_size, block_size, num_blocks, c.suffix_cols, scale,
-                            dtype, max_suffix, partition_size, w + c.ws, c.ws_bytes, stream);
+    // 2. Each sequence's own suffix (part nsplit).
+    st = decode_splitk_impl(parts + (size_t)nsplit * part_elems * 2, lse_parts + (size_t)nsplit * rows,
+                            q, kv_cache, bt_suf, sl_suf, num_seqs, num_heads, num_kv_heads,
+                            head_size, block_size, num_blocks, c.suffix_cols, scale, dtype,
+                            max_suffix, partition_size, w + c.ws, c.ws_bytes, stream);
     if (st != PA_OK)
         return st;
-    // 3. Merge the two.
-    return pa_merge_attn_states(out, nullptr, o_pre, lse_pre, o_suf, lse_suf, num_seqs, num_heads,
-                                head_size, dtype, stream);
+    // 3. Merge the nsplit + 1 parts.
+    const int64_t threads = (int64_t)rows * (head_size / 8);
+    const unsigned grid = (unsigned)((threads + 255) / 256);
+    if (dtype == PA_BF16)
+        merge_parts_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            static_cast<__nv_bfloat16 *>(out), reinterpret_cast<const __nv_bfloat16 *>(parts),
+            lse_parts, nsplit + 1, (int64_t)rows, head_size);
+    else
+        merge_parts_kernel<__half><<<grid, 256, 0, s>>>(
+            static_cast<__half *>(out), reinterpret_cast<const __half *>(parts), lse_parts,
+            nsplit + 1, (int64_t)rows, head_size);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,

@@ -121,6 +121,12 @@ struct PrefillParams {
     int num_tokens, num_heads, num_kv_heads, num_blocks, max_blocks, max_query_len;
     int causal;
     float qscale;                   // scale * log2(e)
+    // Key split (non-causal only): CTA chunk c attends keys
+    // [c*chunk_tiles*128, (c+1)*chunk_tiles*128) and writes part c of out
+    // and lse, part_stride / lse_part_stride elements apart.  key_split 1:
+    // every key, out and lse as given.
+    int key_split, chunk_tiles;
+    long long part_stride, lse_part_stride;
 };
 
 // Prefill over the paged cache on grid (ceil(max_query_len/256), H, R).

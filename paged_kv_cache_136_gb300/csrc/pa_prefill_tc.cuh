@@ -134,7 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+255
     const int r = blockIdx.z;
     const int h = blockIdx.y;
-    const int qb = (int)gridDim.x - 1 - (int)blockIdx.x; // latest (heaviest) rows first
+    const int nsplit = p.key_split;
+    const int csplit = (int)blockIdx.x % nsplit;
+    const int qb = (int)gridDim.x / nsplit - 1 - (int)blockIdx.x / nsplit; // heaviest rows first
     const int i0 = qb * kRowsPerCta;
     const int q0 = __ldg(p.query_start_loc + r);
     const int q1 = __ldg(p.query_start_loc + r + 1);
@@ -149,15 +151,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (i0 >= q_len)
         return;
     const int ctx = L - q_len;
+    // Keys of this CTA: [kt0 * 128, key_hi) (the whole request unless split).
+    const int kt0 = csplit * p.chunk_tiles;
+    const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles) * kTileN) : L;
+    T *const out_base = reinterpret_cast<T *>(p.out) + (size_t)csplit * (size_t)p.part_stride;
+    float *const lse_base = p.lse ? p.lse + (size_t)csplit * (size_t)p.lse_part_stride : nullptr;
     int nv[2], nt[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         nv[t] = min(max(q_len - (i0 + t * kTileM), 0), kTileM);
-        const int ext = p.causal ? min(L, ctx + i0 + t * kTileM + nv[t]) : L;
-        nt[t] = nv[t] > 0 ? (ext + kTileN - 1) / kTileN : 0;
+        const int ext = p.causal ? min(L, ctx + i0 + t * kTileM + nv[t]) : key_hi;
+        nt[t] = nv[t] > 0 ? max(0, (ext - kt0 * kTileN + kTileN - 1) / kTileN) : 0;
     }
     const int n = max(nt[0], nt[1]); // key tiles loaded
-    const bool tail = n * kTileN > L; // the last key tile reaches past seq_len
+    if (n == 0) {
+        // An empty key chunk: zero rows and -inf log-sum-exps (an empty part).
+        for (int i = tid; i < (nv[0] + nv[1]) * D; i += kThreads) {
+            const size_t tok = (size_t)(q0 + i0 + i / D);
+            out_base[(tok * p.num_heads + h) * D + i % D] = T(0.f);
+        }
+        if (lse_base)
+            for (int i = tid; i < nv[0] + nv[1]; i += kThreads)
+                lse_base[(size_t)(q0 + i0 + i) * p.num_heads + h] = -INFINITY;
+        return;
+    }
+    const bool tail = (kt0 + n) * kTileN > L; // the last key tile reaches past seq_len
     const int fixer = nt[1] == n ? 1 : 0;
 
     if (tid == 0) {
@@ -200,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Block-table entries of 64 blocks live in lane registers (this
         // window and the next), refreshed every 32 blocks.
-        const int nblk_req = (L + BS - 1) / BS;
+        const int nblk_req = (key_hi + BS - 1) / BS;
         const int32_t *bt = p.block_tables + (size_t)r * (size_t)p.bt_stride;
-        int cb = 0;
-        int cur = lane < nblk_req ? __ldg(bt + lane) : -1;
-        int nxt = 32 + lane < nblk_req ? __ldg(bt + 32 + lane) : -1;
+        int cb = (kt0 * BPT) & ~31;
+        int cur = cb + lane < nblk_req ? __ldg(bt + cb + lane) : -1;
+        int nxt = cb + 32 + lane < nblk_req ? __ldg(bt + cb + 32 + lane) : -1;
         for (int g = 0; g < 2 * n; ++g) {
             const int k = g >> 1, plane = g & 1, slot = g % S;
             if (g >= S && !warp_wait(&m->kv_empty[slot], ((g / S) - 1) & 1, lane)) {
@@ -212,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT_);
                 break;
             }
-            const int jt = k * BPT;
+            const int jt = (kt0 + k) * BPT;
             if (jt >= cb + 32) {
                 cb += 32;
                 cur = nxt;
@@ -329,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ntt = nt[wg];
         if (ntt > 0) {
             const int pos = ctx + i0 + wg * kTileM + row;
-            const int lim = p.causal ? min(L, pos + 1) : L;              // keys < lim
-            const int lim_lo = p.causal ? min(L, ctx + i0 + wg * kTileM + 1) : L;
+            const int lim = p.causal ? min(L, pos + 1) : key_hi;         // keys < lim
+            const int lim_lo = p.causal ? min(L, ctx + i0 + wg * kTileM + 1) : key_hi;
             const float qs = p.qscale;
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
@@ -352,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     m8[j] = -INFINITY;
-                if ((k + 1) * kTileN > lim_lo) {
-                    const int kl = lim - k * kTileN; // keys of this tile below the limit
+                if ((kt0 + k + 1) * kTileN > lim_lo) {
+                    const int kl = lim - (kt0 + k) * kTileN; // keys of this tile below the limit
 #pragma unroll
                     for (int i = 0; i < kTileN; ++i) {
                         const float x = i < kl ? __uint_as_float(sv[i]) : -INFINITY;
@@ -422,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Zero the V rows of keys >= seq_len in the last tile.
                     const int gv = 2 * k + 1;
                     ok = warp_wait(&m->kv_full[gv % S], (gv / S) & 1, lane);
-                    if (ok && k * kTileN + row >= L) {
+                    if (ok && (kt0 + k) * kTileN + row >= L) {
                         uint8_t *vrow = smem + Gm::kOffKV + (gv % S) * TB + row * 128;
 #pragma unroll
                         for (int hf = 0; hf < NH; ++hf)
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = row < nv[wg];
                 const size_t tok = (size_t)(q0 + i0 + wg * kTileM + row);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                T *o = reinterpret_cast<T *>(p.out) + (tok * p.num_heads + h) * D;
+                T *o = out_base + (tok * p.num_heads + h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
@@ -468,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                     }
                 }
-                if (p.lse && valid)
-                    p.lse[tok * p.num_heads + h] =
+                if (lse_base && valid)
+                    lse_base[tok * p.num_heads + h] =
                         l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
         }

@@ -54,6 +54,8 @@ def test_merge_attn_states_matches_oracle(pa, dtype, D):
     lse_b[1, :] = -float("inf")                   # empty second part
     lse_a[2, :] = lse_b[2, :] = -float("inf")     # both empty
     lse_a[3, :] = lse_b[3, :] + 60                # one part dominates
+    o_a[0, 1, :] = float("nan")                   # an empty part's rows are not read
+    o_b[1, 2, :] = float("nan")
     out = torch.empty_like(o_a)
     out_lse = torch.empty_like(lse_a)
     pa.pa_merge_attn_states(out, o_a, lse_a, o_b, lse_b, out_lse=out_lse)
@@ -61,6 +63,7 @@ def test_merge_attn_states_matches_oracle(pa, dtype, D):
     orc = get()
     wa = orc.widen(wl.bits(o_a), wl.ORACLE_DTYPE[dtype])
     wb = orc.widen(wl.bits(o_b), wl.ORACLE_DTYPE[dtype])
+    wa[0], wb[1] = 0.0, 0.0                       # the oracle's empty parts hold zeros
     ref, ref_lse = orc.merge_attn_states(wa, lse_a.double().cpu().numpy(), wb,
                                          lse_b.double().cpu().numpy())
     check_attention(out, ref, what="merge")
