@@ -569,9 +569,9 @@ def fp8_workload(name: str, args, peak_gbs: float) -> dict:
     out = torch.empty_like(w.q)
     msl = int(w.seq_lens.max().item())
     P = args.partition
-    ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads, w.head_size,
-                                                        msl, P), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.empty(pa.pa_decode_splitk_fp8_workspace_size(w.num_seqs, w.num_heads,
+                                                            w.head_size, msl, P),
+                     dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     def write():

@@ -201,8 +201,13 @@ pa_status pa_decode_splitk_noalloc(void *out, const void *q, const void *kv_cach
  *   flagged (PA_DEVERR_SLOT).
  * pa_decode_fp8 / pa_decode_splitk_fp8: pa_decode / pa_decode_splitk over
  *   keys k_scale * e4m3(K) and values v_scale * e4m3(V); q and out are
- *   `dtype`; the split-K workspace is the same size as pa_decode_splitk's.
+ *   `dtype`.  The split-K call runs on the tensor cores (kind::f8f6f4, the
+ *   query carried as three e4m3 parts with a row scale) and needs
+ *   pa_decode_splitk_fp8_workspace_size bytes of workspace (256-byte
+ *   aligned); the one-pass call runs on the CUDA cores and needs none.
  */
+size_t pa_decode_splitk_fp8_workspace_size(int num_seqs, int num_heads, int head_size,
+                                           int max_seq_len, int partition_size);
 pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_cache,
                                    const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
                                    int head_size, int block_size, int num_blocks,

@@ -22,7 +22,7 @@ __all__ = [
     "pa_device_errors", "pa_selftest_wait_timeout", "pa_copy_blocks", "pa_prefill",
     "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
     "pa_cascade_decode_workspace_size", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-    "pa_decode_splitk_fp8",
+    "pa_decode_splitk_fp8", "pa_decode_splitk_fp8_workspace_size",
     "pa_validate_block_mapping", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
@@ -78,6 +78,8 @@ _lib.pa_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I
 _lib.pa_decode_fp8.restype = _I
 _lib.pa_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I,
                                _P]
+_lib.pa_decode_splitk_fp8_workspace_size.restype = _SZ
+_lib.pa_decode_splitk_fp8_workspace_size.argtypes = [_I, _I, _I, _I, _I]
 _lib.pa_decode_splitk_fp8.restype = _I
 _lib.pa_decode_splitk_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F,
                                       _F, _I, _I, _I, _P, _SZ, _P]
@@ -433,13 +435,19 @@ def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
     return out
 
 
+def pa_decode_splitk_fp8_workspace_size(num_seqs: int, num_heads: int, head_size: int,
+                                        max_seq_len: int, partition_size: int = 512) -> int:
+    return int(_lib.pa_decode_splitk_fp8_workspace_size(num_seqs, num_heads, head_size,
+                                                        max_seq_len, partition_size))
+
+
 def pa_decode_splitk_fp8(out: torch.Tensor, q: torch.Tensor, kv_cache: torch.Tensor,
                          block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                          block_size: int, k_scale: float, v_scale: float, max_seq_len: int,
                          workspace: torch.Tensor, partition_size: int = 512,
                          stream=None) -> torch.Tensor:
-    """Split-K paged decode over an FP8 (e4m3) pool (workspace as for
-    pa_decode_splitk)."""
+    """Split-K paged decode over an FP8 (e4m3) pool on the tensor cores;
+    ``workspace`` holds pa_decode_splitk_fp8_workspace_size bytes."""
     B, H, hkv, d, nb, mb = _fp8_decode_common(out, q, kv_cache, block_tables, seq_lens,
                                               block_size)
     ws_bytes = workspace.numel() * workspace.element_size()

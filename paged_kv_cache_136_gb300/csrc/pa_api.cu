@@ -116,7 +116,8 @@ static bool make_q_map(CUtensorMap *map, const void *q, int dtype, int rows, int
 // FP8 pool as a 4-D byte tensor {D, Hkv, NB*bs, 2}; a box is one kv head's
 // 128-byte rows of `box_rows` tokens, with the 128-byte swizzle.
 static bool make_pool_map_fp8(CUtensorMap *map, const void *cache, int num_blocks,
-                              int block_size, int num_kv_heads, int head_size, int box_rows)
+                              int block_size, int num_kv_heads, int head_size, int box_rows,
+                              int box_heads = 1)
 {
     cudaError_t err;
     auto fn = encode_fn(&err);
@@ -126,9 +127,27 @@ static bool make_pool_map_fp8(CUtensorMap *map, const void *cache, int num_block
                           (cuuint64_t)num_blocks * block_size, 2};
     cuuint64_t strides[3] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads * head_size,
                              (cuuint64_t)num_blocks * block_size * num_kv_heads * head_size};
-    cuuint32_t box[4] = {(cuuint32_t)head_size, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t box[4] = {(cuuint32_t)head_size, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(cache), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// e4m3 query parts [3][rows][128] as a 2-D byte tensor {128, 3*rows}; a box
+// is `box_rows` rows of one part.
+static bool make_q_parts_map(CUtensorMap *map, const void *parts, int rows, int box_rows)
+{
+    cudaError_t err;
+    auto fn = encode_fn(&err);
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {128, (cuuint64_t)rows * 3};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(parts), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -908,6 +927,22 @@ pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, void *kv_
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// FP8 split-K workspace: the 16-bit layout, then the query's e4m3 parts
+// [3][B*H][128] and its row scales [B*H] (tensor-core path).
+static size_t fp8_ws_extra(int num_seqs, int num_heads, int head_size)
+{
+    const size_t rows = (size_t)num_seqs * num_heads;
+    return round_up(3 * rows * head_size, 256) + round_up(rows * 4, 256);
+}
+
+size_t pa_decode_splitk_fp8_workspace_size(int num_seqs, int num_heads, int head_size,
+                                           int max_seq_len, int partition_size)
+{
+    const size_t base = pa_decode_splitk_workspace_size(num_seqs, num_heads, head_size,
+                                                        max_seq_len, partition_size);
+    return base ? base + fp8_ws_extra(num_seqs, num_heads, head_size) : 0;
+}
+
 static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
                                  const int32_t *block_tables, const int32_t *seq_lens,
                                  int num_seqs, int num_heads, int num_kv_heads, int head_size,
@@ -962,8 +997,8 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
     const size_t parts = splitk_parts(max_seq_len, partition_size);
     if (parts > 65535)
         return PA_ERR_UNSUPPORTED;
-    const size_t need = pa_decode_splitk_workspace_size(num_seqs, num_heads, head_size,
-                                                        max_seq_len, partition_size);
+    const size_t need = pa_decode_splitk_fp8_workspace_size(num_seqs, num_heads, head_size,
+                                                            max_seq_len, partition_size);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
         return PA_ERR_WORKSPACE;
     const WsLayout lay = ws_layout(num_seqs, num_heads, head_size, parts);
@@ -972,11 +1007,76 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
     float *ws_ml = reinterpret_cast<float *>(wsb + lay.ml);
     const int64_t cap_tab = (int64_t)max_blocks_per_seq * block_size;
     const int64_t cap_ws = (int64_t)parts * partition_size;
+    const int len_cap = (int)(cap_tab < cap_ws ? cap_tab : cap_ws);
+    if (kernel_choice() != kKernelSimt) {
+        // Tensor cores: query prepass, plan, persistent split-K, reduce.
+        const int rows = num_seqs * num_heads;
+        uint8_t *qparts = reinterpret_cast<uint8_t *>(wsb + lay.total);
+        float *qscales = reinterpret_cast<float *>(wsb + lay.total +
+                                                   round_up(3 * (size_t)rows * head_size, 256));
+        const int hg = tc::heads_per_cta(group, num_kv_heads);
+        const int ngroups = num_kv_heads / hg;
+        const int box_rows = block_size < 128 / hg ? block_size : 128 / hg;
+        alignas(64) CUtensorMap pmap, qmap;
+        if (!make_pool_map_fp8(&pmap, kv_cache, num_blocks, block_size, num_kv_heads, head_size,
+                               box_rows, hg) ||
+            !make_q_parts_map(&qmap, qparts, rows, hg * group))
+            return PA_ERR_CUDA;
+        e = dtype == PA_BF16 ? launch_quantize_q_bf16(q, qparts, qscales, rows, s)
+                             : launch_quantize_q_f16(q, qparts, qscales, rows, s);
+        if (e != cudaSuccess)
+            return PA_ERR_CUDA;
+        uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
+        uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
+        if (dtype == PA_BF16)
+            tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
+                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
+                static_cast<__nv_bfloat16 *>(out), nullptr, err);
+        else
+            tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
+                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
+                static_cast<__half *>(out), nullptr, err);
+        if (cudaGetLastError() != cudaSuccess)
+            return PA_ERR_CUDA;
+        tc::TcParams t = {};
+        t.out = out;
+        t.block_tables = block_tables;
+        t.seq_lens = seq_lens;
+        t.err = err;
+        t.hdr = hdr;
+        t.units = units;
+        t.ws_o = ws_o;
+        t.ws_ml = ws_ml;
+        t.num_heads = num_heads;
+        t.num_kv_heads = num_kv_heads;
+        t.num_groups = ngroups;
+        t.num_blocks = num_blocks;
+        t.max_blocks = max_blocks_per_seq;
+        t.part_tokens = partition_size;
+        t.max_parts = (int)parts;
+        t.len_cap = len_cap;
+        t.qscale = scale * k_scale * kLog2e;
+        const int sms = sm_count(&e);
+        if (!sms)
+            return PA_ERR_CUDA;
+        const size_t bound = (size_t)num_seqs * ngroups * parts;
+        const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
+        auto tl = dtype == PA_BF16 ? launch_decode_tc_fp8_bf16 : launch_decode_tc_fp8_f16;
+        e = tl(block_size, group, hg, pmap, qmap, t, qscales, rows, v_scale, dim3(grid), s);
+        if (e != cudaSuccess)
+            return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
+        if (parts > 1) {
+            ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
+                              len_cap, 1, nullptr};
+            e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
+        }
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     p.ws_o = ws_o;
     p.ws_ml = ws_ml;
     p.part_tokens = partition_size;
     p.max_parts = (int)parts;
-    p.len_cap = (int)(cap_tab < cap_ws ? cap_tab : cap_ws);
+    p.len_cap = len_cap;
     e = launch(block_size, group, true, tmap, p, v_scale,
                dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
     if (e != cudaSuccess)

@@ -109,6 +109,21 @@ cudaError_t launch_reshape_fp8_bf16(const void *key, const void *value, void *ca
                                     float k_scale, float v_scale, unsigned int *err,
                                     cudaStream_t stream);
 
+// FP8 pool on the tensor cores (split-K, persistent grid fed by the plan):
+// the query prepass writes three e4m3 parts [3][rows][128] and row scales.
+cudaError_t launch_decode_tc_fp8_f16(int block_size, int group, int hg, const CUtensorMap &pool,
+                                     const CUtensorMap &qmap, const tc::TcParams &p,
+                                     const float *q_scales, int q_rows, float v_scale, dim3 grid,
+                                     cudaStream_t stream);
+cudaError_t launch_decode_tc_fp8_bf16(int block_size, int group, int hg,
+                                      const CUtensorMap &pool, const CUtensorMap &qmap,
+                                      const tc::TcParams &p, const float *q_scales, int q_rows,
+                                      float v_scale, dim3 grid, cudaStream_t stream);
+cudaError_t launch_quantize_q_f16(const void *q, uint8_t *parts, float *scales, int rows,
+                                  cudaStream_t stream);
+cudaError_t launch_quantize_q_bf16(const void *q, uint8_t *parts, float *scales, int rows,
+                                   cudaStream_t stream);
+
 // Parameters of the tensor-core prefill kernel.
 struct PrefillParams {
     void *out;                      // [num_tokens, H, D]

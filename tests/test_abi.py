@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
               "pa_validate_block_mapping", "pa_selftest_wait_timeout", "pa_prefill",
               "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
               "pa_cascade_decode_workspace_size", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
-              "pa_decode_splitk_fp8"):
+              "pa_decode_splitk_fp8", "pa_decode_splitk_fp8_workspace_size"):
         assert n in names
 
 

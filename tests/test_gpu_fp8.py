@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import workload as wl
-from tests._parity import check_attention, splitk_workspace
+from tests._parity import check_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -17,6 +17,11 @@ def pa():
     import paged_kv_cache_136_gb300 as pa
     pa.pa_device_errors(clear=True)
     return pa
+
+
+def _ws(pa, w, msl, part):
+    n = pa.pa_decode_splitk_fp8_workspace_size(w.num_seqs, w.num_heads, w.head_size, msl, part)
+    return torch.empty(n, dtype=torch.uint8, device=w.q.device)
 
 
 def _oracle_decode_fp8(w, items=None, cache=None):
@@ -52,6 +57,7 @@ CASES = [
     ("gqa8b", 24, 16, None),          # G 4
     ("gqa8b", 16, 32, (16, 8)),       # G 2, block 32
     ("long", 2, 32, None),            # G 8, long (made short below)
+    ("gqa8b", 10, 16, (12, 3)),       # G 4, 3 kv heads: one kv head per CTA
 ]
 
 
@@ -67,7 +73,7 @@ def test_decode_fp8_matches_oracle(pa, name, B, bs, heads, split):
     out = torch.empty_like(w.q)
     if split:
         msl = int(w.seq_lens.max())
-        ws = splitk_workspace(pa, w, msl, 256)
+        ws = _ws(pa, w, msl, 256)
         pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
                                 w.block_size, 0.45, 0.6, msl, ws, 256)
     else:
@@ -86,7 +92,7 @@ def test_fp8_step_write_then_decode(pa):
     ks, vs = w.meta["k_scale"], w.meta["v_scale"]
     pa.pa_reshape_and_cache_fp8(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size, ks, vs)
     msl = int(w.seq_lens.max())
-    ws = splitk_workspace(pa, w, msl, 512)
+    ws = _ws(pa, w, msl, 512)
     out = torch.empty_like(w.q)
     pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
                             w.block_size, ks, vs, msl, ws, 512)
@@ -101,7 +107,7 @@ def test_fp8_step_write_then_decode(pa):
 def test_fp8_full_size_sampled(pa):
     w = wl.make_fp8("mha7b", device="cuda", poison=True, seed=62)
     msl = int(w.seq_lens.max())
-    ws = splitk_workspace(pa, w, msl, 512)
+    ws = _ws(pa, w, msl, 512)
     out = torch.empty_like(w.q)
     pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
                             w.block_size, w.meta["k_scale"], w.meta["v_scale"], msl, ws, 512)
@@ -122,3 +128,30 @@ def test_fp8_bad_block_id_and_empty_sequence(pa):
     assert pa.pa_device_errors(clear=True) & pa.DEVERR_BLOCK_ID
     assert torch.count_nonzero(out[4]) == 0
     assert torch.isfinite(out.float()).all()
+
+
+def test_fp8_split_cuda_core_family(pa):
+    """The CUDA-core split-K path (forced) stays checked too."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import torch, workload as wl\n"
+        "import paged_kv_cache_136_gb300 as pa\n"
+        "from tests._parity import check_attention\n"
+        "from tests.test_gpu_fp8 import _oracle_decode_fp8, _ws\n"
+        "for name, kw in [('gqa8b', dict(num_seqs=12)), ('mha7b', dict(num_seqs=6))]:\n"
+        "    w = wl.make_fp8(name, device='cuda', poison=True, seed=65, **kw)\n"
+        "    msl = int(w.seq_lens.max()); ws = _ws(pa, w, msl, 128)\n"
+        "    out = torch.empty_like(w.q)\n"
+        "    pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens,\n"
+        "                            w.scale, w.block_size, 0.5, 0.5, msl, ws, 128)\n"
+        "    torch.cuda.synchronize()\n"
+        "    check_attention(out, _oracle_decode_fp8(w), what='simt fp8 ' + name)\n"
+        "assert pa.pa_device_errors(clear=True) == 0\n"
+        "print('ok')\n")
+    env = dict(os.environ, PA_DECODE_KERNEL="simt")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-3000:]
