@@ -1016,7 +1016,9 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
                                                    round_up(3 * (size_t)rows * head_size, 256));
         const int hg = tc::heads_per_cta(group, num_kv_heads);
         const int ngroups = num_kv_heads / hg;
-        const int box_rows = block_size < 128 / hg ? block_size : 128 / hg;
+        // A stage of the FP8 kernel holds 256 (token, head) rows: 256/hg tokens.
+        const int stage_tokens = 2 * 128 / hg;
+        const int box_rows = block_size < stage_tokens ? block_size : stage_tokens;
         alignas(64) CUtensorMap pmap, qmap;
         if (!make_pool_map_fp8(&pmap, kv_cache, num_blocks, block_size, num_kv_heads, head_size,
                                box_rows, hg) ||

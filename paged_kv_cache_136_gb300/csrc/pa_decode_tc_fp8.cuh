@@ -18,9 +18,13 @@
 //
 // Everything else -- roles, the (token, kv head) row order of a stage, head
 // groups per CTA, lagged O accumulation, the persistent split-K schedule --
-// is the 16-bit tensor-core kernel's (pa_decode_tc.cuh).  A stage holds 128
-// rows of 128 codes per plane, half the bytes of the 16-bit stage, so the
-// ring has five stages.
+// is the 16-bit tensor-core kernel's (pa_decode_tc.cuh), with one change: a
+// stage holds 256 (token, kv head) rows -- two 128-row blocks, each with its
+// own score columns, and each softmax thread takes one row of each -- so a
+// stage moves the same 64 KB as the 16-bit kernel's and the per-stage
+// hand-offs are paid once per 64 KB.  The values MMA contracts over all 256
+// rows (K = 256); its P operand has one buffer, reused once the previous
+// stage's values MMA has completed.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,24 +46,27 @@ constexpr int kBarEpi = tc::kBarEpi;
 constexpr int kRows = tc::kRows;
 constexpr int kD = tc::kD;
 
-constexpr int kStages = 5;
-constexpr int kRegion = kRows * 128;       // 128 rows x 128 codes
-constexpr int kPlane = kRegion;            // K (or V) of a stage
+constexpr int kStages = 3;
+constexpr int kStageRows = 2 * kRows;      // (token, kv head) rows per stage
+constexpr int kRegion = kRows * 128;       // a block of 128 rows x 128 codes
+constexpr int kPlane = 2 * kRegion;        // K (or V) of a stage: two row blocks
 constexpr int kStageBytes = 2 * kPlane;
 constexpr int kParts = 3;                  // e4m3 parts of q' and of 256 p
 constexpr int kPartRows = 16;              // (head, query) columns per part
 constexpr int kNQ = kParts * kPartRows;    // score columns
 constexpr int kNP = kParts * kPartRows;    // value columns
 constexpr int kQBytes = kNQ * 128;
-constexpr int kPBytes = kNP * 128;
-constexpr uint32_t kTmemCols = 256;        // S: 2 x 48, O: 2 x 48
+constexpr int kPBytes = 2 * kNP * 128;     // K = 256 stage rows: two 128-byte regions
+constexpr int kSCols = 2 * kNQ;            // S of one stage: two row blocks
+constexpr int kOCol = 2 * kSCols;          // O after the two S buffers
+constexpr uint32_t kTmemCols = 512;        // S: 2 x 2 x 48, O: 2 x 48
 constexpr float kPScale = 256.f;
 constexpr float kInvPScale = 1.f / 256.f;
 constexpr float kQRange = 256.f;           // |q'| <= 256
 
 constexpr int kOffQ = kStages * kStageBytes;
 constexpr int kOffP = kOffQ + kStages * kQBytes;
-constexpr int kOffMisc = kOffP + 2 * kPBytes;
+constexpr int kOffMisc = kOffP + kPBytes; // one P buffer
 
 struct Misc {
     StageDesc desc[kStages];
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const float *__restrict__ q_scales, int q_rows, float v_scale)
 {
     constexpr int NV = HG * G;                 // valid (head, query) columns
-    constexpr int TPS = kRows / HG;            // tokens per stage
+    constexpr int TPS = kStageRows / HG;       // tokens per stage
     constexpr int R = BS < TPS ? BS : TPS;     // token rows per TMA box
     constexpr int CH = TPS / R;                // row chunks per stage
     constexpr int BOX_BYTES = R * HG * 128;
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // P entries of other heads' columns stay zero for the whole kernel: a
     // row (token, head h) only ever writes the columns of head h.
-    for (int i = tid; i < 2 * kPBytes / 16; i += kThreads)
+    for (int i = tid; i < kPBytes / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
@@ -423,24 +430,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t kvbase = smem_addr(smem + slot * kStageBytes);
                 if (qk) {
                     const uint32_t qbase = smem_addr(smem + kOffQ + slot * kQBytes);
-                    const uint32_t d_tmem = tmem + (uint32_t)(b * kNQ);
-                    // K = 32 codes per instruction: four steps over the row.
+                    // Each 128-row block of the stage gets its own 48
+                    // columns; K = 32 codes per instruction, four steps.
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_f8(d_tmem, smem_desc_sw128(kvbase + kk * 32, 16, 1024),
-                                smem_desc_sw128(qbase + kk * 32, 16, 1024), kIdescQK,
-                                kk > 0 ? 1u : 0u);
+                    for (int ub = 0; ub < 2; ++ub) {
+                        const uint32_t d_tmem = tmem + (uint32_t)(b * kSCols + ub * kNQ);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f8(d_tmem, smem_desc_sw128(kvbase + ub * kRegion + kk * 32, 16, 1024),
+                                    smem_desc_sw128(qbase + kk * 32, 16, 1024), kIdescQK,
+                                    kk > 0 ? 1u : 0u);
+                    }
                     umma_commit(&m->s_full[b]);
                 } else {
                     const uint32_t vbase = kvbase + kPlane;
-                    const uint32_t pbase = smem_addr(smem + kOffP + b * kPBytes);
-                    const uint32_t d_tmem = tmem + (uint32_t)(2 * kNQ + b * kNP);
-                    // V^T as the MN-major A operand: 32 rows (4 KB) per step.
+                    const uint32_t pbase = smem_addr(smem + kOffP);
+                    const uint32_t d_tmem = tmem + (uint32_t)(kOCol + b * kNP);
+                    // V^T as the MN-major A operand, 32 stage rows (4 KB) per
+                    // step over all 256 rows; P's K runs over two regions.
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < 8; ++kk)
                         umma_f8(d_tmem, smem_desc_sw128(vbase + kk * 4096, kRegion, 1024),
-                                smem_desc_sw128(pbase + kk * 32, 16, 1024), kIdescPV,
-                                kk > 0 ? 1u : 0u);
+                                smem_desc_sw128(pbase + (kk >> 2) * (kNP * 128) + (kk & 3) * 32,
+                                                16, 1024),
+                                kIdescPV, kk > 0 ? 1u : 0u);
                     umma_commit(&m->o_full[b]);
                     umma_commit(&m->empty[slot]);
                 }
@@ -475,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after_sync();
             float o1[16], o2[16], o3[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(2 * kNQ + b * kNP), o1);
-            tmem_ld16(tmem + lane_base + (uint32_t)(2 * kNQ + b * kNP + kPartRows), o2);
-            tmem_ld16(tmem + lane_base + (uint32_t)(2 * kNQ + b * kNP + 2 * kPartRows), o3);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kOCol + b * kNP), o1);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kOCol + b * kNP + kPartRows), o2);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kOCol + b * kNP + 2 * kPartRows), o3);
 #pragma unroll
             for (int n = 0; n < NV; ++n)
                 o_acc[n] = fmaf(o_acc[n], alpha[n], (o1[n] + o2[n] + o3[n]) * kInvPScale);
@@ -518,25 +531,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&m->s_full[b], u & 1);
             __syncwarp();
             tc_fence_after_sync();
-            float sv[16], sv2[16], sv3[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(b * kNQ), sv);
-            tmem_ld16(tmem + lane_base + (uint32_t)(b * kNQ + kPartRows), sv2);
-            tmem_ld16(tmem + lane_base + (uint32_t)(b * kNQ + 2 * kPartRows), sv3);
+            // This thread's two stage rows: t (block 0) and 128 + t (block 1),
+            // both of head h.
+            float x[2][G];
+            bool valid[2];
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
-                sv[n] = (sv[n] + sv2[n] + sv3[n]) * (n < NV ? qsn[n] : 0.f);
-            const bool valid = (t / HG) < d.nvalid;
-            float x[G];
+            for (int ub = 0; ub < 2; ++ub) {
+                float sv[16], sv2[16], sv3[16];
+                const uint32_t sc = tmem + lane_base + (uint32_t)(b * kSCols + ub * kNQ);
+                tmem_ld16(sc, sv);
+                tmem_ld16(sc + kPartRows, sv2);
+                tmem_ld16(sc + 2 * kPartRows, sv3);
+                valid[ub] = ((ub * kRows + t) / HG) < d.nvalid;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float v = (sv[g] + sv2[g] + sv3[g]) * qsn[g];
+#pragma unroll
+                    for (int hh = 1; hh < HG; ++hh)
+                        if (h == hh)
+                            v = (sv[hh * G + g] + sv2[hh * G + g] + sv3[hh * G + g]) *
+                                qsn[hh * G + g];
+                    x[ub][g] = valid[ub] ? v : -INFINITY;
+                }
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float v = sv[g];
-#pragma unroll
-                for (int hh = 1; hh < HG; ++hh)
-                    if (h == hh)
-                        v = sv[hh * G + g];
-                x[g] = valid ? v : -INFINITY;
                 // max over this warp's tokens of the same head
-                float mx = x[g];
+                float mx = fmaxf(x[0][g], x[1][g]);
 #pragma unroll
                 for (int off = HG; off < 32; off <<= 1)
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -558,8 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run[n] = m_new;
             }
             // P as the K-major B operand of the values MMA: column (k index)
-            // = this row t; row h*G+g holds the high part, 16+h*G+g the low.
-            uint8_t *pb = smem + kOffP + b * kPBytes;
+            // = the stage row; row pp*16 + h*G + g holds part pp.  One buffer:
+            // the previous stage's values MMA must have read it.
+            if (k > 0 && !mbar_wait(&m->o_full[(k - 1) & 1], ((k - 1) >> 1) & 1) && t == 0)
+                atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+            uint8_t *pb = smem + kOffP;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float mg = m_run[g], ag = alpha[g];
@@ -569,24 +593,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mg = m_run[hh * G + g];
                         ag = alpha[hh * G + g];
                     }
-                const float pr = ex2(x[g] - mg);
-                l_part[g] = fmaf(l_part[g], ag, pr);
+                const float pr0 = ex2(x[0][g] - mg);
+                const float pr1 = ex2(x[1][g] - mg);
+                l_part[g] = fmaf(l_part[g], ag, pr0 + pr1);
                 // 256 p as three e4m3 parts (about 12 significant bits).
-                uint8_t c3[3];
-                split3_e4m3(pr * kPScale, c3);
                 const int n = h * G + g;
 #pragma unroll
-                for (int pp = 0; pp < kParts; ++pp)
-                    pb[sw128_offset_b8(pp * kPartRows + n, t)] = c3[pp];
-            }
-            if (!valid) {
-                // V rows past the end may hold anything (stale tiles, NaN
-                // padding); P is 0 there, but 0 * NaN would still poison O.
-                uint8_t *vrow = smem + slot * kStageBytes + kPlane + t * 128;
+                for (int ub = 0; ub < 2; ++ub) {
+                    uint8_t c3[3];
+                    split3_e4m3((ub ? pr1 : pr0) * kPScale, c3);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+                    for (int pp = 0; pp < kParts; ++pp)
+                        pb[ub * (kNP * 128) + sw128_offset_b8(pp * kPartRows + n, t)] = c3[pp];
+                }
             }
+#pragma unroll
+            for (int ub = 0; ub < 2; ++ub)
+                if (!valid[ub]) {
+                    // V rows past the end may hold anything (stale tiles, NaN
+                    // padding); P is 0 there, but 0 * NaN would still poison O.
+                    uint8_t *vrow = smem + slot * kStageBytes + kPlane + (ub * kRows + t) * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+                }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
