@@ -259,12 +259,19 @@ def cpu_baseline(w, budget_s: float = 10.0) -> dict:
     n = int(min(len(groups_all), max(len(pilot), budget_s / per_group)))
     n = max(w.num_kv_heads, n // w.num_kv_heads * w.num_kv_heads)   # whole sequences
     sample = groups_all[:n]
-    dt, covered = oracle_sample_run(w, sample, nthreads)
+    # Repeat the sample until the budget is spent (the whole workload can take
+    # far less than the budget on many cores).
+    dt, covered, passes = 0.0, 0, 0
+    while passes == 0 or dt < budget_s:
+        t, c = oracle_sample_run(w, sample, nthreads)
+        dt += t
+        covered += c
+        passes += 1
     seqs = n // w.num_kv_heads
     return {"value": covered / dt / 1e9, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"decode of sequences 0-{seqs - 1} of {w.num_seqs} (all heads), "
-                      f"fp64 two-pass oracle, {dt:.2f} s",
-            "seconds": dt, "seqs_per_s": seqs / dt}
+                      f"{passes} pass(es), fp64 two-pass oracle, {dt:.2f} s",
+            "seconds": dt, "seqs_per_s": passes * seqs / dt}
 
 
 # ---------------------------------------------------------------------------
