@@ -234,18 +234,21 @@ cudaError_t launch_decode(const DecodeKey &key, const CUtensorMap &tmap, const D
 cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int num_seqs,
                           cudaStream_t stream)
 {
+    // Launched as the dependent of the partition kernel: its launch overlaps
+    // that kernel's tail, and it waits for the partial states on the device.
     dim3 grid(p.num_heads, num_seqs);
     if (dtype == PA_FP16 && head_size == 64)
-        splitk_reduce_kernel<__half, 64><<<grid, 64, 0, stream>>>(p);
-    else if (dtype == PA_FP16 && head_size == 128)
-        splitk_reduce_kernel<__half, 128><<<grid, 128, 0, stream>>>(p);
-    else if (dtype == PA_BF16 && head_size == 64)
-        splitk_reduce_kernel<__nv_bfloat16, 64><<<grid, 64, 0, stream>>>(p);
-    else if (dtype == PA_BF16 && head_size == 128)
-        splitk_reduce_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(p);
-    else
-        return cudaErrorNotSupported;
-    return cudaGetLastError();
+        return launch_after_previous(splitk_reduce_kernel<__half, 64>, grid, dim3(64), 0, stream, p);
+    if (dtype == PA_FP16 && head_size == 128)
+        return launch_after_previous(splitk_reduce_kernel<__half, 128>, grid, dim3(128), 0, stream,
+                                     p);
+    if (dtype == PA_BF16 && head_size == 64)
+        return launch_after_previous(splitk_reduce_kernel<__nv_bfloat16, 64>, grid, dim3(64), 0,
+                                     stream, p);
+    if (dtype == PA_BF16 && head_size == 128)
+        return launch_after_previous(splitk_reduce_kernel<__nv_bfloat16, 128>, grid, dim3(128), 0,
+                                     stream, p);
+    return cudaErrorNotSupported;
 }
 
 // ---------------------------------------------------------------------------

@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
     __shared__ float w_s[kReduceChunk];
     __shared__ float red_s[D / 32];
     __shared__ float M_s;
+    griddep_wait(); // the partition kernel's states are complete
     const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);

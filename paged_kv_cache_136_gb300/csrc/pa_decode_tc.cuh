@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = m->tmem_base;
+    // Everything above overlaps the previous kernel (the plan) when launched
+    // as its dependent; from here on its results are read.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == kProducerWarp) {
         // ================================================================ producer
@@ -675,6 +679,7 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t bucket[kPlanBuckets];
     __shared__ uint32_t carry_s;
+    griddep_launch_dependents(); // the decode grid may start its prologue
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     for (int i = tid; i < kPlanBuckets; i += blockDim.x)
@@ -783,6 +788,9 @@ cudaError_t launch_tc_one(const CUtensorMap &pool, const CUtensorMap &qmap, cons
             return e;
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
     }
+    // The split kernel follows the plan kernel as its dependent.
+    if (SPLIT)
+        return launch_after_previous(kern, grid, dim3(kThreads), kSmemBytes, stream, pool, qmap, p);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(pool, qmap, p);
     return cudaGetLastError();
 }

@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = m->tmem_base;
+    // Everything above overlaps the previous kernel (the plan) when launched
+    // as its dependent; from here on its results are read.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == kProducerWarp) {
         // ================================================================ producer
@@ -705,8 +709,9 @@ cudaError_t launch_one(const CUtensorMap &pool, const CUtensorMap &qmap, const T
             return e;
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(pool, qmap, p, q_scales, q_rows, v_scale);
-    return cudaGetLastError();
+    // Follows the plan kernel as its dependent.
+    return launch_after_previous(kern, grid, dim3(kThreads), kSmemBytes, stream, pool, qmap, p,
+                                 q_scales, q_rows, v_scale);
 }
 
 // Split-K only (the query prepass needs the caller's workspace).

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 // Bits of the sticky device error word (the same values as PA_DEVERR_* in
 // pa.h, which the kernels' translation units do not include).
 #define PA_DEVERR_BLOCK_ID_ 0x1u
@@ -14,6 +16,26 @@
 #define PA_DEVERR_TIMEOUT_ 0x8u
 
 namespace pa {
+
+// Launch `kern` so that it may start while the previous kernel on the stream
+// is finishing (programmatic dependent launch); the kernel calls
+// griddep_wait() before it reads anything that kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_previous(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                         size_t smem, cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Kernel parameters of the decode kernels (one-pass and split-K partition).
 struct DecodeParams {

@@ -156,6 +156,19 @@ __device__ __forceinline__ bool bar_sync_or(int id, int nthreads, bool pred)
     return r != 0;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (returns at once for a normal
+// launch); let the dependent grid start launching.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2^x (the PTX ex2.approx instruction).
 __device__ __forceinline__ float ex2(float x)
 {
