@@ -166,7 +166,7 @@ struct PrefillParams {
     long long part_stride, lse_part_stride;
 };
 
-// Prefill over the paged cache on grid (ceil(max_query_len/256), H, R).
+// Prefill over the paged cache on grid (ceil(max_query_len/128) x key_split, H, R).
 cudaError_t launch_prefill_f16(int head_size, int block_size, const CUtensorMap &pool,
                                const CUtensorMap &qmap, const PrefillParams &p, dim3 grid,
                                cudaStream_t stream);
