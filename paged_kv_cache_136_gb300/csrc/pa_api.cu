@@ -872,8 +872,8 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
     p.chunk_tiles = key_split > 1 ? chunk_tiles : 1;
     p.part_stride = part_stride;
     p.lse_part_stride = lse_part_stride;
-    // One CTA per 128 query rows (and key chunk), per head, per request.
-    const dim3 grid((unsigned)((max_query_len + 127) / 128 * key_split), (unsigned)num_heads,
+    // One CTA per 256 query rows (and key chunk), per head, per request.
+    const dim3 grid((unsigned)((max_query_len + 255) / 256 * key_split), (unsigned)num_heads,
                     (unsigned)num_reqs);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = dtype == PA_BF16 ? launch_prefill_bf16(head_size, block_size, pmap, qmap, p, grid, st)
@@ -1235,7 +1235,7 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     if (!sms)
         return PA_ERR_CUDA;
     const int prefix_tiles = (P + 127) / 128;
-    const int ctas_per_chunk = ((num_seqs + 127) / 128) * num_heads;
+    const int ctas_per_chunk = ((num_seqs + 255) / 256) * num_heads;
     int nsplit = (2 * sms + ctas_per_chunk - 1) / ctas_per_chunk;
     nsplit = nsplit < 1 ? 1 : (nsplit > c.max_parts - 1 ? c.max_parts - 1 : nsplit);
     const int chunk_tiles = (prefix_tiles + nsplit - 1) / nsplit;

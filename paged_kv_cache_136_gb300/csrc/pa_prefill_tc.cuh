@@ -8,37 +8,35 @@
 // without the causal mask).  Query row i of request r sits at position
 // seq_len - q_len + i and attends keys 0..position (causal) or every key.
 //
-// A CTA owns a tile of 128 query rows of one (request, query head).  Roles in
-// a CTA of 352 threads:
+// A CTA owns 256 query rows of one (request, query head): two tiles of 128
+// rows that share every K/V tile, each with its own softmax warpgroup and its
+// own MMA issuer warp, so the tensor cores work on one tile's chain of
+// dependent MMAs while the other tile's softmax runs.  Roles in a CTA of 352
+// threads:
 //
-//   warp 8 (producer)  TMA-loads the query tile once, then K and V tiles of
-//                      128 keys into a ring of shared-memory slots, one box
-//                      {64 elements, 1 kv head, block_size rows} per lane and
-//                      block ("Paged attention", k4i.top, section "block
+//   warp 8 (producer)  TMA-loads the two query tiles once, then K and V tiles
+//                      of 128 keys into a ring of shared-memory slots, one
+//                      box {64 elements, 1 kv head, block_size rows} per lane
+//                      and block ("Paged attention", k4i.top, section "block
 //                      table": physical_block = block_table[t // block_size]).
-//   warp 9 (scores)    owns the TMEM columns and issues S_k = Q K_k^T (M=128,
-//                      N=128 keys, K=head_size) into one of three S buffers,
-//                      so the scores of the next key tiles are computed while
-//                      tile k's softmax and values run.
-//   warp 10 (values)   issues O (+)= P_k V_k (M=128, N=head_size, K=128 keys)
-//                      with P read from tensor memory (A operand) and V as an
-//                      MN-major shared-memory operand.  Scores and values are
-//                      separate accumulator chains on separate issuers, which
-//                      the tensor cores overlap.
-//   warps 0-3 / 4-7    softmax, keys 0-63 / 64-127 of every tile: each thread
-//                      takes one query row (TMEM lane) and half of the tile's
-//                      keys, exchanges the half-row maximum with the thread of
-//                      the other warpgroup that owns the same row, computes the
-//                      base-2 exponentials and writes its half of P over its
-//                      own half of S as 16-bit values (bf16: a high part and
-//                      the rounded remainder, so P keeps ~16 significant
-//                      bits); at the end each writes half of out = O / l.
+//   warps 9, 10 (MMA)  one per query tile t (warp 9 owns the 512 TMEM
+//                      columns); per key tile k they issue
+//                        S_t = Q_t K_k^T          (M=128, N=128, K=head_size)
+//                        O_t (+)= P_t V_k         (M=128, N=head_size, K=128)
+//                      with P_t read from tensor memory (A operand) and V_k as
+//                      an MN-major shared-memory operand.
+//   warps 0-3 / 4-7    one query row per thread (TMEM lane): scale and mask
+//   (softmax, tile 0/1) the row's 128 scores, row max, base-2 exponentials,
+//                      write P over S as 16-bit values (bf16: a high part in
+//                      columns 0-63 and the rounded remainder in 64-127, so P
+//                      keeps ~16 significant bits), and at the end
+//                      out = O / l (and the log-sum-exp when asked).
 //
 // The running maximum is updated lazily: O and l are rescaled only when a key
 // tile raises a row's maximum by more than 2^8, so most tiles skip the rescale
-// and P stays below 2^8.  Key rows past seq_len in the last tile are zeroed in
-// shared memory before the values MMA reads them, so stale or NaN bytes never
-// reach O.
+// and P stays below 2^8 (exact in fp16/bf16 range).  Every key row past
+// seq_len that a tile could hold is zeroed in shared memory before the values
+// MMA reads it, so stale or NaN bytes never reach O.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,36 +51,30 @@ namespace pa {
 namespace pf {
 
 constexpr int kThreads = 352;
-constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
-constexpr int kQkWarp = 9;
-constexpr int kPvWarp = 10;
-constexpr int kTileM = 128;         // query rows per CTA
+constexpr int kMmaWarp = 9;               // warps 9 and 10: MMA issuers of query tiles 0 and 1
+constexpr int kTileM = 128;         // query rows per tile
 constexpr int kTileN = 128;         // keys per K/V tile
-constexpr int kHalfN = kTileN / 2;  // keys per softmax warpgroup
+constexpr int kRowsPerCta = 2 * kTileM;
 constexpr float kRescaleLog2 = 8.f; // lazy-rescale threshold, log2 units
-constexpr int kSBufs = 3;           // S buffers: scores run two tiles ahead
-constexpr uint32_t kTmemCols = 512; // S0, S1, S2 (128 each), O (head_size)
-constexpr uint32_t kOCol = kSBufs * 128;
+constexpr uint32_t kTmemCols = 512; // S0, S1, O0, O1: 128 columns each
 constexpr int kRegion = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 
 template <int D>
 struct Geo {
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = kHalves * kRegion; // a Q, K or V tile
-    static constexpr int kSlots = D == 128 ? 5 : 8;      // K/V ring
-    static constexpr int kOffKV = kTileBytes;            // after the Q tile
+    static constexpr int kSlots = D == 128 ? 4 : 8;      // K/V ring
+    static constexpr int kOffKV = 2 * kTileBytes;        // after the two Q tiles
     static constexpr int kOffMisc = kOffKV + kSlots * kTileBytes;
 };
 
 struct Misc {
     uint64_t q_full;
     uint64_t kv_full[8], kv_empty[8];
-    uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
-    uint64_t o_done, drain[2];
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t drain[2];
     uint32_t tmem_base;
-    float half_max[2][2][kTileM]; // [tile parity][key half][row]
-    float half_l[2][kTileM];      // [key half][row]
 };
 
 template <int D>
@@ -128,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(32 % BPT == 0 && BPT * NH <= 32, "key tile geometry");
     constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
     // bf16 keeps only 8 significant bits: P then travels as a high part plus
-    // the rounded remainder (two MMAs on the same V); fp16's 11 bits suffice.
+    // the rounded remainder (two MMAs on the same V), fp16's 11 bits suffice.
     constexpr bool kSplitP = kFmt == 1u;
     constexpr uint32_t kIdescS = idesc_f16_f32(kFmt, 0, 0, kTileM, kTileN);
     constexpr uint32_t kIdescO = idesc_f16_f32(kFmt, 0, 1, kTileM, D);
@@ -141,13 +133,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+127
+    // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+255
     const int r = blockIdx.z;
     const int h = blockIdx.y;
     const int nsplit = p.key_split;
     const int csplit = (int)blockIdx.x % nsplit;
     const int qb = (int)gridDim.x / nsplit - 1 - (int)blockIdx.x / nsplit; // heaviest rows first
-    const int i0 = qb * kTileM;
+    const int i0 = qb * kRowsPerCta;
     const int q0 = __ldg(p.query_start_loc + r);
     const int q1 = __ldg(p.query_start_loc + r + 1);
     const int L = __ldg(p.seq_lens + r);
@@ -166,39 +158,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles) * kTileN) : L;
     T *const out_base = reinterpret_cast<T *>(p.out) + (size_t)csplit * (size_t)p.part_stride;
     float *const lse_base = p.lse ? p.lse + (size_t)csplit * (size_t)p.lse_part_stride : nullptr;
-    const int nv = min(q_len - i0, kTileM);
-    const int ext = p.causal ? min(L, ctx + i0 + nv) : key_hi; // keys the last row reaches
-    const int n = max(0, (ext - kt0 * kTileN + kTileN - 1) / kTileN); // key tiles
+    int nv[2], nt[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        nv[t] = min(max(q_len - (i0 + t * kTileM), 0), kTileM);
+        const int ext = p.causal ? min(L, ctx + i0 + t * kTileM + nv[t]) : key_hi;
+        nt[t] = nv[t] > 0 ? max(0, (ext - kt0 * kTileN + kTileN - 1) / kTileN) : 0;
+    }
+    const int n = max(nt[0], nt[1]); // key tiles loaded
     if (n == 0) {
         // An empty key chunk: zero rows and -inf log-sum-exps (an empty part).
-        for (int i = tid; i < nv * D; i += kThreads) {
+        for (int i = tid; i < (nv[0] + nv[1]) * D; i += kThreads) {
             const size_t tok = (size_t)(q0 + i0 + i / D);
             out_base[(tok * p.num_heads + h) * D + i % D] = T(0.f);
         }
         if (lse_base)
-            for (int i = tid; i < nv; i += kThreads)
+            for (int i = tid; i < nv[0] + nv[1]; i += kThreads)
                 lse_base[(size_t)(q0 + i0 + i) * p.num_heads + h] = -INFINITY;
         return;
     }
     const bool tail = (kt0 + n) * kTileN > L; // the last key tile reaches past seq_len
+    const int fixer = nt[1] == n ? 1 : 0;
 
     if (tid == 0) {
         mbar_init(&m->q_full, 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&m->kv_full[i], 1);
-            mbar_init(&m->kv_empty[i], 1);
+            mbar_init(&m->kv_empty[i], 2); // one arrival per MMA issuer warp
         }
-        for (int i = 0; i < kSBufs; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&m->s_full[i], 1);
-            mbar_init(&m->p_full[i], kSoftmaxThreads / 32);
-            mbar_init(&m->pv_done[i], 1);
+            mbar_init(&m->p_full[i], 4);
+            mbar_init(&m->o_done[i], 1);
         }
         mbar_init(&m->drain[0], 1);
         mbar_init(&m->drain[1], 1);
-        mbar_init(&m->o_done, 1);
         fence_barrier_init();
     }
-    if (warp == kQkWarp) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&m->tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -213,10 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&pool_map);
             prefetch_tensormap(&q_map);
-            mbar_arrive_expect_tx(&m->q_full, (uint32_t)TB);
+            mbar_arrive_expect_tx(&m->q_full, (uint32_t)((nv[1] > 0 ? 2 : 1) * TB));
 #pragma unroll
-            for (int hf = 0; hf < NH; ++hf)
-                tma_load_3d(smem + hf * kRegion, &q_map, &m->q_full, hf * 64, h, q0 + i0);
+            for (int t = 0; t < 2; ++t)
+                if (nv[t] > 0)
+#pragma unroll
+                    for (int hf = 0; hf < NH; ++hf)
+                        tma_load_3d(smem + t * TB + hf * kRegion, &q_map, &m->q_full, hf * 64, h,
+                                    q0 + i0 + t * kTileM);
         }
         // Block-table entries of 64 blocks live in lane registers (this
         // window and the next), refreshed every 32 blocks.
@@ -256,242 +257,256 @@ __global__ void __launch_bounds__(kThreads, 1)
                             &pool_map, &m->kv_full[slot], hf * 64, kvh, row, plane);
             }
         }
-    } else if (warp == kQkWarp) {
-        // ===================================================== scores issuer
-        const uint32_t qa = smem_addr(smem);
-        bool ok = warp_wait(&m->q_full, 0, lane);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ================================= MMA issuer of query tile t
+        // The two tiles' chains of dependent MMAs are issued by separate
+        // warps, so the tensor cores overlap them.  Every K/V slot use gets
+        // one arrival from each warp: a commit after its MMAs read the slot,
+        // or a plain arrive when its tile does not need that key tile.
+        const int t = warp - kMmaWarp;
+        const int ntt = nt[t];
+        auto issue_qk = [&](int slot) {
+            const uint32_t qa = smem_addr(smem + t * TB);
+            const uint32_t ka = smem_addr(smem + Gm::kOffKV + slot * TB);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
+                umma_f16(tmem + (uint32_t)(t * 128), smem_desc_sw128(qa + off, 16, 1024),
+                         smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&m->s_full[t]);
+        };
+        auto issue_pv = [&](int slot, bool acc) {
+            const uint32_t va = smem_addr(smem + Gm::kOffKV + slot * TB);
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk) {
+                const uint64_t vd = smem_desc_sw128(va + kk * 2048, kRegion, 1024);
+                umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128), tmem + (uint32_t)(t * 128 + kk * 8),
+                                vd, kIdescO, (acc || kk > 0) ? 1u : 0u);
+                if (kSplitP) // the low parts of P, 64 columns further on
+                    umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128),
+                                    tmem + (uint32_t)(t * 128 + 64 + kk * 8), vd, kIdescO, 1u);
+            }
+        };
+        // release a slot: commit after this warp's MMAs, or arrive at once
+        auto release = [&](int slot, bool used) {
+            if (used)
+                umma_commit(&m->kv_empty[slot]);
+            else
+                mbar_arrive(&m->kv_empty[slot]);
+        };
+        bool ok = warp_wait(&m->q_full, 0, lane) && warp_wait(&m->kv_full[0], 0, lane);
+        if (ok) {
+            tc_fence_after_sync();
+            if (lane == 0) {
+                if (ntt > 0)
+                    issue_qk(0);
+                release(0, ntt > 0);
+            }
+            __syncwarp();
+        }
+        // Each slot use is released only after its load has landed, so a warp
+        // whose tile needs no more keys still follows the producer one use
+        // at a time (two releases can never fall into one barrier phase).
         for (int k = 0; ok && k < n; ++k) {
-            const int b = k % kSBufs, gk = 2 * k, sk = gk % S;
-            ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
-            // S[b] holds P_{k-3} until the values MMA of tile k-3 is done.
-            if (ok && k >= kSBufs)
-                ok = warp_wait(&m->pv_done[b], ((k / kSBufs) - 1) & 1, lane);
+            const int gv = 2 * k + 1, sv = gv % S;
+            const int gk = 2 * k + 2, sk = gk % S;
+            const bool use = k < ntt, next = k + 1 < n, nuse = k + 1 < ntt;
+            ok = warp_wait(&m->kv_full[sv], (gv / S) & 1, lane);
+            if (ok && use) {
+                // The last tile's rows past seq_len are zeroed by one softmax
+                // warpgroup before it hands over its P.
+                if (tail && k == n - 1)
+                    ok = warp_wait(&m->p_full[fixer], k & 1, lane);
+                if (ok)
+                    ok = warp_wait(&m->p_full[t], k & 1, lane);
+                if (ok) {
+                    tc_fence_after_sync();
+                    if (lane == 0)
+                        issue_pv(sv, k > 0);
+                }
+            }
+            if (ok && next)
+                ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
             if (!ok)
                 break;
             tc_fence_after_sync();
             if (lane == 0) {
-                const uint32_t ka = smem_addr(smem + Gm::kOffKV + sk * TB);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
-                    umma_f16(tmem + (uint32_t)(b * kTileN), smem_desc_sw128(qa + off, 16, 1024),
-                             smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&m->s_full[b]);
-                umma_commit(&m->kv_empty[sk]);
+                if (nuse)
+                    issue_qk(sk);
+                else if (use)
+                    umma_commit(&m->o_done[t]); // the tile's last values MMA
+                release(sv, use);
+                if (next)
+                    release(sk, nuse);
             }
             __syncwarp();
         }
         if (!ok && lane == 0)
             atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+        // Drain: every MMA this warp issued completes before TMEM is freed.
         if (lane == 0)
-            umma_commit(&m->drain[0]);
-        warp_wait(&m->drain[0], 0, lane);
-    } else if (warp == kPvWarp) {
-        // ===================================================== values issuer
-        bool ok = true;
-        for (int k = 0; ok && k < n; ++k) {
-            const int b = k % kSBufs, gv = 2 * k + 1, sv = gv % S;
-            ok = warp_wait(&m->kv_full[sv], (gv / S) & 1, lane) &&
-                 warp_wait(&m->p_full[b], (k / kSBufs) & 1, lane);
-            if (!ok)
-                break;
-            tc_fence_after_sync();
-            if (lane == 0) {
-                const uint32_t va = smem_addr(smem + Gm::kOffKV + sv * TB);
-#pragma unroll
-                for (int kk = 0; kk < kTileN / 16; ++kk) {
-                    // keys 16kk..16kk+15: half kk/4, packed columns 8(kk%4)..
-                    const uint32_t pa = tmem + (uint32_t)(b * kTileN + (kk >> 2) * kHalfN +
-                                                          (kk & 3) * 8);
-                    const uint64_t vd = smem_desc_sw128(va + kk * 2048, kRegion, 1024);
-                    umma_f16_tmem_a(tmem + kOCol, pa, vd, kIdescO, (k > 0 || kk > 0) ? 1u : 0u);
-                    if (kSplitP) // the low parts, 32 columns further on
-                        umma_f16_tmem_a(tmem + kOCol, pa + 32, vd, kIdescO, 1u);
-                }
-                umma_commit(&m->pv_done[b]);
-                umma_commit(&m->kv_empty[sv]);
-            }
-            __syncwarp();
-        }
-        if (lane == 0) {
-            if (ok)
-                umma_commit(&m->o_done);
-            else
-                atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-            umma_commit(&m->drain[1]);
-        }
-        warp_wait(&m->drain[1], 0, lane);
+            umma_commit(&m->drain[t]);
+        warp_wait(&m->drain[t], 0, lane);
     } else {
-        // ============================ softmax / epilogue: key half u, row `row`
-        const int u = warp >> 2;
+        // =========================================== softmax / epilogue (tiles 0, 1)
+        const int wg = warp >> 2;
         const int row = tid & 127;
-        const int pair_bar = 1 + (warp & 3); // warps w and w+4 share rows
         const uint32_t lane_base = (uint32_t)(((warp & 3) * 32) << 16);
-        const uint32_t o_addr = tmem + lane_base + kOCol + (uint32_t)(u * (D / 2));
-        const int pos = ctx + i0 + row;
-        const int lim = p.causal ? min(L, pos + 1) : key_hi;              // keys < lim
-        const int lim_lo = p.causal ? min(L, ctx + i0 + 1) : key_hi;      // lim of row 0
-        const float qs = p.qscale;
-        float m_used = -INFINITY, l = 0.f;
-        // A failed (timed-out) wait sets ok = false; the two warps of a row
-        // pair agree on it at the next pair barrier and leave together, so
-        // neither is left waiting at a named barrier.
-        bool ok = true;
-        for (int k = 0; k < n; ++k) {
-            const int b = k % kSBufs;
-            const int xb = k & 1; // half-max exchange buffer
-            if (ok)
-                ok = warp_wait(&m->s_full[b], (k / kSBufs) & 1, lane);
-            tc_fence_after_sync();
-            const uint32_t s_addr = tmem + lane_base + (uint32_t)(b * kTileN + u * kHalfN);
-            uint32_t sv[kHalfN];
-            tmem_ld32_nowait(s_addr, *reinterpret_cast<uint32_t(*)[32]>(sv));
-            tmem_ld32_nowait(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-            tmem_wait_ld();
-            // Half-row max over the raw scores (scale > 0 commutes with max)
-            // in 8 chains; masked keys become -inf.
-            float m8[8];
+        const uint32_t s_addr = tmem + lane_base + (uint32_t)(wg * 128);
+        const uint32_t o_addr = tmem + lane_base + (uint32_t)(256 + wg * 128);
+        const int ntt = nt[wg];
+        if (ntt > 0) {
+            const int pos = ctx + i0 + wg * kTileM + row;
+            const int lim = p.causal ? min(L, pos + 1) : key_hi;         // keys < lim
+            const int lim_lo = p.causal ? min(L, ctx + i0 + wg * kTileM + 1) : key_hi;
+            const float qs = p.qscale;
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int k = 0; k < ntt; ++k) {
+                ok = warp_wait(&m->s_full[wg], k & 1, lane);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                // The row's 128 raw scores (bits).
+                uint32_t sv[kTileN];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                m8[j] = -INFINITY;
-            const int key0 = (kt0 + k) * kTileN + u * kHalfN;
-            if ((kt0 + k + 1) * kTileN > lim_lo) {
-                const int kl = lim - key0; // keys of this half below the limit
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32_nowait(s_addr + (uint32_t)(c * 32),
+                                     *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+                tmem_wait_ld();
+                // Row max over the raw scores (scale > 0 commutes with max),
+                // in 8 independent chains; masked keys become -inf.
+                float m8[8];
 #pragma unroll
-                for (int i = 0; i < kHalfN; ++i) {
-                    const float x = i < kl ? __uint_as_float(sv[i]) : -INFINITY;
-                    sv[i] = __float_as_uint(x);
-                    m8[i & 7] = fmaxf(m8[i & 7], x);
+                for (int j = 0; j < 8; ++j)
+                    m8[j] = -INFINITY;
+                if ((kt0 + k + 1) * kTileN > lim_lo) {
+                    const int kl = lim - (kt0 + k) * kTileN; // keys of this tile below the limit
+#pragma unroll
+                    for (int i = 0; i < kTileN; ++i) {
+                        const float x = i < kl ? __uint_as_float(sv[i]) : -INFINITY;
+                        sv[i] = __float_as_uint(x);
+                        m8[i & 7] = fmaxf(m8[i & 7], x);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTileN; ++i)
+                        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
                 }
-            } else {
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qs;
+                float alpha = 1.f;
+                bool need = false;
+                if (k == 0) {
+                    m_used = mx;
+                } else if (mx > m_used + kRescaleLog2) {
+                    alpha = ex2(m_used - mx);
+                    m_used = mx;
+                    l *= alpha;
+                    need = true;
+                }
+                // p = 2^(S * scale*log2e - m): one FFMA and one ex2 per key;
+                // the row sum in 4 independent chains.
+                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < kHalfN; ++i)
-                    m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
-            }
-            m->half_max[xb][u][row] = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            if (bar_sync_or(pair_bar, 64, !ok)) {
-                ok = false;
-                break;
-            }
-            const float mx = fmaxf(m->half_max[xb][0][row], m->half_max[xb][1][row]) * qs;
-            float alpha = 1.f;
-            bool need = false;
-            if (k == 0) {
-                m_used = mx;
-            } else if (mx > m_used + kRescaleLog2) {
-                alpha = ex2(m_used - mx);
-                m_used = mx;
-                l *= alpha;
-                need = true;
-            }
-            // p = 2^(S * scale*log2e - m), written over this half of S.
-            const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16], lo[16];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[16], lo[16];
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j]), qs, nmu));
+                        const float p1 =
+                            ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j + 1]), qs, nmu));
+                        l4[j & 3] += p0 + p1;
+                        pk[j] = pack2<T>(p0, p1);
+                        if (kSplitP) {
+                            const float h0 = __uint_as_float(pk[j] << 16);
+                            const float h1 = __uint_as_float(pk[j] & 0xFFFF0000u);
+                            lo[j] = pack2<T>(p0 - h0, p1 - h1);
+                        }
+                    }
+                    tmem_st16(s_addr + (uint32_t)(c * 16), pk);
+                    if (kSplitP)
+                        tmem_st16(s_addr + (uint32_t)(64 + c * 16), lo);
+                }
+                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                if (__any_sync(0xffffffffu, need)) {
+                    // O holds the values of key tiles 0..k-1 (their MMAs are
+                    // complete: S_k was committed after them).  Done after P
+                    // is written so the scores' registers are free.
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j]), qs, nmu));
-                    const float p1 =
-                        ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j + 1]), qs, nmu));
-                    l4[j & 3] += p0 + p1;
-                    pk[j] = pack2<T>(p0, p1);
-                    if (kSplitP) {
-                        const float h0 = __uint_as_float(pk[j] << 16);
-                        const float h1 = __uint_as_float(pk[j] & 0xFFFF0000u);
-                        lo[j] = pack2<T>(p0 - h0, p1 - h1);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32_nowait(o_addr + (uint32_t)(c * 32), v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                        tmem_st32(o_addr + (uint32_t)(c * 32), v);
                     }
                 }
-                tmem_st16(s_addr + (uint32_t)(c * 16), pk);
-                if (kSplitP)
-                    tmem_st16(s_addr + (uint32_t)(32 + c * 16), lo);
-            }
-            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-            if (__any_sync(0xffffffffu, need)) {
-                // O holds the values of tiles 0..k-1 once the values MMA of
-                // tile k-1 is complete; tile k's cannot start before this
-                // warp hands over its P.
-                if (!warp_wait(&m->pv_done[(k - 1) % kSBufs], ((k - 1) / kSBufs) & 1, lane))
-                    ok = false;
-                tc_fence_after_sync();
+                tmem_wait_st();
+                if (tail && wg == fixer && k == n - 1) {
+                    // Zero the V rows of keys >= seq_len in the last tile.
+                    const int gv = 2 * k + 1;
+                    ok = warp_wait(&m->kv_full[gv % S], (gv / S) & 1, lane);
+                    if (ok && (kt0 + k) * kTileN + row >= L) {
+                        uint8_t *vrow = smem + Gm::kOffKV + (gv % S) * TB + row * 128;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
+                        for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4 *>(vrow + hf * kRegion + c * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&m->p_full[wg]);
+                if (!ok)
+                    break;
+            }
+            if (ok)
+                ok = warp_wait(&m->o_done[wg], 0, lane);
+            if (!ok) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+            } else {
+                tc_fence_after_sync();
+                const bool valid = row < nv[wg];
+                const size_t tok = (size_t)(q0 + i0 + wg * kTileM + row);
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                T *o = out_base + (tok * p.num_heads + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32_nowait(o_addr + (uint32_t)(c * 32), v);
                     tmem_wait_ld();
+                    uint32_t w[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-                    tmem_st32(o_addr + (uint32_t)(c * 32), v);
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = pack2<T>(__uint_as_float(v[2 * j]) * inv,
+                                        __uint_as_float(v[2 * j + 1]) * inv);
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    }
                 }
+                if (lse_base && valid)
+                    lse_base[tok * p.num_heads + h] =
+                        l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
-            tmem_wait_st();
-            if (tail && u == 0 && k == n - 1) {
-                // Zero the V rows of keys >= seq_len in the last tile (thread
-                // `row` takes key row `row`).
-                const int gv = 2 * k + 1;
-                if (!warp_wait(&m->kv_full[gv % S], (gv / S) & 1, lane))
-                    ok = false;
-                else if ((kt0 + k) * kTileN + row >= L) {
-                    uint8_t *vrow = smem + Gm::kOffKV + (gv % S) * TB + row * 128;
-#pragma unroll
-                    for (int hf = 0; hf < NH; ++hf)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(vrow + hf * kRegion + c * 16) =
-                                make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&m->p_full[b]);
-        }
-        if (ok)
-            ok = warp_wait(&m->o_done, 0, lane);
-        // Row sum over both halves (every thread of the pair reaches this).
-        m->half_l[u][row] = l;
-        bar_sync(pair_bar, 64);
-        const float l_row = m->half_l[0][row] + m->half_l[1][row];
-        if (!ok) {
-            if (lane == 0)
-                atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-        } else {
-            tc_fence_after_sync();
-            const bool valid = row < nv;
-            const size_t tok = (size_t)(q0 + i0 + row);
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            T *o = out_base + (tok * p.num_heads + h) * D + u * (D / 2);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t v[32];
-                tmem_ld32_nowait(o_addr + (uint32_t)(c * 32), v);
-                tmem_wait_ld();
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    w[j] = pack2<T>(__uint_as_float(v[2 * j]) * inv,
-                                    __uint_as_float(v[2 * j + 1]) * inv);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                }
-            }
-            if (lse_base && valid && u == 0)
-                lse_base[tok * p.num_heads + h] =
-                    l_row > 0.f ? (m_used + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kQkWarp) {
+    if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
