@@ -451,7 +451,7 @@ def run_ours(args) -> dict | None:
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if world == 1 and args.workloads:
-        del w, ws, out, host, out_h
+        del w, ws, out, out_h, dev_buf, host_buf, graph
         torch.cuda.empty_cache()
         line["workloads"] = [other_workload(name, args, peaks["hbm_gbs"])
                              for name in args.workloads.split(",") if name]

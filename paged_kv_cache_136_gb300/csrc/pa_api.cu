@@ -703,6 +703,8 @@ __global__ void __launch_bounds__(256)
 // [nparts][rows]: out = sum_i w_i o_i / sum_i w_i, w_i = exp(lse_i - max).
 // Parts with lse = -inf carry no weight and are not read; a row whose parts
 // are all empty is zero.
+constexpr int kMaxMergeParts = 17; // prefix key chunks (<= 16) + the suffix
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     merge_parts_kernel(T *__restrict__ out, const T *__restrict__ parts,
@@ -715,17 +717,23 @@ __global__ void __launch_bounds__(256)
     if (row >= rows)
         return;
     const int v = (int)(idx - row * vpr);
+    // All the parts' log-sum-exps first (independent loads), then the
+    // weighted sum with the parts' rows loaded side by side.
+    float lv[kMaxMergeParts];
     float M = -INFINITY;
-    for (int i = 0; i < nparts; ++i)
-        M = fmaxf(M, lse_parts[(size_t)i * rows + row]);
+#pragma unroll
+    for (int i = 0; i < kMaxMergeParts; ++i) {
+        lv[i] = i < nparts ? lse_parts[(size_t)i * rows + row] : -INFINITY;
+        M = fmaxf(M, lv[i]);
+    }
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float den = 0.f;
     if (M != -INFINITY) {
-        for (int i = 0; i < nparts; ++i) {
-            const float li = lse_parts[(size_t)i * rows + row];
-            if (li == -INFINITY)
+#pragma unroll
+        for (int i = 0; i < kMaxMergeParts; ++i) {
+            if (lv[i] == -INFINITY)
                 continue;
-            const float w = __expf(li - M);
+            const float w = __expf(lv[i] - M);
             den += w;
             const uint4 u = *reinterpret_cast<const uint4 *>(
                 parts + ((size_t)i * rows + row) * head_size + (size_t)v * 8);
@@ -872,9 +880,14 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
     p.chunk_tiles = key_split > 1 ? chunk_tiles : 1;
     p.part_stride = part_stride;
     p.lse_part_stride = lse_part_stride;
-    // One CTA per 256 query rows (and key chunk), per head, per request.
-    const dim3 grid((unsigned)((max_query_len + 255) / 256 * key_split), (unsigned)num_heads,
-                    (unsigned)num_reqs);
+    // At most 128 query rows per request and an even group size: a CTA's
+    // two tiles take two query heads of one kv head (both busy, one K/V
+    // stream); otherwise one CTA per 256 rows of one head.
+    const int group = num_heads / num_kv_heads;
+    p.head_pairs = (max_query_len <= 128 && group % 2 == 0) ? 1 : 0;
+    const int rows_cta = p.head_pairs ? 128 : 256;
+    const dim3 grid((unsigned)((max_query_len + rows_cta - 1) / rows_cta * key_split),
+                    (unsigned)(p.head_pairs ? num_heads / 2 : num_heads), (unsigned)num_reqs);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = dtype == PA_BF16 ? launch_prefill_bf16(head_size, block_size, pmap, qmap, p, grid, st)
                          : launch_prefill_f16(head_size, block_size, pmap, qmap, p, grid, st);
@@ -1150,7 +1163,7 @@ pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const
 // [suffix lengths] [suffix tables] [parts: prefix key chunks then the suffix,
 // dtype] [their lse] [split-K workspace], 256-byte aligned.  The prefix pass
 // is split over at most kMaxPrefixSplits key chunks.
-constexpr int kMaxPrefixSplits = 16;
+constexpr int kMaxPrefixSplits = kMaxMergeParts - 1;
 
 struct CascadeLayout {
     size_t sl, bt, parts, lse, ws, ws_bytes, total;
@@ -1230,13 +1243,15 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     char *parts = w + c.parts;
     float *lse_parts = reinterpret_cast<float *>(w + c.lse);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Key chunks of the prefix pass: enough CTAs for two waves of the SMs.
+    // Key chunks of the prefix pass: enough CTAs for one wave of the SMs.
     const int sms = sm_count(&e);
     if (!sms)
         return PA_ERR_CUDA;
     const int prefix_tiles = (P + 127) / 128;
-    const int ctas_per_chunk = ((num_seqs + 255) / 256) * num_heads;
-    int nsplit = (2 * sms + ctas_per_chunk - 1) / ctas_per_chunk;
+    const int ctas_per_chunk = (num_seqs <= 128 && (num_heads / num_kv_heads) % 2 == 0)
+                                   ? num_heads / 2
+                                   : ((num_seqs + 255) / 256) * num_heads;
+    int nsplit = (sms + ctas_per_chunk - 1) / ctas_per_chunk;
     nsplit = nsplit < 1 ? 1 : (nsplit > c.max_parts - 1 ? c.max_parts - 1 : nsplit);
     const int chunk_tiles = (prefix_tiles + nsplit - 1) / nsplit;
     nsplit = (prefix_tiles + chunk_tiles - 1) / chunk_tiles;

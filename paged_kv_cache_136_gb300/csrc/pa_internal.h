@@ -164,6 +164,9 @@ struct PrefillParams {
     // every key, out and lse as given.
     int key_split, chunk_tiles;
     long long part_stride, lse_part_stride;
+    // Head pairs: grid.y = H/2 and a CTA's two tiles are query heads 2j and
+    // 2j+1 (same kv head) over the same 128 rows.
+    int head_pairs;
 };
 
 // Prefill over the paged cache on grid (ceil(max_query_len/128) x key_split, H, R).

@@ -135,11 +135,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+255
     const int r = blockIdx.z;
-    const int h = blockIdx.y;
+    // Head pairs (grouped-query heads 2j, 2j+1 share a kv head): tile t
+    // takes the same 128 rows for head 2j+t.  Otherwise tile t takes rows
+    // 128t.. of one head.
+    const bool hp = p.head_pairs != 0;
+    const int h = hp ? 2 * (int)blockIdx.y : (int)blockIdx.y;
     const int nsplit = p.key_split;
     const int csplit = (int)blockIdx.x % nsplit;
     const int qb = (int)gridDim.x / nsplit - 1 - (int)blockIdx.x / nsplit; // heaviest rows first
-    const int i0 = qb * kRowsPerCta;
+    const int i0 = qb * (hp ? kTileM : kRowsPerCta);
+    auto toff = [&](int t) { return hp ? 0 : t * kTileM; };  // tile t's first row
+    auto thead = [&](int t) { return hp ? h + t : h; };       // tile t's query head
     const int q0 = __ldg(p.query_start_loc + r);
     const int q1 = __ldg(p.query_start_loc + r + 1);
     const int L = __ldg(p.seq_lens + r);
@@ -161,20 +167,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nv[2], nt[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        nv[t] = min(max(q_len - (i0 + t * kTileM), 0), kTileM);
-        const int ext = p.causal ? min(L, ctx + i0 + t * kTileM + nv[t]) : key_hi;
+        nv[t] = min(max(q_len - (i0 + toff(t)), 0), kTileM);
+        const int ext = p.causal ? min(L, ctx + i0 + toff(t) + nv[t]) : key_hi;
         nt[t] = nv[t] > 0 ? max(0, (ext - kt0 * kTileN + kTileN - 1) / kTileN) : 0;
     }
     const int n = max(nt[0], nt[1]); // key tiles loaded
     if (n == 0) {
         // An empty key chunk: zero rows and -inf log-sum-exps (an empty part).
-        for (int i = tid; i < (nv[0] + nv[1]) * D; i += kThreads) {
-            const size_t tok = (size_t)(q0 + i0 + i / D);
-            out_base[(tok * p.num_heads + h) * D + i % D] = T(0.f);
+        for (int t = 0; t < 2; ++t) {
+            for (int i = tid; i < nv[t] * D; i += kThreads) {
+                const size_t tok = (size_t)(q0 + i0 + toff(t) + i / D);
+                out_base[(tok * p.num_heads + thead(t)) * D + i % D] = T(0.f);
+            }
+            if (lse_base)
+                for (int i = tid; i < nv[t]; i += kThreads)
+                    lse_base[(size_t)(q0 + i0 + toff(t) + i) * p.num_heads + thead(t)] = -INFINITY;
         }
-        if (lse_base)
-            for (int i = tid; i < nv[0] + nv[1]; i += kThreads)
-                lse_base[(size_t)(q0 + i0 + i) * p.num_heads + h] = -INFINITY;
         return;
     }
     const bool tail = (kt0 + n) * kTileN > L; // the last key tile reaches past seq_len
@@ -216,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nv[t] > 0)
 #pragma unroll
                     for (int hf = 0; hf < NH; ++hf)
-                        tma_load_3d(smem + t * TB + hf * kRegion, &q_map, &m->q_full, hf * 64, h,
-                                    q0 + i0 + t * kTileM);
+                        tma_load_3d(smem + t * TB + hf * kRegion, &q_map, &m->q_full, hf * 64,
+                                    thead(t), q0 + i0 + toff(t));
         }
         // Block-table entries of 64 blocks live in lane registers (this
         // window and the next), refreshed every 32 blocks.
@@ -357,9 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_addr = tmem + lane_base + (uint32_t)(256 + wg * 128);
         const int ntt = nt[wg];
         if (ntt > 0) {
-            const int pos = ctx + i0 + wg * kTileM + row;
+            const int pos = ctx + i0 + toff(wg) + row;
             const int lim = p.causal ? min(L, pos + 1) : key_hi;         // keys < lim
-            const int lim_lo = p.causal ? min(L, ctx + i0 + wg * kTileM + 1) : key_hi;
+            const int lim_lo = p.causal ? min(L, ctx + i0 + toff(wg) + 1) : key_hi;
             const float qs = p.qscale;
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
@@ -477,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 tc_fence_after_sync();
                 const bool valid = row < nv[wg];
-                const size_t tok = (size_t)(q0 + i0 + wg * kTileM + row);
+                const size_t tok = (size_t)(q0 + i0 + toff(wg) + row);
+                const int hw = thead(wg);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                T *o = out_base + (tok * p.num_heads + h) * D;
+                T *o = out_base + (tok * p.num_heads + hw) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
@@ -498,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (lse_base && valid)
-                    lse_base[tok * p.num_heads + h] =
+                    lse_base[tok * p.num_heads + hw] =
                         l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
         }
