@@ -758,6 +758,49 @@ def run_reference(args) -> dict | None:
     }
 
 
+def run_profile_case(name: str, repeat: int) -> None:
+    """Run one case `repeat` times and exit, for a profiler's launch capture:
+    decode_<config> / splitk_<config> (a bench step), prefill_<name>,
+    fp8_<config>, prefix_cascade."""
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    if name.startswith("prefill_"):
+        w = wl.make_prefill(name, device="cuda")
+        out = torch.empty_like(w.q)
+        mq = int(w.q_lens().max())
+        for _ in range(repeat):
+            pa.pa_prefill(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.query_start_loc,
+                          w.scale, w.block_size, mq)
+    elif name.startswith("fp8_"):
+        w = wl.make_fp8(name[4:], device="cuda")
+        msl = int(w.seq_lens.max())
+        ws = torch.empty(pa.pa_decode_splitk_fp8_workspace_size(w.num_seqs, w.num_heads,
+                                                                w.head_size, msl, 512),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(w.q)
+        for _ in range(repeat):
+            pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                                    w.block_size, w.meta["k_scale"], w.meta["v_scale"], msl,
+                                    ws, 512)
+    elif name == "prefix_cascade":
+        w = wl.make("prefix", device="cuda")
+        msl = int(w.seq_lens.max())
+        pb = w.meta["shared_blocks"]
+        n = pa.pa_cascade_decode_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                                w.block_tables.shape[1], pb, msl,
+                                                w.block_size, 512)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(w.q)
+        for _ in range(repeat):
+            pa.pa_cascade_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                                 w.block_size, pb, msl, ws, 512)
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    torch.cuda.synchronize()
+    print(f"{name}: {repeat} runs, device error flags {pa.pa_device_errors()}")
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -778,11 +821,18 @@ def parse_args(argv=None):
                             "prefill_gqa8b,fp8_mha7b,fp8_gqa8b",
                     help="other workloads measured briefly beside the main line ('' for none)")
     ap.add_argument("--workload-steps", type=int, default=50)
+    ap.add_argument("--profile-case", default=None,
+                    help="run one case --repeat times for a profiler and exit (no JSON): "
+                         "prefill_<name>, fp8_<config>, prefix_cascade")
+    ap.add_argument("--repeat", type=int, default=3)
     return ap.parse_args(argv)
 
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args.profile_case, max(1, args.repeat))
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
