@@ -575,15 +575,15 @@ static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const 
             return PA_ERR_CUDA;
         uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
         uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
-        if (dtype == PA_BF16)
-            tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
-                static_cast<__nv_bfloat16 *>(out), lse, err);
-        else
-            tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
-                static_cast<__half *>(out), lse, err);
-        if ((e = cudaGetLastError()) != cudaSuccess)
+        e = dtype == PA_BF16
+                ? launch_after_previous(tc::splitk_plan_kernel<__nv_bfloat16>, dim3(1), dim3(1024), 0,
+                                        s, seq_lens, num_seqs, num_heads, ngroups, partition_size,
+                                        len_cap, hdr, units, static_cast<__nv_bfloat16 *>(out), lse,
+                                        err)
+                : launch_after_previous(tc::splitk_plan_kernel<__half>, dim3(1), dim3(1024), 0, s,
+                                        seq_lens, num_seqs, num_heads, ngroups, partition_size,
+                                        len_cap, hdr, units, static_cast<__half *>(out), lse, err);
+        if (e != cudaSuccess)
             return PA_ERR_CUDA;
         tc::TcParams t = {};
         t.out = out;

@@ -679,7 +679,10 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t bucket[kPlanBuckets];
     __shared__ uint32_t carry_s;
-    griddep_launch_dependents(); // the decode grid may start its prologue
+    // Launched as the dependent of the kernel before it (the cache write):
+    // wait for its results, let the decode grid start its prologue.
+    griddep_wait();
+    griddep_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     for (int i = tid; i < kPlanBuckets; i += blockDim.x)
