@@ -760,7 +760,7 @@ def run_reference(args) -> dict | None:
 
 def run_profile_case(name: str, repeat: int) -> None:
     """Run one case `repeat` times and exit, for a profiler's launch capture:
-    decode_<config> / splitk_<config> (a bench step), prefill_<name>,
+    splitk_<config> (a bench step: cache write, split-K decode), prefill_<name>,
     fp8_<config>, prefix_cascade."""
     import torch
     import paged_kv_cache_136_gb300 as pa
@@ -783,6 +783,17 @@ def run_profile_case(name: str, repeat: int) -> None:
             pa.pa_decode_splitk_fp8(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
                                     w.block_size, w.meta["k_scale"], w.meta["v_scale"], msl,
                                     ws, 512)
+    elif name.startswith("splitk_"):
+        w = wl.make(name[7:], device="cuda")
+        msl = int(w.seq_lens.max())
+        ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads,
+                                                            w.head_size, msl, 512),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(w.q)
+        for _ in range(repeat):
+            pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+            pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                                w.block_size, msl, ws, 512)
     elif name == "prefix_cascade":
         w = wl.make("prefix", device="cuda")
         msl = int(w.seq_lens.max())
@@ -823,7 +834,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload-steps", type=int, default=50)
     ap.add_argument("--profile-case", default=None,
                     help="run one case --repeat times for a profiler and exit (no JSON): "
-                         "prefill_<name>, fp8_<config>, prefix_cascade")
+                         "splitk_<config>, prefill_<name>, fp8_<config>, prefix_cascade")
     ap.add_argument("--repeat", type=int, default=3)
     return ap.parse_args(argv)
 

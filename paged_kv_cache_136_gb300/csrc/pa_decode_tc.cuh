@@ -88,7 +88,7 @@ struct StageDesc {
 struct Misc {
     StageDesc desc[kStages];
     float red[2][4][kNQ];  // per-stage max, double-buffered by stage parity
-    float red2[4][kNQ];    // normaliser sums at item end
+    float red2[2][4][kNQ]; // normaliser sums at item end, double-buffered by item
     int bcast[4];
     uint32_t tmem_base;
     uint32_t pad;
@@ -481,6 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = 0; g < G; ++g)
             l_part[g] = 0.f;
         bool pending = false; // the previous stage's O is still to be accumulated
+        // An item whose last stage's values were still on the tensor cores
+        // when its softmax ended: it is normalised and written once that O is
+        // folded in, after the next stage's softmax, so the wait for the
+        // values MMA overlaps work instead of stalling the ring at every item
+        // change.  Its column sums of l wait in red2[fin_par].
+        bool fin = false;
+        int fin_s = 0, fin_group = 0, fin_part = 0, fin_nparts = 1, fin_par = 0;
+        float fin_m = 0.f; // running max of column t (t < NV) of that item
+        int par = 0;
         // o = alpha*o + O_high + O_low for stage k, then free the O buffer.
         auto take_o = [&](int k, const float (&alpha)[NV]) -> bool {
             const int b = k & 1;
@@ -499,6 +508,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&m->o_free[b]);
             return okw;
         };
+        // Normalise and store the finished item (o_acc holds its sums), then
+        // clear the accumulator for the item under way.
+        auto finish = [&]() {
+            float l[NV];
+#pragma unroll
+            for (int n = 0; n < NV; ++n)
+                l[n] = (m->red2[fin_par][0][n] + m->red2[fin_par][1][n]) +
+                       (m->red2[fin_par][2][n] + m->red2[fin_par][3][n]);
+            const size_t head0 = (size_t)fin_s * p.num_heads + (size_t)fin_group * NV;
+            if (!SPLIT || fin_nparts == 1) {
+                T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
+#pragma unroll
+                for (int n = 0; n < NV; ++n)
+                    out[n * kD + t] = Elem<T>::from(o_acc[n] / l[n]);
+                if (p.lse) {
+#pragma unroll
+                    for (int n = 0; n < NV; ++n)
+                        if (t == n)
+                            p.lse[head0 + n] = (fin_m + __log2f(l[n])) * 0.69314718055994531f;
+                }
+            } else {
+                // Partial state of this partition; the reduce kernel that
+                // follows merges the partitions of the sequence.
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    const size_t row = (head0 + n) * p.max_parts + fin_part;
+                    p.ws_o[row * kD + t] = o_acc[n];
+                    if (t == n) {
+                        p.ws_ml[row * 2] = fin_m;
+                        p.ws_ml[row * 2 + 1] = l[n];
+                    }
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < NV; ++n)
+                o_acc[n] = 0.f;
+            fin = false;
+        };
         for (int k = 0;; ++k) {
             const int slot = k % kStages;
             const int b = k & 1;
@@ -510,18 +557,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT_);
                 break;
             }
-            if (d.flags & kFlagStop)
-                break;
-            if (d.flags & kFlagFirst) {
-#pragma unroll
-                for (int n = 0; n < NV; ++n) {
-                    m_run[n] = -INFINITY;
-                    o_acc[n] = 0.f;
+            if (d.flags & kFlagStop) {
+                // No more work: the last item's final values are still out.
+                if (fin) {
+                    if (!take_o(k - 1, alpha_prev) && t == 0)
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+                    finish();
                 }
+                break;
+            }
+            if (d.flags & kFlagFirst) {
+                // o_acc is cleared by finish() of the item before.
+#pragma unroll
+                for (int n = 0; n < NV; ++n)
+                    m_run[n] = -INFINITY;
 #pragma unroll
                 for (int g = 0; g < G; ++g)
                     l_part[g] = 0.f;
-                pending = false;
             }
             ok = mbar_wait(&m->s_full[b], u & 1);
             __syncwarp();
@@ -596,9 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&m->p_full[b]);
 
             // The previous stage's values ran on the tensor cores while this
-            // stage's softmax was computed; fold them in now.
+            // stage's softmax was computed; fold them in now.  If that stage
+            // ended an item, the item is complete: store it.
             if (pending && !take_o(k - 1, alpha_prev) && t == 0)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+            if (fin)
+                finish();
 #pragma unroll
             for (int n = 0; n < NV; ++n)
                 alpha_prev[n] = alpha[n];
@@ -606,10 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (!(d.flags & kFlagLast))
                 continue;
-            if (!take_o(k, alpha_prev) && t == 0)
-                atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-            pending = false;
-            // ---- end of the item: normaliser of each (head, query) column
+            // ---- last stage of the item: its normaliser sums go to red2[par]
+            // and column t's running max to fin_m; the values of this stage
+            // are folded in (and the item stored) after the next stage's
+            // softmax.
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float v = l_part[g];
@@ -617,38 +672,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int off = HG; off < 32; off <<= 1)
                     v += __shfl_xor_sync(0xffffffffu, v, off);
                 if (lane < HG)
-                    m->red2[warp][lane * G + g] = v;
+                    m->red2[par][warp][lane * G + g] = v;
             }
-            bar_sync(kBarEpi, kEpiThreads);
-            float l[NV];
 #pragma unroll
             for (int n = 0; n < NV; ++n)
-                l[n] = (m->red2[0][n] + m->red2[1][n]) + (m->red2[2][n] + m->red2[3][n]);
-            const size_t head0 = (size_t)d.s * p.num_heads + (size_t)d.group * NV;
-            if (!SPLIT || d.nparts == 1) {
-                T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
-#pragma unroll
-                for (int n = 0; n < NV; ++n)
-                    out[n * kD + t] = Elem<T>::from(o_acc[n] / l[n]);
-                if (p.lse) {
-#pragma unroll
-                    for (int n = 0; n < NV; ++n)
-                        if (t == n)
-                            p.lse[head0 + n] = (m_run[n] + __log2f(l[n])) * 0.69314718055994531f;
-                }
-            } else {
-                // Partial state of this partition; the reduce kernel that
-                // follows merges the partitions of the sequence.
-#pragma unroll
-                for (int n = 0; n < NV; ++n) {
-                    const size_t row = (head0 + n) * p.max_parts + d.part;
-                    p.ws_o[row * kD + t] = o_acc[n];
-                    if (t == n) {
-                        p.ws_ml[row * 2] = m_run[n];
-                        p.ws_ml[row * 2 + 1] = l[n];
-                    }
-                }
-            }
+                if (t == n)
+                    fin_m = m_run[n];
+            fin = true;
+            fin_s = d.s;
+            fin_group = d.group;
+            fin_part = d.part;
+            fin_nparts = d.nparts;
+            fin_par = par;
+            par ^= 1;
         }
     }
 
