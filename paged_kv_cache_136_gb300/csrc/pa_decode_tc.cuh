@@ -92,7 +92,9 @@ struct Misc {
     int bcast[4];
     uint32_t tmem_base;
     uint32_t pad;
-    uint64_t full[kStages], empty[kStages];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];   // V of the slot free (its values MMA is done)
+    uint64_t empty_k[kStages]; // K and Q of the slot free (its scores MMA is done)
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
     uint64_t mma_done[2];
 };
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&m->full[i], 1);
             mbar_init(&m->empty[i], 1);
+            mbar_init(&m->empty_k[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&m->s_full[i], 1);
@@ -329,7 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qrow = s * p.num_heads + kvh0 * G;
             for (int st = 0; st < nst; ++st, ++gk) {
                 const int slot = gk % kStages;
-                if (gk >= kStages && !warp_wait(&m->empty[slot], ((gk / kStages) - 1) & 1, lane)) {
+                const uint32_t ph = ((gk / kStages) - 1) & 1;
+                // K and Q of the slot are released by the scores MMA, V only by
+                // the values MMA after the softmax: K and Q of this stage are
+                // loaded as soon as the first is done, so more of the ring is
+                // in flight while the softmax runs.
+                if (gk >= kStages && !warp_wait(&m->empty_k[slot], ph, lane)) {
                     if (lane == 0)
                         atomicOr(p.err, PA_DEVERR_TIMEOUT_);
                     alive = false;
@@ -346,15 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *kv = smem + slot * kStageBytes;
                 uint8_t *qb = smem + kOffQ + slot * kQBytes;
                 if (lane == 0) {
-                    StageDesc &d = m->desc[slot];
-                    d.s = s;
-                    d.group = group;
-                    d.part = part;
-                    d.nvalid = nvalid;
-                    d.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
-                    d.nparts = nparts;
-                    mbar_arrive_expect_tx(&m->full[slot],
-                                          (uint32_t)(nch * 4 * BOX_BYTES + 2 * NV * 128));
+                    mbar_expect_tx(&m->full[slot], (uint32_t)(nch * 2 * BOX_BYTES + 2 * NV * 128));
                     tma_load_2d(qb, &q_map, &m->full[slot], 0, qrow);
                     tma_load_2d(qb + kNQ * 128, &q_map, &m->full[slot], 64, qrow);
                 }
@@ -364,19 +364,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c = lane >> 2;
                 const int t = t_lo + (c < CH ? c : 0) * R;
                 const int phys = __shfl_sync(0xffffffffu, cur, (t / BS - cbase) & 31);
+                const int plane = (lane >> 1) & 1;
+                int row = 0;
                 if (lane < nch * 4) {
-                    const int plane = (lane >> 1) & 1;
-                    const int r = lane & 1;
-                    int row;
                     if (phys < 0 || phys >= p.num_blocks) {
-                        atomicOr(p.err, PA_DEVERR_BLOCK_ID_);
+                        if (plane == 0)
+                            atomicOr(p.err, PA_DEVERR_BLOCK_ID_);
                         row = p.num_blocks * BS; // past the extent: zero fill
                     } else {
                         row = phys * BS + t % BS;
                     }
-                    tma_load_4d_hint(kv + plane * kPlane + r * kRegion + c * BOX_BYTES, &pool_map,
-                                     &m->full[slot], r * 64, kvh0, row, plane, policy);
                 }
+                if (lane < nch * 4 && plane == 0)
+                    tma_load_4d_hint(kv + (lane & 1) * kRegion + c * BOX_BYTES, &pool_map,
+                                     &m->full[slot], (lane & 1) * 64, kvh0, row, 0, policy);
+                if (gk >= kStages && !warp_wait(&m->empty[slot], ph, lane)) {
+                    // Let the K and Q copies already issued land before leaving;
+                    // the other roles see a stop at this slot.
+                    if (lane == 0) {
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT_);
+                        m->desc[slot].flags = kFlagStop;
+                        mbar_arrive(&m->full[slot]);
+                    }
+                    warp_wait(&m->full[slot], (gk / kStages) & 1, lane);
+                    alive = false;
+                    break;
+                }
+                if (lane == 0) {
+                    StageDesc &d = m->desc[slot];
+                    d.s = s;
+                    d.group = group;
+                    d.part = part;
+                    d.nvalid = nvalid;
+                    d.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
+                    d.nparts = nparts;
+                    mbar_arrive_expect_tx(&m->full[slot], (uint32_t)(nch * 2 * BOX_BYTES));
+                }
+                __syncwarp();
+                if (lane < nch * 4 && plane == 1)
+                    tma_load_4d_hint(kv + kPlane + (lane & 1) * kRegion + c * BOX_BYTES, &pool_map,
+                                     &m->full[slot], (lane & 1) * 64, kvh0, row, 1, policy);
                 // Next item: claim it when three stages of this one are left
                 // to issue (claiming earlier would unbalance the tail), then
                 // its unit, then its length and table.
@@ -443,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&m->s_full[b]);
+                    umma_commit(&m->empty_k[slot]);
                 } else {
                     const uint32_t vbase = kvbase + kPlane;
                     const uint32_t pbase = smem_addr(smem + kOffP + b * kPBytes);
