@@ -263,6 +263,11 @@ __global__ void __launch_bounds__(256)
                              int num_tokens, int row_vecs, int64_t key_stride_vecs,
                              int64_t value_stride_vecs, int64_t num_slots, unsigned int *err)
 {
+    // Launched as the dependent of the kernel before it (which may write the
+    // inputs or read the cache): wait for it, then let the kernel after this
+    // one (the split-K plan) get resident while the copy runs.
+    griddep_wait();
+    griddep_launch_dependents();
     const int tok = blockIdx.y;
     const int64_t slot = slots[tok];
     if (slot < 0)
@@ -414,11 +419,13 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, void *kv_cach
     const int threads = 256;
     int bx = (row_vecs + threads - 1) / threads;
     dim3 grid(bx, num_tokens);
-    reshape_and_cache_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+    const cudaError_t le = launch_after_previous(
+        reshape_and_cache_kernel, grid, dim3(threads), 0, static_cast<cudaStream_t>(stream),
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
-        static_cast<uint4 *>(kv_cache), slot_mapping, num_tokens, row_vecs, key_stride / 8,
-        value_stride / 8, (int64_t)num_blocks * block_size, err);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+        static_cast<uint4 *>(kv_cache), slot_mapping, num_tokens, row_vecs,
+        (int64_t)(key_stride / 8), (int64_t)(value_stride / 8), (int64_t)num_blocks * block_size,
+        err);
+    return le == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_t *block_tables,
