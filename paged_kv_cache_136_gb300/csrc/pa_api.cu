@@ -1048,21 +1048,26 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
                                box_rows, hg) ||
             !make_q_parts_map(&qmap, qparts, rows, hg * group))
             return PA_ERR_CUDA;
+        // The plan reads only seq_lens, the query prepass only q: the prepass
+        // runs as the plan's dependent (it cannot start before the plan has
+        // waited for the kernel before it) and waits for the plan at its end,
+        // so the decode kernel's wait on the prepass covers both.
+        uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
+        uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
+        e = dtype == PA_BF16
+                ? launch_after_previous(tc::splitk_plan_kernel<__nv_bfloat16>, dim3(1), dim3(1024), 0,
+                                        s, seq_lens, num_seqs, num_heads, ngroups, partition_size,
+                                        len_cap, hdr, units, static_cast<__nv_bfloat16 *>(out),
+                                        static_cast<float *>(nullptr), err)
+                : launch_after_previous(tc::splitk_plan_kernel<__half>, dim3(1), dim3(1024), 0, s,
+                                        seq_lens, num_seqs, num_heads, ngroups, partition_size,
+                                        len_cap, hdr, units, static_cast<__half *>(out),
+                                        static_cast<float *>(nullptr), err);
+        if (e != cudaSuccess)
+            return PA_ERR_CUDA;
         e = dtype == PA_BF16 ? launch_quantize_q_bf16(q, qparts, qscales, rows, s)
                              : launch_quantize_q_f16(q, qparts, qscales, rows, s);
         if (e != cudaSuccess)
-            return PA_ERR_CUDA;
-        uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
-        uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
-        if (dtype == PA_BF16)
-            tc::splitk_plan_kernel<__nv_bfloat16><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
-                static_cast<__nv_bfloat16 *>(out), nullptr, err);
-        else
-            tc::splitk_plan_kernel<__half><<<1, 1024, 0, s>>>(
-                seq_lens, num_seqs, num_heads, ngroups, partition_size, len_cap, hdr, units,
-                static_cast<__half *>(out), nullptr, err);
-        if (cudaGetLastError() != cudaSuccess)
             return PA_ERR_CUDA;
         tc::TcParams t = {};
         t.out = out;

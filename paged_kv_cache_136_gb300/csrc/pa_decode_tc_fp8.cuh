@@ -134,10 +134,18 @@ __global__ void __launch_bounds__(128)
     quantize_q_parts_kernel(const T *__restrict__ q, uint8_t *__restrict__ parts,
                             float *__restrict__ scales, int rows)
 {
+    // Launched as the dependent of the split-K plan, which has already waited
+    // for the kernel before it (so q is final); the decode kernel may start
+    // its prologue at once.  Every thread waits for the plan before it exits,
+    // so this grid completes only after the plan: the decode kernel's wait on
+    // it covers both.
+    griddep_launch_dependents();
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows)
+    if (row >= rows) {
+        griddep_wait();
         return;
+    }
     const uint2 raw = *reinterpret_cast<const uint2 *>(q + (size_t)row * kD + lane * 4);
     const T *e = reinterpret_cast<const T *>(&raw);
     float x[4], amax = 0.f;
@@ -164,6 +172,7 @@ __global__ void __launch_bounds__(128)
         *reinterpret_cast<uint32_t *>(parts + ((size_t)pp * rows + row) * kD + lane * 4) = w[pp];
     if (lane == 0)
         scales[row] = sc;
+    griddep_wait();
 }
 
 template <typename T, int BS, int G, int HG, bool SPLIT>
@@ -746,9 +755,8 @@ template <typename T>
 cudaError_t launch_quantize_q(const void *q, uint8_t *parts, float *scales, int rows,
                               cudaStream_t stream)
 {
-    quantize_q_parts_kernel<T><<<(rows + 3) / 4, 128, 0, stream>>>(static_cast<const T *>(q),
-                                                                   parts, scales, rows);
-    return cudaGetLastError();
+    return launch_after_previous(quantize_q_parts_kernel<T>, dim3((rows + 3) / 4), dim3(128), 0,
+                                 stream, static_cast<const T *>(q), parts, scales, rows);
 }
 
 } // namespace tc8
