@@ -98,6 +98,14 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Warp-uniform bounded wait driven by lane 0.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane)
 {
@@ -384,26 +392,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
                 tmem_wait_ld();
                 // Row max over the raw scores (scale > 0 commutes with max),
-                // in 8 independent chains; masked keys become -inf.
-                float m8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    m8[j] = -INFINITY;
+                // three-input maxima in 4 independent chains; masked keys
+                // become -inf.
                 if ((kt0 + k + 1) * kTileN > lim_lo) {
                     const int kl = lim - (kt0 + k) * kTileN; // keys of this tile below the limit
 #pragma unroll
-                    for (int i = 0; i < kTileN; ++i) {
-                        const float x = i < kl ? __uint_as_float(sv[i]) : -INFINITY;
-                        sv[i] = __float_as_uint(x);
-                        m8[i & 7] = fmaxf(m8[i & 7], x);
-                    }
-                } else {
-#pragma unroll
                     for (int i = 0; i < kTileN; ++i)
-                        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
+                        if (i >= kl)
+                            sv[i] = __float_as_uint(-INFINITY);
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qs;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < kTileN / 2; ++i)
+                    m4[i & 3] = fmax3(m4[i & 3], __uint_as_float(sv[2 * i]),
+                                      __uint_as_float(sv[2 * i + 1]));
+                const float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * qs;
                 float alpha = 1.f;
                 bool need = false;
                 if (k == 0) {
@@ -414,31 +417,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= alpha;
                     need = true;
                 }
-                // p = 2^(S * scale*log2e - m): one FFMA and one ex2 per key;
-                // the row sum in 4 independent chains.
+                // p = 2^(S * scale*log2e - m): one packed FFMA per two keys and
+                // one ex2 per key; the row sum in two packed chains.
                 const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                const float2 qs2 = make_float2(qs, qs), nmu2 = make_float2(nmu, nmu);
+                float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16], lo[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j]), qs, nmu));
-                        const float p1 =
-                            ex2(fmaf(__uint_as_float(sv[c * 32 + 2 * j + 1]), qs, nmu));
-                        l4[j & 3] += p0 + p1;
-                        pk[j] = pack2<T>(p0, p1);
+                        const float2 z = __ffma2_rn(make_float2(__uint_as_float(sv[c * 32 + 2 * j]),
+                                                                __uint_as_float(sv[c * 32 + 2 * j + 1])),
+                                                    qs2, nmu2);
+                        const float2 pp = make_float2(ex2(z.x), ex2(z.y));
+                        l2[j & 1] = __fadd2_rn(l2[j & 1], pp);
+                        pk[j] = pack2<T>(pp.x, pp.y);
                         if (kSplitP) {
                             const float h0 = __uint_as_float(pk[j] << 16);
                             const float h1 = __uint_as_float(pk[j] & 0xFFFF0000u);
-                            lo[j] = pack2<T>(p0 - h0, p1 - h1);
+                            lo[j] = pack2<T>(pp.x - h0, pp.y - h1);
                         }
                     }
                     tmem_st16(s_addr + (uint32_t)(c * 16), pk);
                     if (kSplitP)
                         tmem_st16(s_addr + (uint32_t)(64 + c * 16), lo);
                 }
-                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                l += (l2[0].x + l2[1].x) + (l2[0].y + l2[1].y);
                 if (__any_sync(0xffffffffu, need)) {
                     // O holds the values of key tiles 0..k-1 (their MMAs are
                     // complete: S_k was committed after them).  Done after P
