@@ -65,8 +65,11 @@ constexpr float kInvPScale = 1.f / 256.f;
 constexpr float kQRange = 256.f;           // |q'| <= 256
 
 constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kOffP = kOffQ + kStages * kQBytes;
-constexpr int kOffMisc = kOffP + kPBytes; // one P buffer
+// P of a stage lives in the first kPBytes of the stage's K region (see the
+// softmax), so it needs no buffer of its own.
+constexpr int kOffMisc = kOffQ + kStages * kQBytes;
+static_assert(kPBytes <= kPlane && kPBytes % (16 * kEpiThreads) == 0 && (kNP * 128) % 1024 == 0,
+              "P fits the K region, clears in whole 16-byte stores, keeps 1024-byte atoms");
 
 struct Misc {
     StageDesc desc[kStages];
@@ -200,11 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // P entries of other heads' columns stay zero for the whole kernel: a
-    // row (token, head h) only ever writes the columns of head h.
-    for (int i = tid; i < kPBytes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&m->full[i], 1);
@@ -457,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(&m->s_full[b]);
                 } else {
                     const uint32_t vbase = kvbase + kPlane;
-                    const uint32_t pbase = smem_addr(smem + kOffP);
+                    const uint32_t pbase = kvbase; // P over the stage's K (see the softmax)
                     const uint32_t d_tmem = tmem + (uint32_t)(kOCol + b * kNP);
                     // V^T as the MN-major A operand, 32 stage rows (4 KB) per
                     // step over all 256 rows; P's K runs over two regions.
@@ -544,6 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&m->s_full[b], u & 1);
             __syncwarp();
             tc_fence_after_sync();
+            // P of this stage goes over the stage's K: the scores MMA that
+            // read K is complete (s_full), and the producer refills the slot
+            // only after the values MMA has read P.  Each row writes only the
+            // columns of its own head, so the region is cleared first; the
+            // barrier after the row maxima orders the clearing before every
+            // thread's writes.  Stages therefore never wait for the previous
+            // stage's values MMA to release a shared P buffer.
+            uint8_t *pb = smem + slot * kStageBytes;
+#pragma unroll
+            for (int i = 0; i < kPBytes / 16 / kEpiThreads; ++i)
+                reinterpret_cast<uint4 *>(pb)[t + i * kEpiThreads] = make_uint4(0, 0, 0, 0);
             // This thread's two stage rows: t (block 0) and 128 + t (block 1),
             // both of head h.
             float x[2][G];
@@ -592,11 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run[n] = m_new;
             }
             // P as the K-major B operand of the values MMA: column (k index)
-            // = the stage row; row pp*16 + h*G + g holds part pp.  One buffer:
-            // the previous stage's values MMA must have read it.
-            if (k > 0 && !mbar_wait(&m->o_full[(k - 1) & 1], ((k - 1) >> 1) & 1) && t == 0)
-                atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-            uint8_t *pb = smem + kOffP;
+            // = the stage row; row pp*16 + h*G + g holds part pp.
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float mg = m_run[g], ag = alpha[g];
