@@ -893,8 +893,12 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
     const int group = num_heads / num_kv_heads;
     p.head_pairs = (max_query_len <= 128 && group % 2 == 0) ? 1 : 0;
     const int rows_cta = p.head_pairs ? 128 : 256;
-    const dim3 grid((unsigned)((max_query_len + rows_cta - 1) / rows_cta * key_split),
-                    (unsigned)(p.head_pairs ? num_heads / 2 : num_heads), (unsigned)num_reqs);
+    // x = query head (or pair), y = request, z = query block from the end x key chunk
+    const int64_t zdim = (int64_t)((max_query_len + rows_cta - 1) / rows_cta) * key_split;
+    if (zdim > 65535 || num_reqs > 65535)
+        return PA_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)(p.head_pairs ? num_heads / 2 : num_heads), (unsigned)num_reqs,
+                    (unsigned)zdim);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = dtype == PA_BF16 ? launch_prefill_bf16(head_size, block_size, pmap, qmap, p, grid, st)
                          : launch_prefill_f16(head_size, block_size, pmap, qmap, p, grid, st);

@@ -142,16 +142,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
 
     // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+255
-    const int r = blockIdx.z;
+    // Grid: x = query head (or head pair), y = request, z = query block
+    // counted from the request's last one (times the key chunks).  CTAs start
+    // in linear order, x fastest, so the last blocks of all requests -- under
+    // the causal mask the ones that attend to the most keys -- start first and
+    // the short first blocks fill the tail.
+    const int r = blockIdx.y;
     // Head pairs (grouped-query heads 2j, 2j+1 share a kv head): tile t
     // takes the same 128 rows for head 2j+t.  Otherwise tile t takes rows
     // 128t.. of one head.
     const bool hp = p.head_pairs != 0;
-    const int h = hp ? 2 * (int)blockIdx.y : (int)blockIdx.y;
+    const int h = hp ? 2 * (int)blockIdx.x : (int)blockIdx.x;
     const int nsplit = p.key_split;
-    const int csplit = (int)blockIdx.x % nsplit;
-    const int qb = (int)gridDim.x / nsplit - 1 - (int)blockIdx.x / nsplit; // heaviest rows first
-    const int i0 = qb * (hp ? kTileM : kRowsPerCta);
+    const int csplit = (int)blockIdx.z % nsplit;
+    const int rank = (int)blockIdx.z / nsplit;
+    const int rows_cta = hp ? kTileM : kRowsPerCta;
     auto toff = [&](int t) { return hp ? 0 : t * kTileM; };  // tile t's first row
     auto thead = [&](int t) { return hp ? h + t : h; };       // tile t's query head
     const int q0 = __ldg(p.query_start_loc + r);
@@ -160,12 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_len = q1 - q0;
     if (q0 < 0 || q1 > p.num_tokens || q_len < 0 || q_len > p.max_query_len || L < q_len ||
         L > p.max_blocks * BS) {
-        if (tid == 0 && qb == 0 && h == 0)
+        if (tid == 0 && rank == 0 && csplit == 0 && h == 0)
             atomicOr(p.err, PA_DEVERR_SEQ_LEN_);
         return;
     }
-    if (i0 >= q_len)
+    const int qb = (q_len + rows_cta - 1) / rows_cta - 1 - rank;
+    if (qb < 0)
         return;
+    const int i0 = qb * rows_cta;
     const int ctx = L - q_len;
     // Keys of this CTA: [kt0 * 128, key_hi) (the whole request unless split).
     const int kt0 = csplit * p.chunk_tiles;
