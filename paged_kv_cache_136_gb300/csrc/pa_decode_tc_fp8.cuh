@@ -129,6 +129,25 @@ __device__ __forceinline__ void split3_e4m3(float x, uint8_t (&c)[3])
     }
 }
 
+// Two values as three e4m3 parts each, exactly as split3_e4m3 would give, with
+// one paired conversion per step for both.
+__device__ __forceinline__ void split3_e4m3x2(float a, float b, uint8_t (&ca)[3],
+                                              uint8_t (&cb)[3])
+{
+    float ra = a, rb = b;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        unsigned short pair;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(ra), "f"(rb));
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+        ca[i] = (uint8_t)(pair >> 8);
+        cb[i] = (uint8_t)(pair & 0xFFu);
+        ra -= __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+        rb -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    }
+}
+
 // Query prepass: one warp per (sequence, head) row of 128 elements.  scale =
 // max|q| / 256 (1 for an all-zero row); the three e4m3 parts of q / scale go
 // to parts[p][row][0..127], the scale to scales[row].
@@ -616,14 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_part[g] = fmaf(l_part[g], ag, pr0 + pr1);
                 // 256 p as three e4m3 parts (about 12 significant bits).
                 const int n = h * G + g;
+                uint8_t c3[2][3];
+                split3_e4m3x2(pr0 * kPScale, pr1 * kPScale, c3[0], c3[1]);
 #pragma unroll
-                for (int ub = 0; ub < 2; ++ub) {
-                    uint8_t c3[3];
-                    split3_e4m3((ub ? pr1 : pr0) * kPScale, c3);
+                for (int ub = 0; ub < 2; ++ub)
 #pragma unroll
                     for (int pp = 0; pp < kParts; ++pp)
-                        pb[ub * (kNP * 128) + sw128_offset_b8(pp * kPartRows + n, t)] = c3[pp];
-                }
+                        pb[ub * (kNP * 128) + sw128_offset_b8(pp * kPartRows + n, t)] = c3[ub][pp];
             }
 #pragma unroll
             for (int ub = 0; ub < 2; ++ub)
