@@ -231,6 +231,16 @@ cudaError_t launch_decode(const DecodeKey &key, const CUtensorMap &tmap, const D
     return cudaErrorNotSupported;
 }
 
+template <typename T, int D>
+static cudaError_t launch_reduce_t(const ReduceParams &p, dim3 grid, cudaStream_t stream)
+{
+    // Rows of many partitions: four thread groups split a row's partitions.
+    if (p.max_parts >= 32)
+        return launch_after_previous(splitk_reduce_kernel<T, D, 4>, grid, dim3(4 * D), 0, stream,
+                                     p);
+    return launch_after_previous(splitk_reduce_kernel<T, D, 1>, grid, dim3(D), 0, stream, p);
+}
+
 cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int num_seqs,
                           cudaStream_t stream)
 {
@@ -238,16 +248,13 @@ cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int n
     // that kernel's tail, and it waits for the partial states on the device.
     dim3 grid(p.num_heads, num_seqs);
     if (dtype == PA_FP16 && head_size == 64)
-        return launch_after_previous(splitk_reduce_kernel<__half, 64>, grid, dim3(64), 0, stream, p);
+        return launch_reduce_t<__half, 64>(p, grid, stream);
     if (dtype == PA_FP16 && head_size == 128)
-        return launch_after_previous(splitk_reduce_kernel<__half, 128>, grid, dim3(128), 0, stream,
-                                     p);
+        return launch_reduce_t<__half, 128>(p, grid, stream);
     if (dtype == PA_BF16 && head_size == 64)
-        return launch_after_previous(splitk_reduce_kernel<__nv_bfloat16, 64>, grid, dim3(64), 0,
-                                     stream, p);
+        return launch_reduce_t<__nv_bfloat16, 64>(p, grid, stream);
     if (dtype == PA_BF16 && head_size == 128)
-        return launch_after_previous(splitk_reduce_kernel<__nv_bfloat16, 128>, grid, dim3(128), 0,
-                                     stream, p);
+        return launch_reduce_t<__nv_bfloat16, 128>(p, grid, stream);
     return cudaErrorNotSupported;
 }
 

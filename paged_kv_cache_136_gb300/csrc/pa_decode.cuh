@@ -398,66 +398,103 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // Log-sum-exp merge of the partitions of one (sequence, query head):
 // M = max_p m_p, out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
-// The partition weights are computed once into shared memory (chunks of
-// kReduceChunk partitions); each thread then sums its head_size element with
-// independent loads.
+// The weights w_p = 2^(m_p - M) are formed once per partition in shared
+// memory (chunks of kReduceChunk partitions) and the normaliser is a block
+// sum of w_p l_p.  GR groups of D threads split the partitions (group g
+// takes p = g, g + GR, ...); each thread sums its head_size element with four
+// independent accumulators, and the groups' sums are added at the end.  Many
+// partitions (long sequences) want GR > 1, so the loads of all partitions of
+// a row are in flight at once instead of one after another.
 constexpr int kReduceChunk = 512;
 
-template <typename T, int D>
-__global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p)
+template <typename T, int D, int GR>
+__global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParams p)
 {
+    constexpr int NT = D * GR;
+    constexpr int NW = NT / 32;
     __shared__ float w_s[kReduceChunk];
-    __shared__ float red_s[D / 32];
-    __shared__ float M_s;
+    __shared__ float red_s[NW];
+    __shared__ float num_s[GR > 1 ? GR - 1 : 1][D];
+    __shared__ float bc_s;
     griddep_wait(); // the partition kernel's states are complete
-    const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int d = tid % D, g = tid / D, lane = tid & 31, warp = tid >> 5;
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
     const int np = (L + p.part_tokens - 1) / p.part_tokens;
     const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
     T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + h) * D;
     if (np == 0) {
-        out[d] = Elem<T>::from(0.f);
-        if (p.lse && d == 0)
+        if (g == 0)
+            out[d] = Elem<T>::from(0.f);
+        if (p.lse && tid == 0)
             p.lse[(size_t)s * p.num_heads + h] = -INFINITY;
         return;
     }
     if (np == 1 && p.skip_single)
         return;
-    // global max of m over the partitions
-    float M = -INFINITY;
-    for (int q = d; q < np; q += D)
-        M = fmaxf(M, p.ws_ml[(row0 + q) * 2]);
+    // Block-wide max / sum of one value per thread, returned to every thread.
+    auto block_reduce = [&](float v, bool is_max) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if ((d & 31) == 0)
-        red_s[d >> 5] = M;
-    __syncthreads();
-    if (d == 0) {
-        float mm = red_s[0];
-        for (int i = 1; i < D / 32; ++i)
-            mm = fmaxf(mm, red_s[i]);
-        M_s = mm;
-    }
-    __syncthreads();
-    M = M_s;
-    float num = 0.f, den = 0.f;
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, off);
+            v = is_max ? fmaxf(v, o) : v + o;
+        }
+        __syncthreads(); // red_s / bc_s free from the previous use
+        if (lane == 0)
+            red_s[warp] = v;
+        __syncthreads();
+        if (tid == 0) {
+            float r = red_s[0];
+            for (int i = 1; i < NW; ++i)
+                r = is_max ? fmaxf(r, red_s[i]) : r + red_s[i];
+            bc_s = r;
+        }
+        __syncthreads();
+        return bc_s;
+    };
+    float M = -INFINITY;
+    for (int q = tid; q < np; q += NT)
+        M = fmaxf(M, p.ws_ml[(row0 + q) * 2]);
+    M = block_reduce(M, true);
+    float den = 0.f; // this thread's share of sum_p w_p l_p
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     for (int q0 = 0; q0 < np; q0 += kReduceChunk) {
         const int nq = min(kReduceChunk, np - q0);
         __syncthreads();
-        for (int q = d; q < nq; q += D)
-            w_s[q] = ex2(p.ws_ml[(row0 + q0 + q) * 2] - M);
+        for (int q = tid; q < nq; q += NT) {
+            const float w = ex2(p.ws_ml[(row0 + q0 + q) * 2] - M);
+            w_s[q] = w;
+            den = fmaf(w, p.ws_ml[(row0 + q0 + q) * 2 + 1], den);
+        }
         __syncthreads();
-        for (int q = 0; q < nq; ++q)
-            den = fmaf(w_s[q], p.ws_ml[(row0 + q0 + q) * 2 + 1], den);
-#pragma unroll 8
-        for (int q = 0; q < nq; ++q)
-            num = fmaf(w_s[q], p.ws_o[(row0 + q0 + q) * D + d], num);
+        const float *o = p.ws_o + (row0 + q0) * D + d;
+        int q = g;
+#pragma unroll 2
+        for (; q + 3 * GR < nq; q += 4 * GR) {
+            a0 = fmaf(w_s[q], o[(size_t)q * D], a0);
+            a1 = fmaf(w_s[q + GR], o[(size_t)(q + GR) * D], a1);
+            a2 = fmaf(w_s[q + 2 * GR], o[(size_t)(q + 2 * GR) * D], a2);
+            a3 = fmaf(w_s[q + 3 * GR], o[(size_t)(q + 3 * GR) * D], a3);
+        }
+        for (; q < nq; q += GR)
+            a0 = fmaf(w_s[q], o[(size_t)q * D], a0);
     }
-    out[d] = Elem<T>::from(num / den);
-    if (p.lse && d == 0)
-        p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
+    den = block_reduce(den, false);
+    float num = (a0 + a1) + (a2 + a3);
+    if (GR > 1) {
+        if (g > 0)
+            num_s[g - 1][d] = num;
+        __syncthreads();
+        if (g == 0)
+            for (int i = 0; i < GR - 1; ++i)
+                num += num_s[i][d];
+    }
+    if (g == 0) {
+        out[d] = Elem<T>::from(num / den);
+        if (p.lse && d == 0)
+            p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
+    }
 }
 
 // Launch helper shared by the instantiation units.
