@@ -128,6 +128,18 @@ def test_partition_size_invariance(pa):
         assert diff <= 2e-2, (P, diff)
 
 
+def test_reduce_many_partitions(pa):
+    """More partitions per row than one shared-memory chunk of merge weights
+    holds (625 and 514 of 64 tokens: the reduce walks two chunks, with thread
+    groups splitting the partitions unevenly), beside a one-partition
+    sequence and one that ends just past a partition boundary."""
+    w = wl.make("gqa8b", device="cuda", poison=True,
+                lengths=[40000, 64 * 513 + 7, 5, 33001], seed=12)
+    ref = oracle_decode(w)
+    out = _decode(pa, w, True, partition_size=64)
+    check_attention(out, ref, what="hundreds of partitions")
+
+
 @pytest.mark.parametrize("split", [False, True])
 def test_deterministic_and_batch_invariant(pa, split):
     """Same inputs give identical bits; a sequence's output does not depend on
