@@ -725,6 +725,7 @@ __global__ void __launch_bounds__(256)
                        const float *__restrict__ lse_parts, int nparts, int64_t rows,
                        int head_size)
 {
+    griddep_wait(); // launched as the dependent of the suffix decode
     const int vpr = head_size / 8;
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t row = idx / vpr;
@@ -777,6 +778,9 @@ __global__ void cascade_setup_kernel(const int32_t *__restrict__ block_tables,
                                      int32_t *__restrict__ suffix_lens,
                                      int32_t *__restrict__ suffix_tables, unsigned int *err)
 {
+    // The prefix pass that follows waits for this grid before it reads the
+    // metadata written here; it may get resident meanwhile.
+    griddep_launch_dependents();
     const int s = blockIdx.x;
     const int P = prefix_blocks * block_size;
     const int32_t *row = block_tables + (size_t)s * max_blocks;
@@ -1303,15 +1307,19 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     // 3. Merge the nsplit + 1 parts.
     const int64_t threads = (int64_t)rows * (head_size / 8);
     const unsigned grid = (unsigned)((threads + 255) / 256);
-    if (dtype == PA_BF16)
-        merge_parts_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            static_cast<__nv_bfloat16 *>(out), reinterpret_cast<const __nv_bfloat16 *>(parts),
-            lse_parts, nsplit + 1, (int64_t)rows, head_size);
-    else
-        merge_parts_kernel<__half><<<grid, 256, 0, s>>>(
-            static_cast<__half *>(out), reinterpret_cast<const __half *>(parts), lse_parts,
-            nsplit + 1, (int64_t)rows, head_size);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    const cudaError_t me =
+        dtype == PA_BF16
+            ? launch_after_previous(merge_parts_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
+                                    static_cast<__nv_bfloat16 *>(out),
+                                    reinterpret_cast<const __nv_bfloat16 *>(parts),
+                                    static_cast<const float *>(lse_parts), nsplit + 1,
+                                    (int64_t)rows, head_size)
+            : launch_after_previous(merge_parts_kernel<__half>, dim3(grid), dim3(256), 0, s,
+                                    static_cast<__half *>(out),
+                                    reinterpret_cast<const __half *>(parts),
+                                    static_cast<const float *>(lse_parts), nsplit + 1,
+                                    (int64_t)rows, head_size);
+    return me == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_validate_tables(const int32_t *block_tables, const int32_t *seq_lens,

@@ -141,6 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
+    // Launched as the dependent of the kernel before it (which may write the
+    // request metadata, q or the pool): wait for it before reading anything.
+    griddep_wait();
     // ---- this CTA's rows: request r, query head h, query rows i0 .. i0+255
     // Grid: x = query head (or head pair), y = request, z = query block
     // counted from the request's last one (times the key chunks).  CTAs start
@@ -226,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = m->tmem_base;
+    griddep_launch_dependents();
 
     if (warp == kProducerWarp) {
         // ================================================================ producer
@@ -551,8 +555,7 @@ cudaError_t launch_one(const CUtensorMap &pool, const CUtensorMap &qmap, const P
             return e;
         __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<grid, kThreads, kSmem, stream>>>(pool, qmap, p);
-    return cudaGetLastError();
+    return launch_after_previous(kern, grid, dim3(kThreads), (size_t)kSmem, stream, pool, qmap, p);
 }
 
 template <typename T>
