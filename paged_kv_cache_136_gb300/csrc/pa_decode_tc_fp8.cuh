@@ -23,8 +23,9 @@
 // own score columns, and each softmax thread takes one row of each -- so a
 // stage moves the same 64 KB as the 16-bit kernel's and the per-stage
 // hand-offs are paid once per 64 KB.  The values MMA contracts over all 256
-// rows (K = 256); its P operand has one buffer, reused once the previous
-// stage's values MMA has completed.
+// rows (K = 256); its P operand is written over the stage's own K, which is
+// dead once the scores MMA has run, so no stage waits for another's values
+// MMA to release a P buffer.
 #pragma once
 
 #include <cuda_bf16.h>
