@@ -15,22 +15,29 @@
 // threads:
 //
 //   warp 8 (producer)  TMA-loads the two query tiles once, then K and V tiles
-//                      of 128 keys into a ring of shared-memory slots, one
+//                      of TN keys into a ring of shared-memory slots, one
 //                      box {64 elements, 1 kv head, block_size rows} per lane
 //                      and block ("Paged attention", k4i.top, section "block
 //                      table": physical_block = block_table[t // block_size]).
 //   warps 9, 10 (MMA)  one per query tile t (warp 9 owns the 512 TMEM
 //                      columns); per key tile k they issue
-//                        S_t = Q_t K_k^T          (M=128, N=128, K=head_size)
-//                        O_t (+)= P_t V_k         (M=128, N=head_size, K=128)
+//                        S_t = Q_t K_k^T          (M=128, N=TN, K=head_size)
+//                        O_t (+)= P_t V_k         (M=128, N=head_size, K=TN)
 //                      with P_t read from tensor memory (A operand) and V_k as
 //                      an MN-major shared-memory operand.
 //   warps 0-3 / 4-7    one query row per thread (TMEM lane): scale and mask
-//   (softmax, tile 0/1) the row's 128 scores, row max, base-2 exponentials,
+//   (softmax, tile 0/1) the row's TN scores, row max, base-2 exponentials,
 //                      write P over S as 16-bit values (bf16: a high part in
-//                      columns 0-63 and the rounded remainder in 64-127, so P
-//                      keeps ~16 significant bits), and at the end
+//                      the buffer's first TN/2 columns and the rounded
+//                      remainder after them, so P keeps ~16 significant
+//                      bits), and at the end
 //                      out = O / l (and the log-sum-exp when asked).
+//
+// Key tiles: fp16 uses TN = 128 keys and one score buffer per query tile, so
+// a tile's next scores MMA waits for its values MMA (P lies over S).  bf16
+// carries P as two parts (twice the values MMAs) and uses TN = 64 with two
+// score buffers: the next tile's scores are computed into the other buffer
+// while this tile's softmax runs.
 //
 // The running maximum is updated lazily: O and l are rescaled only when a key
 // tile raises a row's maximum by more than 2^8, so most tiles skip the rescale
@@ -54,33 +61,45 @@ constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;               // warps 9 and 10: MMA issuers of query tiles 0 and 1
 constexpr int kTileM = 128;         // query rows per tile
-constexpr int kTileN = 128;         // keys per K/V tile
 constexpr int kRowsPerCta = 2 * kTileM;
 constexpr float kRescaleLog2 = 8.f; // lazy-rescale threshold, log2 units
-constexpr uint32_t kTmemCols = 512; // S0, S1, O0, O1: 128 columns each
-constexpr int kRegion = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+// Tensor memory: tile t's score columns t*128 .. t*128+127 (one buffer of 128
+// keys, or two of 64 keys at t*128 and t*128 + 64; P is written over the
+// scores it came from), O_t at 256 + t*128.
+constexpr uint32_t kTmemCols = 512;
+constexpr int kQRegion = kTileM * 128;  // 128 query rows x 64 elements x 2 bytes
 
-template <int D>
+// Keys per K/V tile.  fp16: 128 keys and one score buffer, so the next tile's
+// scores wait for this tile's values MMA (P lies over S).  bf16 carries P as
+// two parts (twice the values MMAs): 64 keys and two score buffers, so the
+// next tile's scores are computed while this tile's softmax runs.
+template <typename T>
+constexpr int key_tile() { return std::is_same<T, __half>::value ? 128 : 64; }
+
+template <int D, int TN>
 struct Geo {
     static constexpr int kHalves = D / 64;
-    static constexpr int kTileBytes = kHalves * kRegion; // a Q, K or V tile
-    static constexpr int kSlots = D == 128 ? 4 : 8;      // K/V ring
-    static constexpr int kOffKV = 2 * kTileBytes;        // after the two Q tiles
-    static constexpr int kOffMisc = kOffKV + kSlots * kTileBytes;
+    static constexpr int kKVRegion = TN * 128;            // TN key rows x 64 elements x 2 bytes
+    static constexpr int kTileBytes = kHalves * kQRegion; // a Q tile
+    static constexpr int kKVBytes = kHalves * kKVRegion;  // a K or V tile
+    static constexpr int kSlots = kKVBytes >= 32768 ? 4 : 8; // K/V ring of 128 KB (64 KB for D 64)
+    static constexpr int kOffKV = 2 * kTileBytes;         // after the two Q tiles
+    static constexpr int kOffMisc = kOffKV + kSlots * kKVBytes;
 };
 
 struct Misc {
     uint64_t q_full;
     uint64_t kv_full[8], kv_empty[8];
-    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t s_full[2][2], p_full[2][2]; // [query tile][score buffer]
+    uint64_t pv_done[2], o_done[2];      // a values MMA / the last one of a tile done
     uint64_t drain[2];
     uint32_t tmem_base;
 };
 
-template <int D>
+template <int D, int TN>
 constexpr int smem_bytes()
 {
-    return 1024 + Geo<D>::kOffMisc + (int)sizeof(Misc);
+    return 1024 + Geo<D, TN>::kOffMisc + (int)sizeof(Misc);
 }
 
 template <typename T>
@@ -120,9 +139,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap pool_map,
                       const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
 {
-    using Gm = Geo<D>;
+    constexpr int kTileN = key_tile<T>();
+    constexpr int NB = kTileN == 64 ? 2 : 1;     // score buffers per query tile
+    constexpr int kChunkUnit = 128 / kTileN;     // key-split chunks come in units of 128 keys
+    using Gm = Geo<D, kTileN>;
+    constexpr int kKVRegion = Gm::kKVRegion;
     constexpr int NH = Gm::kHalves;
     constexpr int TB = Gm::kTileBytes;
+    constexpr int KB = Gm::kKVBytes;
     constexpr int S = Gm::kSlots;
     constexpr int BPT = kTileN / BS; // pool blocks per key tile
     static_assert(32 % BPT == 0 && BPT * NH <= 32, "key tile geometry");
@@ -178,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i0 = qb * rows_cta;
     const int ctx = L - q_len;
     // Keys of this CTA: [kt0 * 128, key_hi) (the whole request unless split).
-    const int kt0 = csplit * p.chunk_tiles;
-    const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles) * kTileN) : L;
+    const int kt0 = csplit * p.chunk_tiles * kChunkUnit;
+    const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles * kChunkUnit) * kTileN) : L;
     T *const out_base = reinterpret_cast<T *>(p.out) + (size_t)csplit * (size_t)p.part_stride;
     float *const lse_base = p.lse ? p.lse + (size_t)csplit * (size_t)p.lse_part_stride : nullptr;
     int nv[2], nt[2];
@@ -213,8 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&m->kv_empty[i], 2); // one arrival per MMA issuer warp
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&m->s_full[i], 1);
-            mbar_init(&m->p_full[i], 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&m->s_full[i][b], 1);
+                mbar_init(&m->p_full[i][b], 4);
+            }
+            mbar_init(&m->pv_done[i], 1);
             mbar_init(&m->o_done[i], 1);
         }
         mbar_init(&m->drain[0], 1);
@@ -243,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nv[t] > 0)
 #pragma unroll
                     for (int hf = 0; hf < NH; ++hf)
-                        tma_load_3d(smem + t * TB + hf * kRegion, &q_map, &m->q_full, hf * 64,
+                        tma_load_3d(smem + t * TB + hf * kQRegion, &q_map, &m->q_full, hf * 64,
                                     thead(t), q0 + i0 + toff(t));
         }
         // Block-table entries of 64 blocks live in lane registers (this
@@ -280,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     row = phys * BS;
                 }
-                tma_load_4d(smem + Gm::kOffKV + slot * TB + hf * kRegion + c * BS * 128,
+                tma_load_4d(smem + Gm::kOffKV + slot * KB + hf * kKVRegion + c * BS * 128,
                             &pool_map, &m->kv_full[slot], hf * 64, kvh, row, plane);
             }
         }
@@ -292,28 +319,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // or a plain arrive when its tile does not need that key tile.
         const int t = warp - kMmaWarp;
         const int ntt = nt[t];
-        auto issue_qk = [&](int slot) {
+        // S_t[buffer] = Q_t K^T into one of the tile's two score buffers.
+        auto issue_qk = [&](int slot, int buf) {
             const uint32_t qa = smem_addr(smem + t * TB);
-            const uint32_t ka = smem_addr(smem + Gm::kOffKV + slot * TB);
+            const uint32_t ka = smem_addr(smem + Gm::kOffKV + slot * KB);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32);
-                umma_f16(tmem + (uint32_t)(t * 128), smem_desc_sw128(qa + off, 16, 1024),
-                         smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                const uint32_t qoff = (uint32_t)((kk >> 2) * kQRegion + (kk & 3) * 32);
+                const uint32_t koff = (uint32_t)((kk >> 2) * kKVRegion + (kk & 3) * 32);
+                umma_f16(tmem + (uint32_t)(t * 128 + buf * kTileN), smem_desc_sw128(qa + qoff, 16, 1024),
+                         smem_desc_sw128(ka + koff, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
             }
-            umma_commit(&m->s_full[t]);
+            umma_commit(&m->s_full[t][buf]);
         };
-        auto issue_pv = [&](int slot, bool acc) {
-            const uint32_t va = smem_addr(smem + Gm::kOffKV + slot * TB);
+        // O_t (+)= P_t V with P read from the score buffer it was written over.
+        auto issue_pv = [&](int slot, int buf, bool acc) {
+            const uint32_t va = smem_addr(smem + Gm::kOffKV + slot * KB);
+            const uint32_t pa = tmem + (uint32_t)(t * 128 + buf * kTileN);
 #pragma unroll
             for (int kk = 0; kk < kTileN / 16; ++kk) {
-                const uint64_t vd = smem_desc_sw128(va + kk * 2048, kRegion, 1024);
-                umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128), tmem + (uint32_t)(t * 128 + kk * 8),
-                                vd, kIdescO, (acc || kk > 0) ? 1u : 0u);
-                if (kSplitP) // the low parts of P, 64 columns further on
+                const uint64_t vd = smem_desc_sw128(va + kk * 2048, kKVRegion, 1024);
+                umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128), pa + (uint32_t)(kk * 8), vd, kIdescO,
+                                (acc || kk > 0) ? 1u : 0u);
+                if (kSplitP) // the low parts of P, kTileN / 2 columns further on
                     umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128),
-                                    tmem + (uint32_t)(t * 128 + 64 + kk * 8), vd, kIdescO, 1u);
+                                    pa + (uint32_t)(kTileN / 2 + kk * 8), vd, kIdescO, 1u);
             }
+            if (NB == 2)
+                umma_commit(&m->pv_done[t]);
         };
         // release a slot: commit after this warp's MMAs, or arrive at once
         auto release = [&](int slot, bool used) {
@@ -327,44 +360,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             if (lane == 0) {
                 if (ntt > 0)
-                    issue_qk(0);
+                    issue_qk(0, 0);
                 release(0, ntt > 0);
             }
             __syncwarp();
         }
-        // Each slot use is released only after its load has landed, so a warp
-        // whose tile needs no more keys still follows the producer one use
-        // at a time (two releases can never fall into one barrier phase).
+        // Per key tile k.  Two score buffers: first the scores of tile k+1 into
+        // the other buffer (its previous contents, P of tile k-1, were read by
+        // the values MMA issued before, and MMAs run in issue order), so they
+        // are computed while the softmax of tile k runs; then the values of
+        // tile k once its P is written.  One buffer: the values of tile k, then
+        // the scores of tile k+1 over its P.  Each slot use is released only
+        // after its load has landed, so a warp whose tile needs no more keys
+        // still follows the producer one use at a time (two releases can
+        // never fall into one barrier phase).
         for (int k = 0; ok && k < n; ++k) {
             const int gv = 2 * k + 1, sv = gv % S;
             const int gk = 2 * k + 2, sk = gk % S;
             const bool use = k < ntt, next = k + 1 < n, nuse = k + 1 < ntt;
+            if constexpr (NB == 2) {
+                if (next) {
+                    ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    if (lane == 0) {
+                        if (nuse)
+                            issue_qk(sk, (k + 1) & 1);
+                        release(sk, nuse);
+                    }
+                    __syncwarp();
+                }
+            }
             ok = warp_wait(&m->kv_full[sv], (gv / S) & 1, lane);
             if (ok && use) {
                 // The last tile's rows past seq_len are zeroed by one softmax
                 // warpgroup before it hands over its P.
+                const int kb = k % NB, kph = (k / NB) & 1;
                 if (tail && k == n - 1)
-                    ok = warp_wait(&m->p_full[fixer], k & 1, lane);
+                    ok = warp_wait(&m->p_full[fixer][kb], kph, lane);
                 if (ok)
-                    ok = warp_wait(&m->p_full[t], k & 1, lane);
+                    ok = warp_wait(&m->p_full[t][kb], kph, lane);
                 if (ok) {
                     tc_fence_after_sync();
                     if (lane == 0)
-                        issue_pv(sv, k > 0);
+                        issue_pv(sv, kb, k > 0);
                 }
             }
-            if (ok && next)
-                ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
+            if constexpr (NB == 1) {
+                if (ok && next)
+                    ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
+            }
             if (!ok)
                 break;
             tc_fence_after_sync();
             if (lane == 0) {
-                if (nuse)
-                    issue_qk(sk);
-                else if (use)
+                if (NB == 1 && nuse)
+                    issue_qk(sk, 0);
+                else if (use && !nuse)
                     umma_commit(&m->o_done[t]); // the tile's last values MMA
                 release(sv, use);
-                if (next)
+                if (NB == 1 && next)
                     release(sk, nuse);
             }
             __syncwarp();
@@ -391,15 +447,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             for (int k = 0; k < ntt; ++k) {
-                ok = warp_wait(&m->s_full[wg], k & 1, lane);
+                const int buf = k % NB;
+                const uint32_t sb = s_addr + (uint32_t)(buf * kTileN); // this tile's score buffer
+                ok = warp_wait(&m->s_full[wg][buf], (k / NB) & 1, lane);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                // The row's 128 raw scores (bits).
+                // The row's kTileN raw scores (bits).
                 uint32_t sv[kTileN];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld32_nowait(s_addr + (uint32_t)(c * 32),
+                for (int c = 0; c < kTileN / 32; ++c)
+                    tmem_ld32_nowait(sb + (uint32_t)(c * 32),
                                      *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
                 tmem_wait_ld();
                 // Row max over the raw scores (scale > 0 commutes with max),
@@ -429,12 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     need = true;
                 }
                 // p = 2^(S * scale*log2e - m): one packed FFMA per two keys and
-                // one ex2 per key; the row sum in two packed chains.
+                // one ex2 per key; the row sum in two packed chains.  P goes
+                // over the scores it came from (bf16: high parts in the first
+                // kTileN / 2 columns of the buffer, rounded remainders after).
                 const float nmu = m_used == -INFINITY ? 0.f : -m_used;
                 const float2 qs2 = make_float2(qs, qs), nmu2 = make_float2(nmu, nmu);
                 float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kTileN / 32; ++c) {
                     uint32_t pk[16], lo[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -450,15 +510,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             lo[j] = pack2<T>(pp.x - h0, pp.y - h1);
                         }
                     }
-                    tmem_st16(s_addr + (uint32_t)(c * 16), pk);
+                    tmem_st16(sb + (uint32_t)(c * 16), pk);
                     if (kSplitP)
-                        tmem_st16(s_addr + (uint32_t)(64 + c * 16), lo);
+                        tmem_st16(sb + (uint32_t)(kTileN / 2 + c * 16), lo);
                 }
                 l += (l2[0].x + l2[1].x) + (l2[0].y + l2[1].y);
                 if (__any_sync(0xffffffffu, need)) {
-                    // O holds the values of key tiles 0..k-1 (their MMAs are
-                    // complete: S_k was committed after them).  Done after P
+                    // O must hold the values of key tiles 0..k-1.  With two
+                    // score buffers the values MMA of tile k-1 may still run
+                    // (the next scores were issued before it), so wait for
+                    // it; with one, S_k was committed after it.  Done after P
                     // is written so the scores' registers are free.
+                    if (NB == 2 && !warp_wait(&m->pv_done[wg], (k - 1) & 1, lane))
+                        ok = false;
+                    tc_fence_after_sync();
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
@@ -472,16 +537,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 if (tail && wg == fixer && k == n - 1) {
-                    // Zero the V rows of keys >= seq_len in the last tile.
+                    // Zero the V rows of keys >= seq_len in the last tile (one
+                    // thread per key row).
                     const int gv = 2 * k + 1;
-                    ok = warp_wait(&m->kv_full[gv % S], (gv / S) & 1, lane);
-                    if (ok && (kt0 + k) * kTileN + row >= L) {
-                        uint8_t *vrow = smem + Gm::kOffKV + (gv % S) * TB + row * 128;
+                    if (!warp_wait(&m->kv_full[gv % S], (gv / S) & 1, lane))
+                        ok = false;
+                    if (ok && row < kTileN && (kt0 + k) * kTileN + row >= L) {
+                        uint8_t *vrow = smem + Gm::kOffKV + (gv % S) * KB + row * 128;
 #pragma unroll
                         for (int hf = 0; hf < NH; ++hf)
 #pragma unroll
                             for (int c = 0; c < 8; ++c)
-                                *reinterpret_cast<uint4 *>(vrow + hf * kRegion + c * 16) =
+                                *reinterpret_cast<uint4 *>(vrow + hf * kKVRegion + c * 16) =
                                     make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
@@ -489,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&m->p_full[wg]);
+                    mbar_arrive(&m->p_full[wg][buf]);
                 if (!ok)
                     break;
             }
@@ -542,7 +609,7 @@ cudaError_t launch_one(const CUtensorMap &pool, const CUtensorMap &qmap, const P
                        dim3 grid, cudaStream_t stream)
 {
     auto kern = prefill_tc_kernel<T, D, BS>;
-    constexpr int kSmem = smem_bytes<D>();
+    constexpr int kSmem = smem_bytes<D, key_tile<T>()>();
     static unsigned long long done_mask = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
