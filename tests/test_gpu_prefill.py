@@ -41,6 +41,8 @@ SHAPES = [
     ([300, 17], [1000, 0], 4, 1, 128, 16, torch.bfloat16),
     ([1, 20, 37, 130], [0, 5, 0, 70], 4, 4, 64, 16, torch.float16),
     ([200, 511], [64, 0], 2, 2, 64, 32, torch.bfloat16),
+    ([33, 190], [70, 0], 4, 2, 64, 16, torch.bfloat16),
+    ([150, 3], [40, 260], 4, 2, 128, 32, torch.float16),
     # at most 128 query rows and an even group: a CTA's tiles are two heads
     ([100, 7, 128], [50, 300, 0], 8, 2, 128, 16, torch.bfloat16),
     ([1, 64], [10, 0], 16, 2, 64, 32, torch.float16),
