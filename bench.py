@@ -372,9 +372,9 @@ def run_ours(args) -> dict | None:
     e2e_steps = max(1, min(K, args.e2e_steps))
 
     def e2e_body():
-        dev_buf[:h2d_len].copy_(host_buf[:h2d_len], non_blocking=True)
+        pa.pa_stage_copy(dev_buf[:h2d_len], host_buf[:h2d_len])
         step()
-        out_h.copy_(out, non_blocking=True)
+        pa.pa_stage_copy(out_h, out)
 
     for _ in range(3):
         e2e_body()
@@ -442,7 +442,8 @@ def run_ours(args) -> dict | None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "method": ("CUDA graph of the API calls" if graph is not None else "eager API calls")
                           + ": one pinned staging copy in, cache write + decode, result copy"
-                            " out, host waits every step"},
+                            " out (both copies on the SMs, pa_stage_copy), host waits every"
+                            " step"},
         "gpu_launches": K * (1 + decode_launches(w, split, P)),
         "clocks": clk,
         "device_error_flags": flags,

@@ -12,6 +12,8 @@
  *   pa_merge_attn_states  merge two partial attention results
  *   pa_cascade_decode     decode for sequences sharing a prefix (cascade)
  *   pa_*_fp8              the cache write and decode with an FP8 (e4m3) pool
+ *   pa_stage_copy         move a step's data between pinned host memory and
+ *                         the device on the SMs
  *
  * Data layout (all tensors contiguous, row-major, caller-owned):
  *
@@ -347,6 +349,21 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
  *                  are skipped and flagged (PA_DEVERR_BLOCK_ID).
  * num_pairs == 0 is a no-op; num_pairs <= 65535.
  */
+/*
+ * Copy bytes from src to dst on the GPU's SMs (16-byte moves), stream-
+ * ordered on stream.  Either pointer may be device memory or pinned host
+ * memory with a device mapping (page-locked by the CUDA runtime, for example
+ * through cudaHostAlloc); the SMs then read or write the host memory directly
+ * over the host link, which for the few MB of a decode step's inputs and
+ * outputs is faster than a copy-engine transfer.  Pointers without a device
+ * mapping, or not 16-byte aligned, or a size that is not a multiple of 16,
+ * are handed to cudaMemcpyAsync (cudaMemcpyDefault) instead.  The pages have
+ * no counterpart of this call: it stages a step's data.
+ * Errors: PA_ERR_INVALID_ARG for a null pointer with bytes > 0; PA_ERR_CUDA
+ * for a failed launch or copy.
+ */
+pa_status pa_stage_copy(void *dst, const void *src, size_t bytes, void *stream);
+
 pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
                          int num_blocks, int block_size, int num_kv_heads, int head_size,
                          pa_dtype dtype, void *stream);

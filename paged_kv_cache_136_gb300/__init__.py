@@ -65,6 +65,8 @@ _lib.pa_device_errors.argtypes = [ctypes.POINTER(_U), _I]
 _lib.pa_decode_splitk_lse.restype = _I
 _lib.pa_decode_splitk_lse.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                       _I, _I, _I, _P, _SZ, _P]
+_lib.pa_stage_copy.restype = _I
+_lib.pa_stage_copy.argtypes = [_P, _P, _SZ, _P]
 _lib.pa_merge_attn_states.restype = _I
 _lib.pa_merge_attn_states.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]
 _lib.pa_cascade_decode_workspace_size.restype = _SZ
@@ -478,6 +480,22 @@ def pa_copy_blocks(kv_cache: torch.Tensor, block_mapping: torch.Tensor, block_si
     _check(_lib.pa_copy_blocks(_dev(kv_cache, "kv_cache"), _dev(block_mapping, "block_mapping"),
                                n, nb, block_size, hkv, d, _DTYPE[kv_cache.dtype],
                                _stream(stream)), "pa_copy_blocks")
+
+
+def pa_stage_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Copy ``src`` into ``dst`` (same byte count, both contiguous) on the
+    GPU's SMs, stream-ordered.  Each side is a CUDA tensor or a pinned host
+    tensor, which the SMs read or write directly through its device mapping."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src must hold the same number of bytes")
+    _check(_lib.pa_stage_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()),
+                              nbytes, _stream(stream)), "pa_stage_copy")
 
 
 def pa_validate_block_mapping(block_mapping: torch.Tensor, num_blocks: int) -> int:

@@ -1364,6 +1364,57 @@ pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int blo
     return PA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Staging copy on the SMs: 16-byte moves over a grid of a few CTAs per SM.
+// Either side may be pinned host memory, which the SMs reach through its
+// device mapping over the host link; for the few MB of a decode step's inputs
+// and outputs that is faster than a copy-engine transfer.  Pointers that have
+// no device mapping, or are not 16-byte aligned, go to cudaMemcpyAsync.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    stage_copy_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, size_t n16)
+{
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+// The address under which the device reaches p, or null when it has none.
+static const void *device_view(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+        a.type == cudaMemoryTypeHost)
+        return a.devicePointer;
+    return nullptr;
+}
+
+pa_status pa_stage_copy(void *dst, const void *src, size_t bytes, void *stream)
+{
+    if (bytes == 0)
+        return PA_OK;
+    if (!dst || !src)
+        return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *dd = const_cast<void *>(device_view(dst));
+    const void *ds = device_view(src);
+    cudaError_t e;
+    const int sms = (dd && ds) ? sm_count(&e) : 0;
+    if (!dd || !ds || !sms || !aligned(dd, 16) || !aligned(ds, 16) || bytes % 16)
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s) == cudaSuccess ? PA_OK
+                                                                                : PA_ERR_CUDA;
+    const size_t n16 = bytes / 16;
+    const size_t want = (n16 + 255) / 256;
+    const unsigned grid = (unsigned)(want < (size_t)(4 * sms) ? want : (size_t)(4 * sms));
+    stage_copy_kernel<<<grid, 256, 0, s>>>(static_cast<uint4 *>(dd), static_cast<const uint4 *>(ds),
+                                           n16);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
                          int num_blocks, int block_size, int num_kv_heads, int head_size,
                          pa_dtype dtype, void *stream)

@@ -238,3 +238,30 @@ def test_copy_on_write_step_on_gpu(pa):
     torch.cuda.synchronize()
     check_attention(out, oracle_decode(w), what="copy-on-write step")
     assert torch.equal(out[0].view(torch.int16), out[2].view(torch.int16))
+
+
+def test_stage_copy_bit_exact(pa):
+    """Pinned host -> device, device -> pinned host and device -> device on the
+    SMs, and the stream-copy fallback for a size that is not a multiple of 16
+    and for a misaligned start, all bit-exact."""
+    g = torch.Generator().manual_seed(21)
+    n = 1606400
+    src_h = torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).pin_memory()
+    dev = torch.empty(n, dtype=torch.uint8, device="cuda")
+    pa.pa_stage_copy(dev, src_h)
+    back = torch.empty(n, dtype=torch.uint8).pin_memory()
+    pa.pa_stage_copy(back, dev)
+    dev2 = torch.empty(n, dtype=torch.uint8, device="cuda")
+    pa.pa_stage_copy(dev2, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src_h)
+    assert torch.equal(dev2.cpu(), src_h)
+    # 1000 bytes (not a multiple of 16), and a start one byte past alignment
+    odd = torch.empty(1000, dtype=torch.uint8, device="cuda")
+    pa.pa_stage_copy(odd, src_h[:1000])
+    mis = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    pa.pa_stage_copy(mis, src_h[1:4097])
+    torch.cuda.synchronize()
+    assert torch.equal(odd.cpu(), src_h[:1000])
+    assert torch.equal(mis.cpu(), src_h[1:4097])
+    assert pa.pa_device_errors(clear=True) == 0
