@@ -1374,6 +1374,11 @@ pa_status pa_validate_slots(const int64_t *slot_mapping, int num_tokens, int blo
 __global__ void __launch_bounds__(256)
     stage_copy_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, size_t n16)
 {
+    // Launched as the dependent of the kernel before it (which may write src
+    // or read dst): wait for it, then let the next kernel (the cache write of
+    // a step whose inputs this copies in) get resident while the copy runs.
+    griddep_wait();
+    griddep_launch_dependents();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
          i += (size_t)gridDim.x * blockDim.x)
         dst[i] = src[i];
@@ -1410,9 +1415,11 @@ pa_status pa_stage_copy(void *dst, const void *src, size_t bytes, void *stream)
     const size_t n16 = bytes / 16;
     const size_t want = (n16 + 255) / 256;
     const unsigned grid = (unsigned)(want < (size_t)(4 * sms) ? want : (size_t)(4 * sms));
-    stage_copy_kernel<<<grid, 256, 0, s>>>(static_cast<uint4 *>(dd), static_cast<const uint4 *>(ds),
-                                           n16);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_after_previous(stage_copy_kernel, dim3(grid), dim3(256), 0, s,
+                                 static_cast<uint4 *>(dd), static_cast<const uint4 *>(ds), n16) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
