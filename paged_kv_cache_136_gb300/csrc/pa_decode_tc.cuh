@@ -816,15 +816,31 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
             carry_s += warp_tot[nwarps - 1];
         __syncthreads();
     }
-    // Bucket start offsets after the full partitions (buckets in size order).
-    if (tid == 0) {
-        uint32_t acc = carry_s;
-        for (int b = 0; b < kPlanBuckets; ++b) {
-            const uint32_t c = bucket[b];
-            bucket[b] = acc;
-            acc += c;
+    // Bucket start offsets after the full partitions (buckets in size order):
+    // an exclusive scan of the counts over the first kPlanBuckets threads,
+    // one bucket each (the kernel is launched with 1024 threads).
+    static_assert(kPlanBuckets % 32 == 0 && kPlanBuckets <= 1024, "one bucket per thread");
+    uint32_t bc = 0, bi = 0; // this thread's bucket count, inclusive scan in its warp
+    if (tid < kPlanBuckets) {
+        bc = bucket[tid];
+        bi = bc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, bi, off);
+            if (lane >= off)
+                bi += y;
         }
-        hdr[1] = acc * (uint32_t)num_groups;
+        if (lane == 31)
+            warp_tot[warp] = bi;
+    }
+    __syncthreads();
+    if (tid < kPlanBuckets) {
+        uint32_t before = carry_s;
+        for (int w = 0; w < warp; ++w)
+            before += warp_tot[w];
+        bucket[tid] = before + bi - bc;
+        if (tid == kPlanBuckets - 1)
+            hdr[1] = (before + bi) * (uint32_t)num_groups;
     }
     __syncthreads();
     // Pass 2: place each last partition in its bucket.
