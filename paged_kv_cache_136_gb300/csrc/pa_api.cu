@@ -234,11 +234,14 @@ cudaError_t launch_decode(const DecodeKey &key, const CUtensorMap &tmap, const D
 template <typename T, int D>
 static cudaError_t launch_reduce_t(const ReduceParams &p, dim3 grid, cudaStream_t stream)
 {
+    // Rows of at most 32 partitions: one warp per row.
+    if (p.max_parts <= 32)
+        return launch_after_previous(
+            splitk_reduce_warp_kernel<T, D>,
+            dim3((grid.x + kReduceWarpHeads - 1) / kReduceWarpHeads, grid.y),
+            dim3(32 * kReduceWarpHeads), 0, stream, p);
     // Rows of many partitions: four thread groups split a row's partitions.
-    if (p.max_parts >= 32)
-        return launch_after_previous(splitk_reduce_kernel<T, D, 4>, grid, dim3(4 * D), 0, stream,
-                                     p);
-    return launch_after_previous(splitk_reduce_kernel<T, D, 1>, grid, dim3(D), 0, stream, p);
+    return launch_after_previous(splitk_reduce_kernel<T, D, 4>, grid, dim3(4 * D), 0, stream, p);
 }
 
 cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int num_seqs,

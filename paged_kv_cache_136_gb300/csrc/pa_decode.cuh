@@ -497,6 +497,73 @@ __global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParam
     }
 }
 
+// The same merge for rows of at most 32 partitions: one warp per
+// (sequence, query head), kReduceWarpHeads heads per CTA.  Lane q holds
+// partition q's (m_q, l_q), so M and sum_q w_q l_q are warp shuffles with no
+// block barrier, and lane j sums output columns j, j+32, ... over the
+// partitions (each load instruction of a warp reads 128 contiguous bytes).
+// All rows of a decode batch then fit on the GPU at once.
+constexpr int kReduceWarpHeads = 8;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kReduceWarpHeads)
+    splitk_reduce_warp_kernel(const ReduceParams p)
+{
+    constexpr int E = D / 32; // output columns per lane
+    griddep_wait();           // the partition kernel's states are complete
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.x * kReduceWarpHeads + (threadIdx.x >> 5);
+    const int s = blockIdx.y;
+    if (h >= p.num_heads)
+        return;
+    int L = p.seq_lens[s];
+    L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
+    const int np = (L + p.part_tokens - 1) / p.part_tokens;
+    const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
+    T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + h) * D;
+    if (np == 0) {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            out[lane + 32 * e] = Elem<T>::from(0.f);
+        if (p.lse && lane == 0)
+            p.lse[(size_t)s * p.num_heads + h] = -INFINITY;
+        return;
+    }
+    if (np == 1 && p.skip_single)
+        return;
+    float m = -INFINITY, l = 0.f;
+    if (lane < np) {
+        m = p.ws_ml[(row0 + lane) * 2];
+        l = p.ws_ml[(row0 + lane) * 2 + 1];
+    }
+    float M = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = lane < np ? ex2(m - M) : 0.f;
+    float den = w * l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        den += __shfl_xor_sync(0xffffffffu, den, off);
+    const float *o = p.ws_o + row0 * D + lane;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        acc[e] = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < np; ++q) {
+        const float wq = __shfl_sync(0xffffffffu, w, q);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            acc[e] = fmaf(wq, o[(size_t)q * D + 32 * e], acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        out[lane + 32 * e] = Elem<T>::from(acc[e] / den);
+    if (p.lse && lane == 0)
+        p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
+}
+
 // Launch helper shared by the instantiation units.
 template <typename T, int D, int BS, int G, bool SPLIT>
 cudaError_t launch_one(const CUtensorMap &tmap, const DecodeParams &p, dim3 grid,

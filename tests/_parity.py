@@ -40,6 +40,17 @@ def oracle_prefill(w, items=None, cache_bits=None, causal=True, block_tables=Non
                        items=items)
 
 
+def oracle_decode_lse(w: Workload, items=None) -> np.ndarray:
+    """Decode rows' natural-log softmax denominators from the oracle's
+    prefill with one query row per request (the decode step is that case)."""
+    B = w.num_seqs
+    _, lse = get_oracle().prefill(bits(w.q), bits(w.kv_cache), w.block_tables.cpu().numpy(),
+                                  w.seq_lens.cpu().numpy(), np.arange(B + 1, dtype=np.int32),
+                                  w.num_kv_heads, w.block_size, w.scale, ORACLE_DTYPE[w.dtype],
+                                  items=items)
+    return lse
+
+
 def check_lse(got: torch.Tensor, ref: np.ndarray, items=None, what: str = ""):
     """Log-sum-exps agree to 1e-3 absolute (the scores are fp32 dot products
     of 16-bit inputs; the log of the denominator is insensitive to P's

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import workload as wl
-from tests._parity import check_attention, check_lse, oracle_decode, splitk_workspace
+from tests._parity import (check_attention, check_lse, oracle_decode, oracle_decode_lse,
+                           splitk_workspace)
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -22,18 +23,6 @@ def pa():
     import paged_kv_cache_136_gb300 as pa
     pa.pa_device_errors(clear=True)
     return pa
-
-
-def _oracle_decode_lse(w, items=None):
-    """Decode rows' log-sum-exps from the oracle's prefill with one query row
-    per request (the decode step is that case)."""
-    from oracle.oracle import get
-    B = w.num_seqs
-    _, lse = get().prefill(wl.bits(w.q), wl.bits(w.kv_cache), w.block_tables.cpu().numpy(),
-                           w.seq_lens.cpu().numpy(), np.arange(B + 1, dtype=np.int32),
-                           w.num_kv_heads, w.block_size, w.scale, wl.ORACLE_DTYPE[w.dtype],
-                           items=items)
-    return lse
 
 
 # ---------------------------------------------------------------------------
@@ -101,7 +90,7 @@ def test_decode_splitk_lse(pa, name, part):
     L = w.seq_lens.cpu().numpy()
     keep = np.repeat(L > 0, w.num_heads)
     items = np.nonzero(keep)[0]
-    ref = _oracle_decode_lse(w, items=items)
+    ref = oracle_decode_lse(w, items=items)
     check_lse(lse, ref, items=items, what=f"{name} lse")
     if name != "tiny":
         assert torch.all(lse[3] == -float("inf"))
@@ -113,8 +102,7 @@ def test_decode_splitk_lse_simt_family(pa):
         "import torch, numpy as np, workload as wl\n"
         "import paged_kv_cache_136_gb300 as pa\n"
         "from tests._parity import splitk_workspace\n"
-        "from tests.test_gpu_cascade import _oracle_decode_lse\n"
-        "from tests._parity import check_lse\n"
+        "from tests._parity import check_lse, oracle_decode_lse\n"
         "w = wl.make('gqa8b', device='cuda', poison=True, num_seqs=12, seed=33)\n"
         "msl = int(w.seq_lens.max()); ws = splitk_workspace(pa, w, msl, 128)\n"
         "out = torch.empty_like(w.q)\n"
@@ -122,7 +110,7 @@ def test_decode_splitk_lse_simt_family(pa):
         "pa.pa_decode_splitk_lse(out, lse, w.q, w.kv_cache, w.block_tables, w.seq_lens,\n"
         "                        w.scale, w.block_size, msl, ws, 128)\n"
         "torch.cuda.synchronize()\n"
-        "check_lse(lse, _oracle_decode_lse(w), what='simt lse')\n"
+        "check_lse(lse, oracle_decode_lse(w), what='simt lse')\n"
         "print('ok')\n")
     env = dict(os.environ, PA_DECODE_KERNEL="simt")
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,

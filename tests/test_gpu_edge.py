@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import workload as wl
-from tests._parity import check_attention, oracle_decode, splitk_workspace
+from tests._parity import (check_attention, check_lse, oracle_decode, oracle_decode_lse,
+                           splitk_workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -138,6 +139,27 @@ def test_reduce_many_partitions(pa):
     ref = oracle_decode(w)
     out = _decode(pa, w, True, partition_size=64)
     check_attention(out, ref, what="hundreds of partitions")
+
+
+@pytest.mark.parametrize("max_parts", [32, 33])
+def test_reduce_partition_count_boundary(pa, max_parts):
+    """Rows of up to 32 partitions are merged one warp per row, longer ones by
+    the thread-group reduce: both sides of the switch, with rows of 1, 2, 31
+    and the maximum number of 64-token partitions, a head count that is not a
+    multiple of the heads one reduce CTA takes, and the log-sum-exp output."""
+    P = 64
+    lens = [P * max_parts, P * 30 + 1, P, P + 1, P * max_parts - 5]
+    w = wl.make("gqa8b", device="cuda", poison=True, lengths=lens, num_heads=12,
+                num_kv_heads=6, seed=40 + max_parts)
+    msl = P * max_parts
+    ws = splitk_workspace(pa, w, msl, P)
+    out = torch.empty_like(w.q)
+    lse = torch.empty((w.num_seqs, w.num_heads), dtype=torch.float32, device="cuda")
+    pa.pa_decode_splitk_lse(out, lse, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                            w.block_size, msl, ws, P)
+    check_attention(out, oracle_decode(w), what=f"max_parts={max_parts}")
+    check_lse(lse, oracle_decode_lse(w), what=f"max_parts={max_parts}")
+    assert pa.pa_device_errors(clear=True) == 0
 
 
 @pytest.mark.parametrize("split", [False, True])
