@@ -357,8 +357,9 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
  * over the host link, which for the few MB of a decode step's inputs and
  * outputs is faster than a copy-engine transfer.  Pointers without a device
  * mapping, or not 16-byte aligned, or a size that is not a multiple of 16,
- * are handed to cudaMemcpyAsync (cudaMemcpyDefault) instead.  The pages have
- * no counterpart of this call: it stages a step's data.
+ * are handed to cudaMemcpyAsync (cudaMemcpyDefault) instead.  src and dst
+ * must not overlap; both stay owned by the caller.  The pages have no
+ * counterpart of this call: it stages a step's data.
  * Errors: PA_ERR_INVALID_ARG for a null pointer with bytes > 0; PA_ERR_CUDA
  * for a failed launch or copy.
  */
