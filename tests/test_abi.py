@@ -261,3 +261,22 @@ def test_fp8_calls_reject_bad_arguments(pa):
                   [ctypes.c_int, ctypes.c_void_p])
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 64, 16, 8, 4, 0.1, 1.0, 1.0, 0, None) == 2
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 2, 128, 16, 8, 4, 0.1, 0.0, 1.0, 0, None) == 1
+
+
+def test_stage_copy_rejects_bad_arguments(pa):
+    """A zero-byte copy is a no-op whatever the pointers; a null pointer with
+    bytes to move is rejected before any CUDA call.  The binding refuses
+    pageable host tensors (the SMs cannot reach them) and strided views."""
+    import torch
+    lib = _raw(pa)
+    f = lib.pa_stage_copy
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert f(None, None, 0, None) == 0
+    assert f(None, FAKE, 16, None) == 1
+    assert f(FAKE, None, 16, None) == 1
+    host = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor or pinned"):
+        pa.pa_stage_copy(host, host)
+    with pytest.raises(ValueError, match="contiguous"):
+        pa.pa_stage_copy(torch.zeros(128, dtype=torch.uint8)[::2], host)
