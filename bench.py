@@ -6,14 +6,17 @@ KV bytes per step = sum_s seq_len_s * num_kv_heads * head_size * 2 (K and V)
 * element size: each (sequence, token, kv head) row of K and of V counted once,
 no block-tail padding and no re-reads by grouped query heads.
 
-Default workload (one GPU): the MHA 7B-like decode layer -- 64 sequences with
-lengths uniform on [128, 2048], 32 q / 32 kv heads, head_size 128,
-block_size 16, fp16 pool [2, num_blocks, 16, 32, 128] 1.25x the blocks in use
-with blocks scattered at random, N(0,1) data.  One step = the cache write of
-the 64 new tokens (pa_reshape_and_cache) followed by one decode pass over all
-sequences (pa_decode_splitk with 512-token partitions, or pa_decode with
---decode onepass).  The KV pool (1.4 GB) is larger than the 129 MB L2, so no
-L2 flush is needed between steps.
+Default workload (one GPU): the long-context split-K decode -- 8 sequences of
+131072 tokens, 64 q / 8 kv heads, head_size 128, block_size 32, bf16 pool of
+4.3 GB of keys and values (1.25x the blocks in use, scattered at random), 1% of
+the key rows scaled by 8.  One step = the cache write of the 8 new tokens
+(pa_reshape_and_cache) followed by one decode pass over all sequences
+(pa_decode_splitk with 512-token partitions and the log-sum-exp reduce).  The
+pool is far larger than the 129 MB L2, so no L2 flush is needed between
+steps.  The other decode configurations (MHA 7B-like, GQA 8B-like, prefix
+sharing, tiny) are measured the same way and reported per configuration under
+``roofline.by_config``; prefill, cascade, FP8 and block-copy workloads follow
+under ``workloads``.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With N > 1 the script runs under torch.distributed.run, one replica per GPU on
@@ -159,19 +162,47 @@ def kv_bytes(w) -> int:
     return w.kv_bytes()
 
 
+def _multi_part_rows(w, partition: int) -> int:
+    """(sequence, partition) units of sequences that span several partitions:
+    only those write partial states; a one-partition sequence writes its
+    output row directly."""
+    import torch
+    L = w.seq_lens.to(torch.int64)
+    parts = (L + partition - 1) // partition
+    return int(parts[parts > 1].sum().item())
+
+
 def decode_launch_bytes(w, split: bool, partition: int) -> int:
-    """Bytes the decode call must move: KV rows once, q, out, the block-table
-    entries in use, seq_lens, and for split-K the partial states written by
-    the partition kernel and read back by the reduce."""
+    """Bytes the whole decode call must move: KV rows once, q, out, the
+    block-table entries in use, seq_lens, and for split-K the partial states
+    of multi-partition sequences, written by the partition kernel and read
+    back by the reduce."""
     import torch
     el = w.kv_cache.element_size()
     L = w.seq_lens.to(torch.int64)
     nblk = int(((L + w.block_size - 1) // w.block_size).sum().item())
     b = kv_bytes(w) + 2 * w.q.numel() * el + nblk * 4 + w.num_seqs * 4
     if split:
-        parts = int(((L + partition - 1) // partition).sum().item())
-        b += 2 * parts * w.num_heads * (w.head_size + 2) * 4
+        b += 2 * _multi_part_rows(w, partition) * w.num_heads * (w.head_size + 2) * 4
     return b
+
+
+def decode_kernel_bytes(w, split: bool, partition: int) -> int:
+    """Bytes the main attention kernel alone must move: KV rows once, q, the
+    block-table entries in use, seq_lens, the output rows of one-partition
+    sequences, and the partial states of multi-partition ones (written once;
+    the reduce reads them and writes those sequences' output rows)."""
+    import torch
+    el = w.kv_cache.element_size()
+    L = w.seq_lens.to(torch.int64)
+    nblk = int(((L + w.block_size - 1) // w.block_size).sum().item())
+    b = kv_bytes(w) + w.q.numel() * el + nblk * 4 + w.num_seqs * 4
+    if not split:
+        return b + w.q.numel() * el
+    parts = (L + partition - 1) // partition
+    single = int((parts <= 1).sum().item())
+    row = w.num_heads * w.head_size * el
+    return b + single * row + _multi_part_rows(w, partition) * w.num_heads * (w.head_size + 2) * 4
 
 
 def decode_launches(w, split: bool, partition: int) -> int:
@@ -278,6 +309,110 @@ def cpu_baseline(w, budget_s: float = 10.0) -> dict:
 # Our arm
 # ---------------------------------------------------------------------------
 
+def main_kernel_name(w, split: bool) -> str:
+    """The attention kernel a decode call launches for this shape (mirrors the
+    library's choice: tensor cores for head_size 128 in split-K and for
+    grouped heads; PA_DECODE_KERNEL forces a family)."""
+    forced = os.environ.get("PA_DECODE_KERNEL", "")
+    G = w.num_heads // w.num_kv_heads
+    tc = w.head_size == 128 and forced != "simt" and (forced == "tcgen05" or split or G >= 2)
+    return "pa::tc::decode_tc_kernel" if tc else "pa::decode_kernel"
+
+
+def time_main_kernel(pa, decode, n: int, stream) -> float:
+    """Mean duration (ms) of the main attention kernel of `n` decode calls,
+    from CUDA events the library records on the call's stream right before
+    and after that kernel (pa_profile_kernel_events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:                       # torch creates events on first record
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    try:
+        for a, b in evs:
+            pa.pa_profile_kernel_events(a, b)
+            decode()
+    finally:
+        pa.pa_profile_kernel_events(None, None)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def decode_config_entry(name: str, args, peak_gbs: float, w=None) -> dict:
+    """One decode configuration through the bench step (cache write +
+    pa_decode_splitk), device-resident: the step, the decode call and its main
+    kernel, each timed with CUDA events on the launching stream."""
+    import torch
+    import paged_kv_cache_136_gb300 as pa
+    import workload as wl
+    own = w is None
+    if own:
+        w = wl.make(name, device="cuda", seed=args.seed)
+    out = torch.empty_like(w.q)
+    msl = int(w.seq_lens.max().item())
+    P = args.partition
+    ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                                        msl, P), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def decode():
+        pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                            w.block_size, msl, ws, P)
+
+    for _ in range(5):
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        decode()
+    n = max(3, args.workload_steps)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(n):
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        decode()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        ev[i][0].record(stream)
+        decode()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    call_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    kern_ms = time_main_kernel(pa, decode, n, stream)
+    kvb = kv_bytes(w)
+    cb = decode_launch_bytes(w, True, P)
+    kb = decode_kernel_bytes(w, True, P)
+    res = {"workload": WORKLOAD_TEXT[name], "call": "pa_decode_splitk", "partition_size": P,
+           "steps": n, "kv_bytes_per_step": kvb,
+           "ms_per_step": round(ms, 5), "step_gbs": round(kvb / ms / 1e6, 2),
+           "seqs_per_s": round(w.num_seqs / (ms / 1e3), 1),
+           "call_ms": round(call_ms, 5), "call_bytes": cb,
+           "call_gbs": round(cb / call_ms / 1e6, 2),
+           "call_frac": round(cb / call_ms / 1e6 / peak_gbs, 4),
+           "kernel": main_kernel_name(w, True), "kernel_ms": round(kern_ms, 5),
+           "kernel_bytes": kb, "kernel_gbs": round(kb / kern_ms / 1e6, 2),
+           "kernel_frac": round(kb / kern_ms / 1e6 / peak_gbs, 4),
+           "device_error_flags": pa.pa_device_errors(clear=True)}
+    if name == "prefix":
+        ub = w.unique_kv_bytes()
+        res["unique_kv_bytes_per_step"] = ub
+        res["unique_call_gbs"] = round(ub / call_ms / 1e6, 2)
+        res["note"] = ("the shared 8 MB prefix is read from L2 by all 128 sequences, so logical "
+                       "bytes exceed the HBM rate; the unique bytes are the HBM-bound figure")
+    if name == "tiny":
+        res["note"] = "117,760 KV bytes: launch-latency bound, no HBM roofline applies"
+    if own:
+        del w
+    del ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args) -> dict | None:
     import torch
     rank, world, local = dist_env()
@@ -313,8 +448,10 @@ def run_ours(args) -> dict | None:
     torch.cuda.synchronize()
     pa.pa_device_errors(clear=True)
 
+    # The timed region: K steps back to back, events only at its two ends
+    # (an event between two kernels would stop the next one's launch from
+    # overlapping the previous one's tail).
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local) if rank == 0 else None
@@ -323,33 +460,45 @@ def run_ours(args) -> dict | None:
     barrier(dist_mod)
     torch.cuda.synchronize()
     t_start.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
-        ev[i][1].record(stream)
-        decode()
-        ev[i][2].record(stream)
+    for _ in range(K):
+        step()
     t_stop.record(stream)
     torch.cuda.synchronize()
     barrier(dist_mod)
     clk = clocks.stop() if clocks else None
     ms_local = t_start.elapsed_time(t_stop)
+    flags = pa.pa_device_errors(clear=True)
+
+    # Per-call times (outside the timed region): events around each call.
+    n_calls = max(3, min(K, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_calls)]
+    torch.cuda.synchronize()
+    for i in range(n_calls):
+        ev[i][0].record(stream)
+        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
     dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     rsh_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    flags = pa.pa_device_errors(clear=True)
 
     ms_max = reduce_scalar(ms_local, "max", dist_mod, dev)
     bytes_all = reduce_scalar(float(kv_bytes(w)) * K, "sum", dist_mod, dev)
     seqs_all = reduce_scalar(float(w.num_seqs) * K, "sum", dist_mod, dev)
     value = bytes_all / (ms_max / 1e3) / 1e9
 
+    # The main attention kernel alone (outside the timed region above: the
+    # events between the kernels of a call stop its launch overlap).
+    kern_ms = time_main_kernel(pa, decode, n_calls, stream)
+
     # End to end through the public API: per step, copy the step's inputs
     # from pinned host memory, run the step, read the result back, and wait
     # for it on the host (a decode loop needs step i's output before it can
     # build step i+1's input).  The inputs live in one staging buffer (one
-    # copy per step, as a serving engine stages them), and the step -- copy
-    # in, cache write, decode, copy out -- is replayed as a CUDA graph of the
-    # same API calls.
+    # copy per step, as a serving engine stages them).  The headline runs the
+    # Python API calls eagerly, every host-side check and launch included;
+    # the same step replayed as a CUDA graph is reported beside it.
     names = ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens")
     offs, total = {}, 0
     for k in names:
@@ -376,42 +525,52 @@ def run_ours(args) -> dict | None:
         step()
         pa.pa_stage_copy(out_h, out)
 
-    for _ in range(3):
+    def e2e_eager():
         e2e_body()
-    torch.cuda.synchronize()
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_eager()
+    barrier(dist_mod)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_eager()
+    e2e_local = time.perf_counter() - t0
+    barrier(dist_mod)
+    e2e_max = reduce_scalar(e2e_local, "max", dist_mod, dev)
+    e2e_bytes = reduce_scalar(float(kv_bytes(w)) * e2e_steps, "sum", dist_mod, dev)
+
     graph = None
     try:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             e2e_body()
         torch.cuda.synchronize()
-    except Exception:                      # capture unavailable: run the calls eagerly
+    except Exception:                      # capture unavailable on this setup
         graph = None
         torch.cuda.synchronize()
-
-    def e2e_step():
-        if graph is not None:
+    g_value = None
+    if graph is not None:
+        for _ in range(3):
             graph.replay()
-        else:
-            e2e_body()
-        torch.cuda.current_stream().synchronize()
-
-    for _ in range(3):
-        e2e_step()
-    barrier(dist_mod)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_local = time.perf_counter() - t0
-    barrier(dist_mod)
-    e2e_max = reduce_scalar(e2e_local, "max", dist_mod, dev)
-    e2e_bytes = reduce_scalar(float(kv_bytes(w)) * e2e_steps, "sum", dist_mod, dev)
+            torch.cuda.current_stream().synchronize()
+        barrier(dist_mod)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            graph.replay()
+            torch.cuda.current_stream().synchronize()
+        g_local = time.perf_counter() - t0
+        barrier(dist_mod)
+        g_max = reduce_scalar(g_local, "max", dist_mod, dev)
+        g_value = round(e2e_bytes / g_max / 1e9, 2)
 
     if rank != 0:
         return None
     peaks = measured_peaks()
-    dec_bytes = decode_launch_bytes(w, split, P)
-    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    call_bytes = decode_launch_bytes(w, split, P)
+    kern_bytes = decode_kernel_bytes(w, split, P)
+    achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+    call_gbs = call_bytes / (dec_ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_max / K, 5),
@@ -428,22 +587,30 @@ def run_ours(args) -> dict | None:
                    "parallelism": f"replicas x{world}", "seed": args.seed},
         "seqs_per_s": round(seqs_all / (ms_max / 1e3), 1),
         "pct_hbm_peak": round(100.0 * value / peaks["hbm_gbs"], 2),
-        "roofline": {"bound": "hbm", "kernel": ("pa_decode_splitk call (plan, decode and reduce "
-                                                "kernels together)") if split else "pa_decode",
+        "roofline": {"bound": "hbm", "kernel": main_kernel_name(w, split),
                      "achieved": round(achieved, 2),
-                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak": peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy, burst",
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": recorded_traffic(args.config, "splitk" if split else "onepass"),
-                     "algorithmic_bytes_per_launch": dec_bytes,
-                     "ms_per_launch": round(dec_ms, 5)},
+                     "algorithmic_bytes_per_launch": kern_bytes,
+                     "ms_per_launch": round(kern_ms, 5),
+                     "timing": "CUDA events recorded by the library right before and after "
+                               "the kernel (pa_profile_kernel_events), mean of the launches",
+                     "call": {"what": ("pa_decode_splitk call: plan, partition and reduce "
+                                       "kernels") if split else "pa_decode call",
+                              "ms_per_launch": round(dec_ms, 5),
+                              "algorithmic_bytes_per_launch": call_bytes,
+                              "achieved": round(call_gbs, 2),
+                              "frac": round(call_gbs / peaks["hbm_gbs"], 4)}},
         "reshape": {"ms_per_launch": round(rsh_ms, 5),
                     "algorithmic_bytes_per_launch": reshape_launch_bytes(w)},
         "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "method": ("CUDA graph of the API calls" if graph is not None else "eager API calls")
-                          + ": one pinned staging copy in, cache write + decode, result copy"
-                            " out (both copies on the SMs, pa_stage_copy), host waits every"
-                            " step"},
+                "method": "eager Python API calls each step: one pinned staging copy in, "
+                          "cache write, decode, result copy out (both copies on the SMs, "
+                          "pa_stage_copy), host waits for the result",
+                "graph_value": g_value,
+                "graph_method": "the same step captured once as a CUDA graph and replayed"},
         "gpu_launches": K * (1 + decode_launches(w, split, P)),
         "clocks": clk,
         "device_error_flags": flags,
@@ -451,9 +618,21 @@ def run_ours(args) -> dict | None:
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    del w, ws, out, out_h, dev_buf, host_buf, graph
+    torch.cuda.empty_cache()
+    if world == 1 and args.configs:
+        by = {args.config: {"kernel": line["roofline"]["kernel"],
+                            "kernel_frac": line["roofline"]["frac"],
+                            "kernel_gbs": line["roofline"]["achieved"],
+                            "kernel_ms": line["roofline"]["ms_per_launch"],
+                            "call_frac": line["roofline"]["call"]["frac"],
+                            "call_ms": line["roofline"]["call"]["ms_per_launch"],
+                            "step_gbs": line["value"], "seqs_per_s": line["seqs_per_s"]}}
+        for name in args.configs.split(","):
+            if name and name != args.config:
+                by[name] = decode_config_entry(name, args, peaks["hbm_gbs"])
+        line["roofline"]["by_config"] = by
     if world == 1 and args.workloads:
-        del w, ws, out, out_h, dev_buf, host_buf, graph
-        torch.cuda.empty_cache()
         line["workloads"] = [other_workload(name, args, peaks["hbm_gbs"])
                              for name in args.workloads.split(",") if name]
     return line
@@ -659,11 +838,8 @@ def fp8_workload(name: str, args, peak_gbs: float) -> dict:
 
 
 def other_workload(name: str, args, peak_gbs: float) -> dict:
-    """Short device-resident measurement of another workload through the same
-    step (cache write + split-K decode), reported beside the main line."""
-    import torch
-    import paged_kv_cache_136_gb300 as pa
-    import workload as wl
+    """Short device-resident measurement of another workload, reported beside
+    the main line."""
     if name == "copy_blocks":
         return copy_blocks_workload(args, peak_gbs)
     if name.startswith("prefill_"):
@@ -672,51 +848,7 @@ def other_workload(name: str, args, peak_gbs: float) -> dict:
         return cascade_workload(args, peak_gbs)
     if name.startswith("fp8_"):
         return fp8_workload(name, args, peak_gbs)
-    w = wl.make(name, device="cuda")
-    out = torch.empty_like(w.q)
-    msl = int(w.seq_lens.max().item())
-    P = args.partition
-    ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads, w.head_size,
-                                                        msl, P), dtype=torch.uint8,
-                     device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def step():
-        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
-        pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
-                            w.block_size, msl, ws, P)
-
-    for _ in range(5):
-        step()
-    n = max(3, args.workload_steps)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(n):
-        pa.pa_reshape_and_cache(w.key, w.value, w.kv_cache, w.slot_mapping, w.block_size)
-        ev[i][0].record(stream)
-        pa.pa_decode_splitk(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
-                            w.block_size, msl, ws, P)
-        ev[i][1].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / n
-    dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    kvb = kv_bytes(w)
-    res = {"name": name, "workload": WORKLOAD_TEXT[name], "decode": "pa_decode_splitk",
-           "partition_size": P, "steps": n, "kv_bytes_per_step": kvb,
-           "step_gbs": round(kvb / ms / 1e6, 2), "ms_per_step": round(ms, 5),
-           "decode_gbs": round(decode_launch_bytes(w, True, P) / dec_ms / 1e6, 2),
-           "decode_frac": round(decode_launch_bytes(w, True, P) / dec_ms / 1e6 / peak_gbs, 4),
-           "seqs_per_s": round(w.num_seqs / (ms / 1e3), 1)}
-    if name == "prefix":
-        ub = w.unique_kv_bytes()
-        res["unique_kv_bytes_per_step"] = ub
-        res["unique_step_gbs"] = round(ub / ms / 1e6, 2)
-    del w, ws, out
-    torch.cuda.empty_cache()
-    return res
+    return dict(decode_config_entry(name, args, peak_gbs), name=name)
 
 
 # ---------------------------------------------------------------------------
@@ -819,18 +951,21 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(WORKLOAD_TEXT), default="mha7b")
+    ap.add_argument("--config", choices=sorted(WORKLOAD_TEXT), default="long")
     ap.add_argument("--decode", choices=["splitk", "onepass"], default="splitk")
     ap.add_argument("--partition", type=int, default=512)
     ap.add_argument("--seed", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=200,
+    ap.add_argument("--e2e-steps", type=int, default=50,
                     help="steps in the end-to-end (host buffers) measurement")
+    ap.add_argument("--configs", default="mha7b,gqa8b,prefix,tiny",
+                    help="other decode configurations measured like the main one and "
+                         "reported under roofline.by_config ('' for none)")
     ap.add_argument("--workloads",
-                    default="gqa8b,long,prefix,prefix_cascade,tiny,copy_blocks,prefill_mha7b,"
-                            "prefill_gqa8b,fp8_mha7b,fp8_gqa8b",
+                    default="prefix_cascade,copy_blocks,prefill_mha7b,prefill_gqa8b,fp8_mha7b,"
+                            "fp8_gqa8b",
                     help="other workloads measured briefly beside the main line ('' for none)")
     ap.add_argument("--workload-steps", type=int, default=50)
     ap.add_argument("--profile-case", default=None,

@@ -59,7 +59,10 @@
  *     clamped, slots write nothing) and sets a bit in a sticky per-device
  *     error word that pa_device_errors reads.  Kernels never trap.
  *   - Every wait inside a kernel is bounded; a wait that runs out sets
- *     PA_DEVERR_TIMEOUT and the kernel returns.
+ *     PA_DEVERR_TIMEOUT and the kernel returns.  A timeout is a device-side
+ *     event that happens after the call has returned, so it has no status
+ *     code of its own: it is reported by the sticky word, like the other
+ *     device-side guards.
  */
 #ifndef PA_H
 #define PA_H
@@ -173,7 +176,11 @@ pa_status pa_decode_splitk(void *out, const void *q, const void *kv_cache,
  *   - The array occupies PA_NOALLOC_SCRATCH_BYTES of device memory on every
  *     GPU where the library's module is loaded, until the process exits.
  *   - The first call on a device looks up the array's device address and
- *     caches it; make that first call before any stream capture.
+ *     caches it for that device and its current driver context; make that
+ *     first call before any stream capture.  After cudaDeviceReset, or from
+ *     another driver context on the same device, the array is a new one and
+ *     its address is looked up again on the next call, which should then
+ *     also come before any capture.
  *   - All calls on one device share the array.  Calls that overlap on the GPU
  *     race; order them (one stream, or events).  Nothing in the array needs
  *     to start at zero.
@@ -349,6 +356,11 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
  *                  are skipped and flagged (PA_DEVERR_BLOCK_ID).
  * num_pairs == 0 is a no-op; num_pairs <= 65535.
  */
+
+pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
+                         int num_blocks, int block_size, int num_kv_heads, int head_size,
+                         pa_dtype dtype, void *stream);
+
 /*
  * Copy bytes from src to dst on the GPU's SMs (16-byte moves), stream-
  * ordered on stream.  Either pointer may be device memory or pinned host
@@ -364,10 +376,6 @@ pa_status pa_prefill(void *out, float *lse, const void *q, const void *kv_cache,
  * for a failed launch or copy.
  */
 pa_status pa_stage_copy(void *dst, const void *src, size_t bytes, void *stream);
-
-pa_status pa_copy_blocks(void *kv_cache, const int64_t *block_mapping, int num_pairs,
-                         int num_blocks, int block_size, int num_kv_heads, int head_size,
-                         pa_dtype dtype, void *stream);
 
 /*
  * Host-side check of a HOST copy of a block mapping for pa_copy_blocks: ids in
@@ -410,6 +418,21 @@ pa_status pa_device_errors(unsigned int *flags, int clear);
  * the pages (it checks the library's own bounded-wait rule).
  */
 pa_status pa_selftest_wait_timeout(void *stream);
+
+/*
+ * Measurement aid.  For every later decode call made by the calling host
+ * thread (pa_decode, pa_decode_splitk, pa_decode_splitk_lse,
+ * pa_decode_splitk_noalloc and the FP8 decodes), record the CUDA event
+ * `before` on the call's stream just before its main attention kernel is
+ * launched and `after` just after, so that the elapsed time between them is
+ * that kernel's alone (the split-K plan and reduce kernels fall outside).
+ * Both are cudaEvent_t passed as void*, created and owned by the caller, and
+ * must stay valid while set; (NULL, NULL) turns the recording off, one NULL
+ * alone is PA_ERR_INVALID_ARG.  While set, the main kernel no longer
+ * overlaps its launch with the kernel before it.  No counterpart on the
+ * pages: it serves the library's own roofline measurement.
+ */
+pa_status pa_profile_kernel_events(void *before, void *after);
 
 /* Static, human-readable name of a status code. */
 const char *pa_status_string(pa_status status);

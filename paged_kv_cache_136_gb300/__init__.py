@@ -23,7 +23,8 @@ __all__ = [
     "pa_decode_splitk_lse", "pa_merge_attn_states", "pa_cascade_decode",
     "pa_cascade_decode_workspace_size", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
     "pa_decode_splitk_fp8", "pa_decode_splitk_fp8_workspace_size",
-    "pa_validate_block_mapping", "pa_status_string", "pa_version", "DEVERR_BLOCK_ID",
+    "pa_validate_block_mapping", "pa_status_string", "pa_version", "pa_profile_kernel_events",
+    "DEVERR_BLOCK_ID",
     "DEVERR_SEQ_LEN", "DEVERR_SLOT", "DEVERR_TIMEOUT",
 ]
 
@@ -94,6 +95,8 @@ _lib.pa_validate_block_mapping.restype = _I
 _lib.pa_validate_block_mapping.argtypes = [_P, _I, _I]
 _lib.pa_selftest_wait_timeout.restype = _I
 _lib.pa_selftest_wait_timeout.argtypes = [_P]
+_lib.pa_profile_kernel_events.restype = _I
+_lib.pa_profile_kernel_events.argtypes = [_P, _P]
 _lib.pa_status_string.restype = ctypes.c_char_p
 _lib.pa_status_string.argtypes = [_I]
 _lib.pa_version.restype = _I
@@ -508,6 +511,19 @@ def pa_selftest_wait_timeout(stream=None) -> None:
     """Run the bounded-wait self-test kernel (a wait nothing completes); it
     sets DEVERR_TIMEOUT after ~2 s and returns."""
     _check(_lib.pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
+
+
+def pa_profile_kernel_events(before, after) -> None:
+    """Record CUDA events ``before``/``after`` (torch.cuda.Event, already
+    recorded once so that they exist, or None to stop) around the main
+    attention kernel of this thread's later decode calls."""
+    def raw(ev):
+        if ev is None:
+            return ctypes.c_void_p(0)
+        if not ev.cuda_event:
+            raise ValueError("record the event once before passing it (it is created lazily)")
+        return ctypes.c_void_p(ev.cuda_event)
+    _check(_lib.pa_profile_kernel_events(raw(before), raw(after)), "pa_profile_kernel_events")
 
 
 def pa_device_errors(clear: bool = True) -> int:

@@ -51,6 +51,23 @@ static unsigned int *device_error_word(cudaError_t *err)
 // (default: one head, one block) of one plane, loaded with the 128-byte
 // swizzle.  Rows at or past NB*BS are out of bounds and read as zeros.
 // ---------------------------------------------------------------------------
+// Measurement aid (pa_profile_kernel_events): events recorded around the main
+// attention kernel of this host thread's later decode calls.
+static thread_local cudaEvent_t t_mark_before = nullptr;
+static thread_local cudaEvent_t t_mark_after = nullptr;
+
+static inline void mark_before(cudaStream_t s)
+{
+    if (t_mark_before)
+        cudaEventRecord(t_mark_before, s);
+}
+
+static inline void mark_after(cudaStream_t s)
+{
+    if (t_mark_after)
+        cudaEventRecord(t_mark_after, s);
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -385,6 +402,15 @@ extern "C" {
 
 int pa_version(void) { return 10000; }
 
+pa_status pa_profile_kernel_events(void *before, void *after)
+{
+    if ((before == nullptr) != (after == nullptr))
+        return PA_ERR_INVALID_ARG;
+    t_mark_before = static_cast<cudaEvent_t>(before);
+    t_mark_after = static_cast<cudaEvent_t>(after);
+    return PA_OK;
+}
+
 const char *pa_status_string(pa_status status)
 {
     switch (status) {
@@ -479,8 +505,10 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_
         t.len_cap = max_blocks_per_seq * block_size;
         t.qscale = scale * kLog2e;
         auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
+        mark_before(static_cast<cudaStream_t>(stream));
         e = launch(block_size, group, hg, false, pmap, qmap, t,
                    dim3(num_kv_heads / hg, num_seqs), static_cast<cudaStream_t>(stream));
+        mark_after(static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
     }
     DecodeParams p = {};
@@ -498,8 +526,10 @@ pa_status pa_decode(void *out, const void *q, const void *kv_cache, const int32_
     p.len_cap = max_blocks_per_seq * block_size;
     p.qscale = scale * kLog2e;
     DecodeKey key = {(int)dtype, head_size, block_size, num_heads / num_kv_heads, false};
+    mark_before(static_cast<cudaStream_t>(stream));
     e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, 1),
                       static_cast<cudaStream_t>(stream));
+    mark_after(static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
 }
 
@@ -540,13 +570,14 @@ size_t pa_decode_splitk_workspace_size(int num_seqs, int num_heads, int head_siz
 
 } // extern "C"
 
+// out_f32: write float32 output rows (the cascade's parts) instead of dtype.
 static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const void *kv_cache,
                                     const int32_t *block_tables, const int32_t *seq_lens,
                                     int num_seqs, int num_heads, int num_kv_heads, int head_size,
                                     int block_size, int num_blocks, int max_blocks_per_seq,
                                     float scale, pa_dtype dtype, int max_seq_len,
                                     int partition_size, void *workspace, size_t workspace_bytes,
-                                    void *stream)
+                                    void *stream, bool out_f32 = false)
 {
     pa_status st = check_decode_args(out, q, kv_cache, block_tables, seq_lens, num_seqs,
                                      num_heads, num_kv_heads, head_size, block_size, num_blocks,
@@ -596,10 +627,11 @@ static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const 
                 ? launch_after_previous(tc::splitk_plan_kernel<__nv_bfloat16>, dim3(1), dim3(1024), 0,
                                         s, seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__nv_bfloat16 *>(out), lse,
-                                        err)
+                                        err, out_f32 ? 1 : 0)
                 : launch_after_previous(tc::splitk_plan_kernel<__half>, dim3(1), dim3(1024), 0, s,
                                         seq_lens, num_seqs, num_heads, ngroups, partition_size,
-                                        len_cap, hdr, units, static_cast<__half *>(out), lse, err);
+                                        len_cap, hdr, units, static_cast<__half *>(out), lse, err,
+                                        out_f32 ? 1 : 0);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
         tc::TcParams t = {};
@@ -621,19 +653,22 @@ static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const 
         t.len_cap = len_cap;
         t.qscale = scale * kLog2e;
         t.lse = lse;
+        t.out_f32 = out_f32 ? 1 : 0;
         const int sms = sm_count(&e);
         if (!sms)
             return PA_ERR_CUDA;
         const size_t bound = (size_t)num_seqs * ngroups * parts;
         const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
         auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
+        mark_before(s);
         e = launch(block_size, group, hg, true, pmap, qmap, t, dim3(grid), s);
+        mark_after(s);
         if (e != cudaSuccess)
             return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
         if (parts > 1) {
             // Merge the partitions of multi-partition sequences.
             ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
-                              len_cap, 1, lse};
+                              len_cap, 1, lse, out_f32 ? 1 : 0};
             e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
         }
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -656,11 +691,13 @@ static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const 
     p.qscale = scale * kLog2e;
     p.lse = lse;
     DecodeKey key = {(int)dtype, head_size, block_size, group, true};
+    mark_before(s);
     e = launch_decode(key, tmap, p, dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
+    mark_after(s);
     if (e != cudaSuccess)
         return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
     ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size, len_cap,
-                      0, lse};
+                      0, lse, out_f32 ? 1 : 0};
     e = launch_reduce((int)dtype, head_size, r, num_seqs, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -716,15 +753,16 @@ __global__ void __launch_bounds__(256)
         out_lse[row] = lse;
 }
 
-// N-way merge of parts [nparts][rows][head_size] with log-sum-exps
+// N-way merge of float32 parts [nparts][rows][head_size] with log-sum-exps
 // [nparts][rows]: out = sum_i w_i o_i / sum_i w_i, w_i = exp(lse_i - max).
-// Parts with lse = -inf carry no weight and are not read; a row whose parts
-// are all empty is zero.
+// The parts stay in float32 so that the only 16-bit rounding is the final
+// one.  Parts with lse = -inf carry no weight and are not read; a row whose
+// parts are all empty is zero.
 constexpr int kMaxMergeParts = 17; // prefix key chunks (<= 16) + the suffix
 
 template <typename T>
 __global__ void __launch_bounds__(256)
-    merge_parts_kernel(T *__restrict__ out, const T *__restrict__ parts,
+    merge_parts_kernel(T *__restrict__ out, const float *__restrict__ parts,
                        const float *__restrict__ lse_parts, int nparts, int64_t rows,
                        int head_size)
 {
@@ -753,12 +791,13 @@ __global__ void __launch_bounds__(256)
                 continue;
             const float w = __expf(lv[i] - M);
             den += w;
-            const uint4 u = *reinterpret_cast<const uint4 *>(
+            const float4 *src = reinterpret_cast<const float4 *>(
                 parts + ((size_t)i * rows + row) * head_size + (size_t)v * 8);
-            const T *e = reinterpret_cast<const T *>(&u);
+            const float4 u0 = src[0], u1 = src[1];
+            const float e[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                acc[j] = fmaf(w, Elem<T>::one(e[j]), acc[j]);
+                acc[j] = fmaf(w, e[j], acc[j]);
         }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -848,7 +887,7 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
                               int num_kv_heads, int head_size, int block_size, int num_blocks,
                               int max_blocks_per_seq, float scale, int causal, pa_dtype dtype,
                               int key_split, int chunk_tiles, int64_t part_stride,
-                              int64_t lse_part_stride, void *stream)
+                              int64_t lse_part_stride, void *stream, bool out_f32 = false)
 {
     if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
         num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_size <= 0 ||
@@ -901,6 +940,7 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
     p.chunk_tiles = key_split > 1 ? chunk_tiles : 1;
     p.part_stride = part_stride;
     p.lse_part_stride = lse_part_stride;
+    p.out_f32 = out_f32 ? 1 : 0;
     // At most 128 query rows per request and an even group size: a CTA's
     // two tiles take two query heads of one kv head (both busy, one K/V
     // stream); otherwise one CTA per 256 rows of one head.
@@ -1032,7 +1072,9 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
         p.part_tokens = 0;
         p.max_parts = 1;
         p.len_cap = max_blocks_per_seq * block_size;
+        mark_before(s);
         e = launch(block_size, group, false, tmap, p, v_scale, dim3(num_kv_heads, num_seqs, 1), s);
+        mark_after(s);
         return e == cudaSuccess ? PA_OK
                                 : (e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA);
     }
@@ -1076,11 +1118,11 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
                 ? launch_after_previous(tc::splitk_plan_kernel<__nv_bfloat16>, dim3(1), dim3(1024), 0,
                                         s, seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__nv_bfloat16 *>(out),
-                                        static_cast<float *>(nullptr), err)
+                                        static_cast<float *>(nullptr), err, 0)
                 : launch_after_previous(tc::splitk_plan_kernel<__half>, dim3(1), dim3(1024), 0, s,
                                         seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__half *>(out),
-                                        static_cast<float *>(nullptr), err);
+                                        static_cast<float *>(nullptr), err, 0);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
         e = dtype == PA_BF16 ? launch_quantize_q_bf16(q, qparts, qscales, rows, s)
@@ -1111,7 +1153,9 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
         const size_t bound = (size_t)num_seqs * ngroups * parts;
         const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
         auto tl = dtype == PA_BF16 ? launch_decode_tc_fp8_bf16 : launch_decode_tc_fp8_f16;
+        mark_before(s);
         e = tl(block_size, group, hg, pmap, qmap, t, qscales, rows, v_scale, dim3(grid), s);
+        mark_after(s);
         if (e != cudaSuccess)
             return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
         if (parts > 1) {
@@ -1126,8 +1170,10 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
     p.part_tokens = partition_size;
     p.max_parts = (int)parts;
     p.len_cap = len_cap;
+    mark_before(s);
     e = launch(block_size, group, true, tmap, p, v_scale,
                dim3(num_kv_heads, num_seqs, (unsigned)parts), s);
+    mark_after(s);
     if (e != cudaSuccess)
         return e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
     ReduceParams r = {out, ws_o, ws_ml, seq_lens, num_heads, (int)parts, partition_size,
@@ -1191,7 +1237,7 @@ pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const
 
 // Cascade workspace: [256 B header: query_start_loc {0, B}, prefix seq_len]
 // [suffix lengths] [suffix tables] [parts: prefix key chunks then the suffix,
-// dtype] [their lse] [split-K workspace], 256-byte aligned.  The prefix pass
+// float32] [their lse] [split-K workspace], 256-byte aligned.  The prefix pass
 // is split over at most kMaxPrefixSplits key chunks.
 constexpr int kMaxPrefixSplits = kMaxMergeParts - 1;
 
@@ -1212,7 +1258,7 @@ static CascadeLayout cascade_layout(int num_seqs, int num_heads, int head_size,
     c.sl = 256;
     c.bt = c.sl + round_up((size_t)num_seqs * 4, 256);
     c.parts = c.bt + round_up((size_t)num_seqs * c.suffix_cols * 4, 256);
-    c.lse = c.parts + round_up((size_t)c.max_parts * rows * head_size * 2, 256);
+    c.lse = c.parts + round_up((size_t)c.max_parts * rows * head_size * 4, 256);
     c.ws = c.lse + round_up((size_t)c.max_parts * rows * 4, 256);
     c.ws_bytes = ws_layout(num_seqs, num_heads, head_size,
                            splitk_parts(max_suffix_len, partition_size)).total;
@@ -1297,14 +1343,14 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     st = prefill_impl(parts, lse_parts, q, kv_cache, block_tables, max_blocks_per_seq, hdr + 2,
                       hdr, 1, num_seqs, num_seqs, num_heads, num_kv_heads, head_size,
                       block_size, num_blocks, prefix_blocks, scale, 0, dtype, nsplit,
-                      chunk_tiles, part_elems, (int64_t)rows, stream);
+                      chunk_tiles, part_elems, (int64_t)rows, stream, true);
     if (st != PA_OK)
         return st;
     // 2. Each sequence's own suffix (part nsplit).
-    st = decode_splitk_impl(parts + (size_t)nsplit * part_elems * 2, lse_parts + (size_t)nsplit * rows,
+    st = decode_splitk_impl(parts + (size_t)nsplit * part_elems * 4, lse_parts + (size_t)nsplit * rows,
                             q, kv_cache, bt_suf, sl_suf, num_seqs, num_heads, num_kv_heads,
                             head_size, block_size, num_blocks, c.suffix_cols, scale, dtype,
-                            max_suffix, partition_size, w + c.ws, c.ws_bytes, stream);
+                            max_suffix, partition_size, w + c.ws, c.ws_bytes, stream, true);
     if (st != PA_OK)
         return st;
     // 3. Merge the nsplit + 1 parts.
@@ -1314,12 +1360,12 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
         dtype == PA_BF16
             ? launch_after_previous(merge_parts_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
                                     static_cast<__nv_bfloat16 *>(out),
-                                    reinterpret_cast<const __nv_bfloat16 *>(parts),
+                                    reinterpret_cast<const float *>(parts),
                                     static_cast<const float *>(lse_parts), nsplit + 1,
                                     (int64_t)rows, head_size)
             : launch_after_previous(merge_parts_kernel<__half>, dim3(grid), dim3(256), 0, s,
                                     static_cast<__half *>(out),
-                                    reinterpret_cast<const __half *>(parts),
+                                    reinterpret_cast<const float *>(parts),
                                     static_cast<const float *>(lse_parts), nsplit + 1,
                                     (int64_t)rows, head_size);
     return me == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -75,6 +75,18 @@ struct Elem<__nv_bfloat16> {
     static __device__ __forceinline__ __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Element idx of an output row buffer: the input dtype T, or float32 when
+// f32 is set (the cascade keeps its partial results in float32 so that
+// merging them adds no 16-bit rounding).
+template <typename T>
+__device__ __forceinline__ void put_out(void *base, size_t idx, float v, int f32)
+{
+    if (f32)
+        reinterpret_cast<float *>(base)[idx] = v;
+    else
+        reinterpret_cast<T *>(base)[idx] = Elem<T>::from(v);
+}
+
 template <typename T>
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
 {
@@ -423,10 +435,10 @@ __global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParam
     L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
     const int np = (L + p.part_tokens - 1) / p.part_tokens;
     const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
-    T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + h) * D;
+    const size_t out0 = ((size_t)s * p.num_heads + h) * D;
     if (np == 0) {
         if (g == 0)
-            out[d] = Elem<T>::from(0.f);
+            put_out<T>(p.out, out0 + d, 0.f, p.out_f32);
         if (p.lse && tid == 0)
             p.lse[(size_t)s * p.num_heads + h] = -INFINITY;
         return;
@@ -491,7 +503,7 @@ __global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParam
                 num += num_s[i][d];
     }
     if (g == 0) {
-        out[d] = Elem<T>::from(num / den);
+        put_out<T>(p.out, out0 + d, num / den, p.out_f32);
         if (p.lse && d == 0)
             p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
     }
@@ -520,11 +532,11 @@ __global__ void __launch_bounds__(32 * kReduceWarpHeads)
     L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
     const int np = (L + p.part_tokens - 1) / p.part_tokens;
     const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
-    T *out = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_heads + h) * D;
+    const size_t out0 = ((size_t)s * p.num_heads + h) * D;
     if (np == 0) {
 #pragma unroll
         for (int e = 0; e < E; ++e)
-            out[lane + 32 * e] = Elem<T>::from(0.f);
+            put_out<T>(p.out, out0 + lane + 32 * e, 0.f, p.out_f32);
         if (p.lse && lane == 0)
             p.lse[(size_t)s * p.num_heads + h] = -INFINITY;
         return;
@@ -559,7 +571,7 @@ __global__ void __launch_bounds__(32 * kReduceWarpHeads)
     }
 #pragma unroll
     for (int e = 0; e < E; ++e)
-        out[lane + 32 * e] = Elem<T>::from(acc[e] / den);
+        put_out<T>(p.out, out0 + lane + 32 * e, acc[e] / den, p.out_f32);
     if (p.lse && lane == 0)
         p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
 }

@@ -115,6 +115,7 @@ struct TcParams {
     int part_tokens, max_parts, len_cap;
     float qscale;
     float *lse;                  // [B, H] natural-log softmax denominators, or null
+    int out_f32;                 // out holds float32 rows instead of T
 };
 
 template <typename T>
@@ -306,10 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 static_done = 1;
                 if (!have) {
                     // Empty sequence: its output rows are zero.
-                    T *out = reinterpret_cast<T *>(p.out) +
-                             ((size_t)s * p.num_heads + group * NV) * kD;
+                    const size_t out0 = ((size_t)s * p.num_heads + group * NV) * kD;
                     for (int i = lane; i < NV * kD; i += 32)
-                        out[i] = Elem<T>::from(0.f);
+                        put_out<T>(p.out, out0 + i, 0.f, p.out_f32);
                     if (p.lse && lane < NV)
                         p.lse[(size_t)s * p.num_heads + group * NV + lane] = -INFINITY;
                 }
@@ -546,10 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (m->red2[fin_par][2][n] + m->red2[fin_par][3][n]);
             const size_t head0 = (size_t)fin_s * p.num_heads + (size_t)fin_group * NV;
             if (!SPLIT || fin_nparts == 1) {
-                T *out = reinterpret_cast<T *>(p.out) + head0 * kD;
 #pragma unroll
                 for (int n = 0; n < NV; ++n)
-                    out[n * kD + t] = Elem<T>::from(o_acc[n] / l[n]);
+                    put_out<T>(p.out, (head0 + n) * kD + t, o_acc[n] / l[n], p.out_f32);
                 if (p.lse) {
 #pragma unroll
                     for (int n = 0; n < NV; ++n)
@@ -738,7 +737,7 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
                                                            int len_cap, uint32_t *hdr,
                                                            uint32_t *units,
                                                            T *out, float *lse,
-                                                           unsigned int *err)
+                                                           unsigned int *err, int out_f32)
 {
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t bucket[kPlanBuckets];
@@ -781,7 +780,7 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
                 atomicAdd(&bucket[size_bucket(L - (n - 1) * part_tokens)], 1u);
             } else {
                 for (int i = 0; i < H * 128; ++i)
-                    out[(size_t)s * H * 128 + i] = Elem<T>::from(0.f);
+                    put_out<T>(out, (size_t)s * H * 128 + i, 0.f, out_f32);
                 if (lse)
                     for (int h = 0; h < H; ++h)
                         lse[(size_t)s * H + h] = -INFINITY;

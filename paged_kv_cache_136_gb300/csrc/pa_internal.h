@@ -69,6 +69,7 @@ struct ReduceParams {
     int len_cap;
     int skip_single; // rows of one-partition sequences are already final
     float *lse;      // [B, H] natural-log softmax denominators, or null
+    int out_f32;     // out holds float32 rows instead of the input dtype
 };
 
 // Key of a decode kernel instantiation.
@@ -167,6 +168,7 @@ struct PrefillParams {
     // Head pairs: grid.y = H/2 and a CTA's two tiles are query heads 2j and
     // 2j+1 (same kv head) over the same 128 rows.
     int head_pairs;
+    int out_f32;                    // out holds float32 rows instead of the input dtype
 };
 
 // Prefill over the paged cache on grid (ceil(max_query_len/128) x key_split, H, R).

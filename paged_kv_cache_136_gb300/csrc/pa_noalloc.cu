@@ -13,8 +13,10 @@
 // The array holds PA_NOALLOC_SCRATCH_BYTES on every GPU where the library's
 // module is loaded, until the process exits.  On each device the entry
 // point's first call looks up the array's device address
-// (cudaGetSymbolAddress, with that device current) and caches it; that first
-// call should therefore come before any stream capture.  All calls on a
+// (cudaGetSymbolAddress, with that device current) and caches it per device
+// and context; that first call (and the first call after a device reset or
+// in another driver context) should therefore come before any stream
+// capture.  All calls on a
 // device share the one array: calls that overlap on the GPU race, so callers
 // must order them (one stream, or events).
 #include <cuda_runtime.h>
@@ -30,30 +32,74 @@ namespace {
 // from scratch_address().
 __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device (looked up once
-// per device).  Returns nullptr and sets *err if the lookup fails.
+// cuCtxGetCurrent through the runtime's driver entry point (no link against
+// the driver library).  Returns nullptr if the driver does not export it.
+typedef int (*ctx_get_current_fn)(void **ctx);
+
+ctx_get_current_fn ctx_get_current()
+{
+    static ctx_get_current_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<ctx_get_current_fn>(p);
+    });
+    return fn;
+}
+
+// Device address of g_noalloc_scratch in the current device's current
+// context.  The lookup is done once per (device, context) and cached: a new
+// context on a device (after cudaDeviceReset, or a caller that switched
+// driver contexts) loads the module again with a new copy of the array, so
+// its address is looked up again.  Returns nullptr and sets *err if the
+// lookup fails.
 void *scratch_address(cudaError_t *err)
 {
-    static void *addr[64] = {nullptr};
+    struct entry {
+        int dev;
+        void *ctx;
+        void *addr;
+    };
+    static entry cache[64];
+    static int n_cached = 0;
     static std::mutex mu;
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess)
         return nullptr;
-    if (dev < 0 || dev >= 64) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
+    void *ctx = nullptr;
+    ctx_get_current_fn get_ctx = ctx_get_current();
+    if (get_ctx && get_ctx(&ctx) != 0)
+        ctx = nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (*err != cudaSuccess || !p)
-            return nullptr;
-        addr[dev] = p;
-    }
+    for (int i = 0; i < n_cached; ++i)
+        if (cache[i].dev == dev && cache[i].ctx == ctx) {
+            *err = cudaSuccess;
+            return cache[i].addr;
+        }
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess || !p)
+        return nullptr;
+    // With no context current before the lookup, the runtime has just made
+    // the device's primary context current: key the entry on that one.
+    if (!ctx && get_ctx && get_ctx(&ctx) != 0)
+        ctx = nullptr;
+    // Replace an entry of the same device (its context is gone or no longer
+    // current), else append; a full table recycles its oldest slot.
+    int slot = -1;
+    for (int i = 0; i < n_cached; ++i)
+        if (cache[i].dev == dev)
+            slot = i;
+    if (slot < 0)
+        slot = n_cached < 64 ? n_cached++ : 0;
+    cache[slot] = {dev, ctx, p};
     *err = cudaSuccess;
-    return addr[dev];
+    return p;
 }
 
 } // namespace

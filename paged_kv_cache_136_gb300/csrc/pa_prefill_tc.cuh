@@ -27,17 +27,15 @@
 //                      an MN-major shared-memory operand.
 //   warps 0-3 / 4-7    one query row per thread (TMEM lane): scale and mask
 //   (softmax, tile 0/1) the row's TN scores, row max, base-2 exponentials,
-//                      write P over S as 16-bit values (bf16: a high part in
+//                      write P over S as 16-bit values (a high part in
 //                      the buffer's first TN/2 columns and the rounded
-//                      remainder after them, so P keeps ~16 significant
-//                      bits), and at the end
+//                      remainder after them, so P keeps 16 or more
+//                      significant bits), and at the end
 //                      out = O / l (and the log-sum-exp when asked).
 //
-// Key tiles: fp16 uses TN = 128 keys and one score buffer per query tile, so
-// a tile's next scores MMA waits for its values MMA (P lies over S).  bf16
-// carries P as two parts (twice the values MMAs) and uses TN = 64 with two
-// score buffers: the next tile's scores are computed into the other buffer
-// while this tile's softmax runs.
+// Key tiles: P travels as two parts (twice the values MMAs), with TN = 64
+// keys and two score buffers per query tile: the next tile's scores are
+// computed into the other buffer while this tile's softmax runs.
 //
 // The running maximum is updated lazily: O and l are rescaled only when a key
 // tile raises a row's maximum by more than 2^8, so most tiles skip the rescale
@@ -69,12 +67,11 @@ constexpr float kRescaleLog2 = 8.f; // lazy-rescale threshold, log2 units
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQRegion = kTileM * 128;  // 128 query rows x 64 elements x 2 bytes
 
-// Keys per K/V tile.  fp16: 128 keys and one score buffer, so the next tile's
-// scores wait for this tile's values MMA (P lies over S).  bf16 carries P as
-// two parts (twice the values MMAs): 64 keys and two score buffers, so the
-// next tile's scores are computed while this tile's softmax runs.
+// Keys per K/V tile: 64 keys and two score buffers, so the next tile's
+// scores are computed while this tile's softmax runs (P, in two parts, lies
+// over the scores it came from).
 template <typename T>
-constexpr int key_tile() { return std::is_same<T, __half>::value ? 128 : 64; }
+constexpr int key_tile() { return 64; }
 
 template <int D, int TN>
 struct Geo {
@@ -117,6 +114,20 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// The two values of a packed pair, back to float.
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t w)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {
@@ -151,9 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int BPT = kTileN / BS; // pool blocks per key tile
     static_assert(32 % BPT == 0 && BPT * NH <= 32, "key tile geometry");
     constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-    // bf16 keeps only 8 significant bits: P then travels as a high part plus
-    // the rounded remainder (two MMAs on the same V), fp16's 11 bits suffice.
-    constexpr bool kSplitP = kFmt == 1u;
+    // P travels as a high part plus the rounded remainder (two MMAs on the
+    // same V): a 16-bit P alone (8 or 11 significant bits) puts the
+    // relative error of a row whose keys' values cancel above 1e-2.
+    constexpr bool kSplitP = true;
     constexpr uint32_t kIdescS = idesc_f16_f32(kFmt, 0, 0, kTileM, kTileN);
     constexpr uint32_t kIdescO = idesc_f16_f32(kFmt, 0, 1, kTileM, D);
 
@@ -204,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Keys of this CTA: [kt0 * 128, key_hi) (the whole request unless split).
     const int kt0 = csplit * p.chunk_tiles * kChunkUnit;
     const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles * kChunkUnit) * kTileN) : L;
-    T *const out_base = reinterpret_cast<T *>(p.out) + (size_t)csplit * (size_t)p.part_stride;
+    // Output rows in T, or float32 (out_f32: the cascade's parts).
+    const size_t out_elem0 = (size_t)csplit * (size_t)p.part_stride;
     float *const lse_base = p.lse ? p.lse + (size_t)csplit * (size_t)p.lse_part_stride : nullptr;
     int nv[2], nt[2];
 #pragma unroll
@@ -219,7 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             for (int i = tid; i < nv[t] * D; i += kThreads) {
                 const size_t tok = (size_t)(q0 + i0 + toff(t) + i / D);
-                out_base[(tok * p.num_heads + thead(t)) * D + i % D] = T(0.f);
+                const size_t e = out_elem0 + (tok * p.num_heads + thead(t)) * D + i % D;
+                if (p.out_f32)
+                    static_cast<float *>(p.out)[e] = 0.f;
+                else
+                    static_cast<T *>(p.out)[e] = T(0.f);
             }
             if (lse_base)
                 for (int i = tid; i < nv[t]; i += kThreads)
@@ -505,9 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l2[j & 1] = __fadd2_rn(l2[j & 1], pp);
                         pk[j] = pack2<T>(pp.x, pp.y);
                         if (kSplitP) {
-                            const float h0 = __uint_as_float(pk[j] << 16);
-                            const float h1 = __uint_as_float(pk[j] & 0xFFFF0000u);
-                            lo[j] = pack2<T>(pp.x - h0, pp.y - h1);
+                            const float2 hf = unpack2<T>(pk[j]);
+                            lo[j] = pack2<T>(pp.x - hf.x, pp.y - hf.y);
                         }
                     }
                     tmem_st16(sb + (uint32_t)(c * 16), pk);
@@ -571,19 +587,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t tok = (size_t)(q0 + i0 + toff(wg) + row);
                 const int hw = thead(wg);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                T *o = out_base + (tok * p.num_heads + hw) * D;
+                const size_t o_elem = out_elem0 + (tok * p.num_heads + hw) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32_nowait(o_addr + (uint32_t)(c * 32), v);
                     tmem_wait_ld();
+                    if (p.out_f32) {
+                        if (valid) {
+                            float4 *dst =
+                                reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o_elem + c * 32);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = make_float4(__uint_as_float(v[4 * j]) * inv,
+                                                     __uint_as_float(v[4 * j + 1]) * inv,
+                                                     __uint_as_float(v[4 * j + 2]) * inv,
+                                                     __uint_as_float(v[4 * j + 3]) * inv);
+                        }
+                        continue;
+                    }
                     uint32_t w[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         w[j] = pack2<T>(__uint_as_float(v[2 * j]) * inv,
                                         __uint_as_float(v[2 * j + 1]) * inv);
                     if (valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
+                        uint4 *dst =
+                            reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + o_elem + c * 32);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);

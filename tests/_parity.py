@@ -1,15 +1,31 @@
 """Shared helpers of the GPU parity tests: run the CUDA library and the CPU
 oracle on the same seeded inputs and compare.
 
-Attention tolerance: the required bound is max-abs 2e-3 and max-rel 1e-2 on
-fp16/bf16 inputs with fp32 accumulation.  It is applied element by element as
-|gpu - ref| <= 2e-3 + 1e-2 * |ref|, with ref the oracle's fp64 result before
-output rounding.  (A bf16 output of magnitude ~1 alone carries up to 2^-9 of
-rounding error, so a pure 2e-3 absolute bound could not hold; the relative
-term covers it.)  Tests also record the maximum absolute error and the
-maximum relative error over |ref| >= 1e-2.
+Attention tolerance.  The required bound is max-abs error 2e-3 and max-rel
+error 1e-2 for fp16/bf16 inputs with fp32 accumulation.  `ref` is the
+oracle's fp64 result before output rounding.
+
+- fp16 outputs: the bound as stated.  max |gpu - ref| <= 2e-3 over every
+  element, and max |gpu - ref| / |ref| <= 1e-2 over the elements with
+  |ref| >= 1e-2 (below that, relative error of a value that is mostly
+  cancellation carries no information and the absolute bound governs).  An
+  fp16 output below 4 carries at most 2^-10 of its own rounding, so the
+  absolute bound leaves room for the fp32 arithmetic.
+- bf16 outputs: the relative bound as stated.  The absolute bound is taken on
+  the error beyond the output's own rounding: |gpu - ref| <= 2e-3 + half a
+  bf16 ulp at max(|gpu|, |ref|).  A bf16 value in [1, 2) is a multiple of
+  2^-7, so its correctly rounded form alone can be 3.9e-3 away from ref and
+  the plain absolute bound could not hold for any bf16 kernel.
+
+Every call records its error statistics; when the environment variable
+PA_PARITY_LOG names a file, one JSON line per call is appended to it (test
+id, output dtype, element count, max-abs, max-rel over |ref| >= 1e-2, the
+worst error beyond output rounding).
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -17,8 +33,31 @@ import torch
 from oracle.oracle import get as get_oracle
 from workload import ORACLE_DTYPE, Workload, bits
 
-ATOL = 2e-3
-RTOL = 1e-2
+ATOL = 2e-3          # max-abs bound
+RTOL = 1e-2          # max-rel bound
+REL_FLOOR = 1e-2     # max-rel is taken over |ref| >= REL_FLOOR
+
+# significand bits after the leading one, and the smallest normal exponent
+_FORMAT = {torch.float16: (10, -14), torch.bfloat16: (7, -126)}
+
+
+def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """Half the spacing of `dtype` values at magnitude |x| (the largest
+    rounding error of a correctly rounded result there)."""
+    mant, emin = _FORMAT[dtype]
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, emin)
+    return np.ldexp(0.5, (e - mant).astype(np.int64))
+
+
+def _log(rec: dict) -> None:
+    path = os.environ.get("PA_PARITY_LOG")
+    if not path:
+        return
+    rec = dict(rec, test=os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0])
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
 
 
 def oracle_decode(w: Workload, items=None, cache_bits=None) -> np.ndarray:
@@ -52,16 +91,22 @@ def oracle_decode_lse(w: Workload, items=None) -> np.ndarray:
 
 
 def check_lse(got: torch.Tensor, ref: np.ndarray, items=None, what: str = ""):
-    """Log-sum-exps agree to 1e-3 absolute (the scores are fp32 dot products
-    of 16-bit inputs; the log of the denominator is insensitive to P's
-    16-bit rounding)."""
+    """Log-sum-exps agree to 2e-5 absolute plus 1e-6 relative.  The kernels
+    form the softmax denominator as an fp32 sum of fp32 exponentials of fp32
+    scores (exact products of the 16-bit inputs): its relative error is a
+    few fp32 ulps times the depth of the summation tree, about 1e-6 for the
+    lengths tested, and the log turns that relative error into an absolute
+    one.  The relative term covers the fp32 rounding of the running maximum
+    added back (an fp32 ulp of lse is 1.2e-7 * |lse|)."""
     g = got.detach().cpu().numpy().astype(np.float64).reshape(-1)
     r = np.asarray(ref).reshape(-1)
     if items is not None:
         g, r = g[np.asarray(items)], r[np.asarray(items)]
     assert np.isfinite(g).all() and np.isfinite(r).all(), f"{what}: non-finite lse"
     err = np.abs(g - r)
-    assert (err <= 1e-3 + 1e-4 * np.abs(r)).all(), f"{what}: lse max err {err.max()}"
+    _log({"what": what + " [lse]", "dtype": "float32", "n": int(err.size),
+          "max_abs": float(err.max()) if err.size else 0.0})
+    assert (err <= 2e-5 + 1e-6 * np.abs(r)).all(), f"{what}: lse max err {err.max()}"
 
 
 def oracle_reshape(w: Workload, cache_bits=None) -> np.ndarray:
@@ -71,28 +116,64 @@ def oracle_reshape(w: Workload, cache_bits=None) -> np.ndarray:
                                  w.block_size)
 
 
+def attention_stats(g: np.ndarray, ref: np.ndarray, dtype: torch.dtype) -> dict:
+    """Error statistics of output `g` (fp64 copy of a `dtype` tensor) against
+    the fp64 reference."""
+    err = np.abs(g - ref)
+    big = np.abs(ref) >= REL_FLOOR
+    excess = err - half_ulp(np.maximum(np.abs(g), np.abs(ref)), dtype)
+    return {
+        "n": int(err.size),
+        "max_abs": float(err.max()) if err.size else 0.0,
+        "max_rel_ge_1e-2": float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0,
+        "max_abs_beyond_rounding": float(excess.max()) if err.size else 0.0,
+    }
+
+
 def check_attention(got: torch.Tensor, ref: np.ndarray, items=None, what: str = "") -> dict:
+    """Assert the attention tolerance (module docstring) element by element;
+    return the error statistics."""
+    dtype = got.dtype
+    assert dtype in _FORMAT, f"{what}: unexpected output dtype {dtype}"
     g = got.detach().float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
     if items is not None:
         B, H, D = g.shape
         g = g.reshape(B * H, D)[np.asarray(items)]
         ref = ref.reshape(B * H, D)[np.asarray(items)]
     assert np.isfinite(ref).all(), f"{what}: oracle produced non-finite values"
     assert np.isfinite(g).all(), f"{what}: GPU output has non-finite values"
+    stats = attention_stats(g, ref, dtype)
+    _log({"what": what, "dtype": str(dtype).replace("torch.", ""), **stats})
     err = np.abs(g - ref)
-    bound = ATOL + RTOL * np.abs(ref)
-    big = np.abs(ref) >= 1e-2
-    stats = {
-        "max_abs": float(err.max()) if err.size else 0.0,
-        "max_rel_ge_1e-2": float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0,
-        "worst_ratio": float((err / bound).max()) if err.size else 0.0,
-    }
-    bad = err > bound
+    abs_bound = np.full_like(err, ATOL)
+    if dtype == torch.bfloat16:
+        abs_bound += half_ulp(np.maximum(np.abs(g), np.abs(ref)), dtype)
+    big = np.abs(ref) >= REL_FLOOR
+    bad_abs = err > abs_bound
+    bad_rel = big & (err > RTOL * np.abs(ref))
+    bad = bad_abs | bad_rel
     if bad.any():
-        idx = np.unravel_index(np.argmax(err / bound), err.shape)
-        raise AssertionError(f"{what}: {int(bad.sum())} elements outside tolerance; worst at "
-                             f"{idx}: gpu={g[idx]!r} ref={ref[idx]!r} stats={stats}")
+        score = np.maximum(err / abs_bound, np.where(big, err / (RTOL * np.abs(ref) + 1e-300), 0))
+        idx = np.unravel_index(np.argmax(score), err.shape)
+        raise AssertionError(
+            f"{what}: {int(bad_abs.sum())} elements over the abs bound, {int(bad_rel.sum())} "
+            f"over the rel bound; worst at {idx}: gpu={g[idx]!r} ref={ref[idx]!r} "
+            f"stats={stats}")
     return stats
+
+
+def check_agree(a: torch.Tensor, b: torch.Tensor, what: str = "") -> float:
+    """Two GPU results of the same attention (different partitionings) agree
+    within the abs bound plus one output ulp: each is a correctly rounded
+    fp32 accumulation of the same sum, which may round to neighbouring
+    values."""
+    x = a.detach().float().cpu().numpy().astype(np.float64)
+    y = b.detach().float().cpu().numpy().astype(np.float64)
+    d = np.abs(x - y)
+    bound = ATOL + 2.0 * half_ulp(np.maximum(np.abs(x), np.abs(y)), a.dtype)
+    assert (d <= bound).all(), f"{what}: max diff {d.max()} (bound there {bound.flat[d.argmax()]})"
+    return float(d.max()) if d.size else 0.0
 
 
 def splitk_workspace(pa, w: Workload, max_seq_len: int, partition_size: int,

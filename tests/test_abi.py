@@ -44,6 +44,16 @@ def test_library_exports_every_declared_symbol(pa):
     assert not missing, missing
 
 
+def test_profile_hook_arguments(pa):
+    lib = ctypes.CDLL(pa.lib_path())
+    f = lib.pa_profile_kernel_events
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert f(ctypes.c_void_p(FAKE), None) == 1      # one event alone: PA_ERR_INVALID_ARG
+    assert f(None, ctypes.c_void_p(FAKE)) == 1
+    assert f(None, None) == 0                       # off
+
+
 def test_status_strings(pa):
     assert pa.pa_status_string(0) == "PA_OK"
     assert pa.pa_status_string(3) == "PA_ERR_WORKSPACE"
@@ -223,7 +233,7 @@ def test_cascade_workspace_size_covers_its_parts(pa):
     B, H, D, MB, pb, bs, P = 128, 32, 128, 157, 125, 16, 512
     n = pa.pa_cascade_decode_workspace_size(B, H, D, MB, pb, 2500, bs, P)
     split = pa.pa_decode_splitk_workspace_size(B, H, D, 2500 - pb * bs, P)
-    parts = B * H * D * 2 * 2 + B * H * 4 * 2 + B * 4 + B * (MB - pb) * 4
+    parts = B * H * D * 4 * 2 + B * H * 4 * 2 + B * 4 + B * (MB - pb) * 4   # float32 parts
     assert n >= split + parts and n % 256 == 0
     assert pa.pa_cascade_decode_workspace_size(B, H, D, MB, MB + 1, 2500, bs, P) == 0
 

@@ -60,4 +60,26 @@ def test_bench_arguments(argv, expect):
     import bench
     a = bench.parse_args(argv)
     assert (a.impl, a.gpus, a.steps) == expect
-    assert a.config == "mha7b"
+    assert a.config == "long"
+
+
+def test_bench_byte_accounting_counts_partials_of_split_sequences_only():
+    """Algorithmic bytes of the decode call and of its main kernel on a small
+    CPU workload, written out by hand: one sequence of 1 token (one
+    partition, its output row written by the kernel), one of 65 tokens (two
+    partitions of 64: partial states written by the kernel, read by the
+    reduce)."""
+    import bench
+    import workload as wl
+    w = wl.make("tiny", device="cpu", lengths=[1, 65], seed=1)
+    el, H, Hkv, D, bs = 2, w.num_heads, w.num_kv_heads, w.head_size, w.block_size
+    kv = (1 + 65) * Hkv * D * el * 2
+    q = 2 * H * D * el
+    tables = (1 + 5) * 4 + 2 * 4          # blocks in use (bs 16) + seq_lens
+    partial = H * (D + 2) * 4             # one (sequence, head) partial state
+    assert bench.kv_bytes(w) == kv
+    assert bench.decode_launch_bytes(w, False, 64) == kv + 2 * q + tables
+    assert bench.decode_launch_bytes(w, True, 64) == kv + 2 * q + tables + 2 * 2 * partial
+    row = H * D * el
+    assert bench.decode_kernel_bytes(w, True, 64) == kv + q + tables + row + 2 * partial
+    assert bench.decode_kernel_bytes(w, False, 64) == kv + 2 * q + tables
