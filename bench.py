@@ -891,7 +891,7 @@ def run_reference(args) -> dict | None:
     }
 
 
-def run_profile_case(name: str, repeat: int) -> None:
+def run_profile_case(name: str, repeat: int, num_seqs: int | None = None) -> None:
     """Run one case `repeat` times and exit, for a profiler's launch capture:
     splitk_<config> (a bench step: cache write, split-K decode), prefill_<name>,
     fp8_<config>, prefix_cascade."""
@@ -917,7 +917,7 @@ def run_profile_case(name: str, repeat: int) -> None:
                                     w.block_size, w.meta["k_scale"], w.meta["v_scale"], msl,
                                     ws, 512)
     elif name.startswith("splitk_"):
-        w = wl.make(name[7:], device="cuda")
+        w = wl.make(name[7:], device="cuda", num_seqs=num_seqs)
         msl = int(w.seq_lens.max())
         ws = torch.empty(pa.pa_decode_splitk_workspace_size(w.num_seqs, w.num_heads,
                                                             w.head_size, msl, 512),
@@ -972,13 +972,15 @@ def parse_args(argv=None):
                     help="run one case --repeat times for a profiler and exit (no JSON): "
                          "splitk_<config>, prefill_<name>, fp8_<config>, prefix_cascade")
     ap.add_argument("--repeat", type=int, default=3)
+    ap.add_argument("--profile-seqs", type=int, default=None,
+                    help="with --profile-case splitk_<config>: only the first N sequences")
     return ap.parse_args(argv)
 
 
 def main(argv=None):
     args = parse_args(argv)
     if args.profile_case:
-        run_profile_case(args.profile_case, max(1, args.repeat))
+        run_profile_case(args.profile_case, max(1, args.repeat), args.profile_seqs)
         return 0
     if args.warmup < 3:
         args.warmup = 3

@@ -9,33 +9,36 @@
 // seq_len - q_len + i and attends keys 0..position (causal) or every key.
 //
 // A CTA owns 256 query rows of one (request, query head): two tiles of 128
-// rows that share every K/V tile, each with its own softmax warpgroup and its
-// own MMA issuer warp, so the tensor cores work on one tile's chain of
-// dependent MMAs while the other tile's softmax runs.  Roles in a CTA of 352
-// threads:
+// rows that share every K/V tile, each with its own softmax warpgroup.  Roles
+// in a CTA of 320 threads:
 //
 //   warp 8 (producer)  TMA-loads the two query tiles once, then K and V tiles
-//                      of TN keys into a ring of shared-memory slots, one
+//                      of 128 keys into a ring of shared-memory slots, one
 //                      box {64 elements, 1 kv head, block_size rows} per lane
 //                      and block ("Paged attention", k4i.top, section "block
 //                      table": physical_block = block_table[t // block_size]).
-//   warps 9, 10 (MMA)  one per query tile t (warp 9 owns the 512 TMEM
-//                      columns); per key tile k they issue
-//                        S_t = Q_t K_k^T          (M=128, N=TN, K=head_size)
-//                        O_t (+)= P_t V_k         (M=128, N=head_size, K=TN)
+//   warp 9 (MMA)       owns the 512 TMEM columns and issues, for both tiles,
+//                        S_t = Q_t K_k^T          (M=128, N=128, K=head_size)
+//                        O_t (+)= P_t V_k         (M=128, N=head_size, K=128)
 //                      with P_t read from tensor memory (A operand) and V_k as
-//                      an MN-major shared-memory operand.
+//                      an MN-major shared-memory operand, in the order
+//                        PV_0(k), QK_0(k+1), PV_1(k), QK_1(k+1), ...
+//                      so tile 0's softmax of key tile k+1 runs while the
+//                      tensor cores work on tile 1, and the other way round.
 //   warps 0-3 / 4-7    one query row per thread (TMEM lane): scale and mask
-//   (softmax, tile 0/1) the row's TN scores, row max, base-2 exponentials,
-//                      write P over S as 16-bit values (a high part in
-//                      the buffer's first TN/2 columns and the rounded
-//                      remainder after them, so P keeps 16 or more
-//                      significant bits), and at the end
-//                      out = O / l (and the log-sum-exp when asked).
+//   (softmax, tile 0/1) the row's 128 scores, row max, base-2 exponentials,
+//                      write P over S as a 16-bit high part (the buffer's
+//                      first 64 columns) plus the rounded remainder (the
+//                      next 64), so P keeps 16 or more significant bits, and
+//                      at the end out = O / l (and the log-sum-exp when
+//                      asked).
 //
-// Key tiles: P travels as two parts (twice the values MMAs), with TN = 64
-// keys and two score buffers per query tile: the next tile's scores are
-// computed into the other buffer while this tile's softmax runs.
+// Tensor memory: tile t's scores (then P) in columns t*128 .. t*128+127, O_t
+// at 256 + t*128.  The scores of key tile k+1 go over P of key tile k, so a
+// tile's chain is QK -> softmax -> PV -> QK; the two tiles' chains interleave
+// on the tensor cores.  MMAs issued by one thread run in issue order and a
+// commit tracks all of them, so when the scores of key tile k are committed
+// the values MMA of tile k-1 is complete too, and the softmax may rescale O.
 //
 // The running maximum is updated lazily: O and l are rescaled only when a key
 // tile raises a row's maximum by more than 2^8, so most tiles skip the rescale
@@ -55,31 +58,23 @@
 namespace pa {
 namespace pf {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;               // warps 9 and 10: MMA issuers of query tiles 0 and 1
+constexpr int kMmaWarp = 9;         // the MMA issuer of both query tiles
 constexpr int kTileM = 128;         // query rows per tile
 constexpr int kRowsPerCta = 2 * kTileM;
+constexpr int kTileN = 128;         // keys per K/V tile
 constexpr float kRescaleLog2 = 8.f; // lazy-rescale threshold, log2 units
-// Tensor memory: tile t's score columns t*128 .. t*128+127 (one buffer of 128
-// keys, or two of 64 keys at t*128 and t*128 + 64; P is written over the
-// scores it came from), O_t at 256 + t*128.
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQRegion = kTileM * 128;  // 128 query rows x 64 elements x 2 bytes
 
-// Keys per K/V tile: 64 keys and two score buffers, so the next tile's
-// scores are computed while this tile's softmax runs (P, in two parts, lies
-// over the scores it came from).
-template <typename T>
-constexpr int key_tile() { return 64; }
-
-template <int D, int TN>
+template <int D>
 struct Geo {
     static constexpr int kHalves = D / 64;
-    static constexpr int kKVRegion = TN * 128;            // TN key rows x 64 elements x 2 bytes
+    static constexpr int kKVRegion = kTileN * 128;        // 128 key rows x 64 elements x 2 bytes
     static constexpr int kTileBytes = kHalves * kQRegion; // a Q tile
     static constexpr int kKVBytes = kHalves * kKVRegion;  // a K or V tile
-    static constexpr int kSlots = kKVBytes >= 32768 ? 4 : 8; // K/V ring of 128 KB (64 KB for D 64)
+    static constexpr int kSlots = kKVBytes >= 32768 ? 4 : 8; // K/V ring of 128 KB
     static constexpr int kOffKV = 2 * kTileBytes;         // after the two Q tiles
     static constexpr int kOffMisc = kOffKV + kSlots * kKVBytes;
 };
@@ -87,16 +82,16 @@ struct Geo {
 struct Misc {
     uint64_t q_full;
     uint64_t kv_full[8], kv_empty[8];
-    uint64_t s_full[2][2], p_full[2][2]; // [query tile][score buffer]
-    uint64_t pv_done[2], o_done[2];      // a values MMA / the last one of a tile done
-    uint64_t drain[2];
+    uint64_t s_full[2], p_full[2]; // per query tile
+    uint64_t o_done[2];            // the tile's last values MMA done
+    uint64_t drain;
     uint32_t tmem_base;
 };
 
-template <int D, int TN>
+template <int D>
 constexpr int smem_bytes()
 {
-    return 1024 + Geo<D, TN>::kOffMisc + (int)sizeof(Misc);
+    return 1024 + Geo<D>::kOffMisc + (int)sizeof(Misc);
 }
 
 template <typename T>
@@ -150,10 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap pool_map,
                       const __grid_constant__ CUtensorMap q_map, const PrefillParams p)
 {
-    constexpr int kTileN = key_tile<T>();
-    constexpr int NB = kTileN == 64 ? 2 : 1;     // score buffers per query tile
-    constexpr int kChunkUnit = 128 / kTileN;     // key-split chunks come in units of 128 keys
-    using Gm = Geo<D, kTileN>;
+    using Gm = Geo<D>;
     constexpr int kKVRegion = Gm::kKVRegion;
     constexpr int NH = Gm::kHalves;
     constexpr int TB = Gm::kTileBytes;
@@ -165,7 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // P travels as a high part plus the rounded remainder (two MMAs on the
     // same V): a 16-bit P alone (8 or 11 significant bits) puts the
     // relative error of a row whose keys' values cancel above 1e-2.
-    constexpr bool kSplitP = true;
     constexpr uint32_t kIdescS = idesc_f16_f32(kFmt, 0, 0, kTileM, kTileN);
     constexpr uint32_t kIdescO = idesc_f16_f32(kFmt, 0, 1, kTileM, D);
 
@@ -214,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i0 = qb * rows_cta;
     const int ctx = L - q_len;
     // Keys of this CTA: [kt0 * 128, key_hi) (the whole request unless split).
-    const int kt0 = csplit * p.chunk_tiles * kChunkUnit;
-    const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles * kChunkUnit) * kTileN) : L;
+    const int kt0 = csplit * p.chunk_tiles;
+    const int key_hi = nsplit > 1 ? min(L, (kt0 + p.chunk_tiles) * kTileN) : L;
     // Output rows in T, or float32 (out_f32: the cascade's parts).
     const size_t out_elem0 = (size_t)csplit * (size_t)p.part_stride;
     float *const lse_base = p.lse ? p.lse + (size_t)csplit * (size_t)p.lse_part_stride : nullptr;
@@ -245,24 +236,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     const bool tail = (kt0 + n) * kTileN > L; // the last key tile reaches past seq_len
-    const int fixer = nt[1] == n ? 1 : 0;
+    // The softmax warpgroup that zeroes the last key tile's V rows past
+    // seq_len: tile 0 whenever it reads that tile (its values MMA comes
+    // first), else tile 1.
+    const int fixer = nt[0] == n ? 0 : 1;
 
     if (tid == 0) {
         mbar_init(&m->q_full, 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&m->kv_full[i], 1);
-            mbar_init(&m->kv_empty[i], 2); // one arrival per MMA issuer warp
+            mbar_init(&m->kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(&m->s_full[i][b], 1);
-                mbar_init(&m->p_full[i][b], 4);
-            }
-            mbar_init(&m->pv_done[i], 1);
+            mbar_init(&m->s_full[i], 1);
+            mbar_init(&m->p_full[i], 4);
             mbar_init(&m->o_done[i], 1);
         }
-        mbar_init(&m->drain[0], 1);
-        mbar_init(&m->drain[1], 1);
+        mbar_init(&m->drain, 1);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -328,126 +318,110 @@ __global__ void __launch_bounds__(kThreads, 1)
                             &pool_map, &m->kv_full[slot], hf * 64, kvh, row, plane);
             }
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // ================================= MMA issuer of query tile t
-        // The two tiles' chains of dependent MMAs are issued by separate
-        // warps, so the tensor cores overlap them.  Every K/V slot use gets
-        // one arrival from each warp: a commit after its MMAs read the slot,
-        // or a plain arrive when its tile does not need that key tile.
-        const int t = warp - kMmaWarp;
-        const int ntt = nt[t];
-        // S_t[buffer] = Q_t K^T into one of the tile's two score buffers.
-        auto issue_qk = [&](int slot, int buf) {
-            const uint32_t qa = smem_addr(smem + t * TB);
-            const uint32_t ka = smem_addr(smem + Gm::kOffKV + slot * KB);
+    } else if (warp == kMmaWarp) {
+        // ============================================ MMA issuer of both tiles
+        // Shared-memory descriptors are formed once: a K/V slot's descriptor is
+        // the ring's base descriptor plus the slot offset, and each 16-wide
+        // step adds a constant, so issuing an MMA costs one 64-bit add
+        // instead of a chain of address arithmetic.
+        const uint64_t q_desc[2] = {smem_desc_sw128(smem_addr(smem), 16, 1024),
+                                    smem_desc_sw128(smem_addr(smem + TB), 16, 1024)};
+        const uint64_t k_desc0 = smem_desc_sw128(smem_addr(smem + Gm::kOffKV), 16, 1024);
+        const uint64_t v_desc0 = smem_desc_sw128(smem_addr(smem + Gm::kOffKV), kKVRegion, 1024);
+        auto slot_off = [](int slot) { return (uint64_t)((uint32_t)(slot * KB) >> 4); };
+        // S_t = Q_t K^T into tile t's score buffer.
+        auto issue_qk = [&](int t, int slot) {
+            const uint64_t kd = k_desc0 + slot_off(slot);
+            const uint64_t qd = q_desc[t];
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t qoff = (uint32_t)((kk >> 2) * kQRegion + (kk & 3) * 32);
-                const uint32_t koff = (uint32_t)((kk >> 2) * kKVRegion + (kk & 3) * 32);
-                umma_f16(tmem + (uint32_t)(t * 128 + buf * kTileN), smem_desc_sw128(qa + qoff, 16, 1024),
-                         smem_desc_sw128(ka + koff, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                const uint64_t qo = (uint64_t)(((kk >> 2) * kQRegion + (kk & 3) * 32) >> 4);
+                const uint64_t ko = (uint64_t)(((kk >> 2) * kKVRegion + (kk & 3) * 32) >> 4);
+                umma_f16(tmem + (uint32_t)(t * 128), qd + qo, kd + ko, kIdescS, kk > 0 ? 1u : 0u);
             }
-            umma_commit(&m->s_full[t][buf]);
+            umma_commit(&m->s_full[t]);
         };
-        // O_t (+)= P_t V with P read from the score buffer it was written over.
-        auto issue_pv = [&](int slot, int buf, bool acc) {
-            const uint32_t va = smem_addr(smem + Gm::kOffKV + slot * KB);
-            const uint32_t pa = tmem + (uint32_t)(t * 128 + buf * kTileN);
+        // O_t (+)= P_t V with P (high parts, then low parts 64 columns on)
+        // read from the score buffer it was written over.
+        auto issue_pv = [&](int t, int slot, bool acc) {
+            const uint64_t vd0 = v_desc0 + slot_off(slot);
+            const uint32_t pa = tmem + (uint32_t)(t * 128);
+            const uint32_t od = tmem + (uint32_t)(256 + t * 128);
 #pragma unroll
             for (int kk = 0; kk < kTileN / 16; ++kk) {
-                const uint64_t vd = smem_desc_sw128(va + kk * 2048, kKVRegion, 1024);
-                umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128), pa + (uint32_t)(kk * 8), vd, kIdescO,
-                                (acc || kk > 0) ? 1u : 0u);
-                if (kSplitP) // the low parts of P, kTileN / 2 columns further on
-                    umma_f16_tmem_a(tmem + (uint32_t)(256 + t * 128),
-                                    pa + (uint32_t)(kTileN / 2 + kk * 8), vd, kIdescO, 1u);
+                const uint64_t vd = vd0 + (uint64_t)((kk * 2048) >> 4);
+                umma_f16_tmem_a(od, pa + (uint32_t)(kk * 8), vd, kIdescO, (acc || kk > 0) ? 1u : 0u);
+                umma_f16_tmem_a(od, pa + (uint32_t)(kTileN / 2 + kk * 8), vd, kIdescO, 1u);
             }
-            if (NB == 2)
-                umma_commit(&m->pv_done[t]);
-        };
-        // release a slot: commit after this warp's MMAs, or arrive at once
-        auto release = [&](int slot, bool used) {
-            if (used)
-                umma_commit(&m->kv_empty[slot]);
-            else
-                mbar_arrive(&m->kv_empty[slot]);
         };
         bool ok = warp_wait(&m->q_full, 0, lane) && warp_wait(&m->kv_full[0], 0, lane);
         if (ok) {
             tc_fence_after_sync();
             if (lane == 0) {
-                if (ntt > 0)
-                    issue_qk(0, 0);
-                release(0, ntt > 0);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    if (nt[t] > 0)
+                        issue_qk(t, 0);
+                umma_commit(&m->kv_empty[0]); // K of key tile 0 read by both
             }
             __syncwarp();
         }
-        // Per key tile k.  Two score buffers: first the scores of tile k+1 into
-        // the other buffer (its previous contents, P of tile k-1, were read by
-        // the values MMA issued before, and MMAs run in issue order), so they
-        // are computed while the softmax of tile k runs; then the values of
-        // tile k once its P is written.  One buffer: the values of tile k, then
-        // the scores of tile k+1 over its P.  Each slot use is released only
-        // after its load has landed, so a warp whose tile needs no more keys
-        // still follows the producer one use at a time (two releases can
-        // never fall into one barrier phase).
+        // Per key tile k: for each tile t that needs it, the values of k once
+        // P_t(k) is written, then the scores of k+1 over that P (the MMAs run
+        // in issue order).  V of k is released after both tiles' values
+        // MMAs, K of k+1 after both tiles' scores MMAs.  Tile 0 goes first,
+        // so tile 0's softmax of k+1 overlaps tile 1's MMAs and tile 1's
+        // softmax overlaps tile 0's next values and scores.
         for (int k = 0; ok && k < n; ++k) {
             const int gv = 2 * k + 1, sv = gv % S;
             const int gk = 2 * k + 2, sk = gk % S;
-            const bool use = k < ntt, next = k + 1 < n, nuse = k + 1 < ntt;
-            if constexpr (NB == 2) {
-                if (next) {
-                    ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
-                    if (!ok)
-                        break;
-                    tc_fence_after_sync();
-                    if (lane == 0) {
-                        if (nuse)
-                            issue_qk(sk, (k + 1) & 1);
-                        release(sk, nuse);
-                    }
-                    __syncwarp();
-                }
-            }
-            ok = warp_wait(&m->kv_full[sv], (gv / S) & 1, lane);
-            if (ok && use) {
-                // The last tile's rows past seq_len are zeroed by one softmax
-                // warpgroup before it hands over its P.
-                const int kb = k % NB, kph = (k / NB) & 1;
-                if (tail && k == n - 1)
-                    ok = warp_wait(&m->p_full[fixer][kb], kph, lane);
-                if (ok)
-                    ok = warp_wait(&m->p_full[t][kb], kph, lane);
-                if (ok) {
-                    tc_fence_after_sync();
+            const bool next = k + 1 < n;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!ok || k >= nt[t])
+                    continue;
+                // Before tile 0's MMAs: V of k, K of k+1 and P_0(k), each
+                // awaited by its own lane at the same time; before tile 1's
+                // (issued after tile 0's when both need k): P_1(k).
+                bool w = true;
+                if (t == 0 || k >= nt[0]) {
                     if (lane == 0)
-                        issue_pv(sv, kb, k > 0);
+                        w = mbar_wait(&m->kv_full[sv], (gv / S) & 1);
+                    else if (lane == 1 && next)
+                        w = mbar_wait(&m->kv_full[sk], (gk / S) & 1);
+                    else if (lane == 2)
+                        w = mbar_wait(&m->p_full[t], k & 1);
+                } else if (lane == 2) {
+                    w = mbar_wait(&m->p_full[t], k & 1);
                 }
-            }
-            if constexpr (NB == 1) {
-                if (ok && next)
-                    ok = warp_wait(&m->kv_full[sk], (gk / S) & 1, lane);
+                ok = __all_sync(0xffffffffu, w);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                if (lane == 0) {
+                    issue_pv(t, sv, k > 0);
+                    if (k + 1 < nt[t])
+                        issue_qk(t, sk);
+                    else
+                        umma_commit(&m->o_done[t]); // the tile's last values MMA
+                }
+                __syncwarp();
             }
             if (!ok)
                 break;
-            tc_fence_after_sync();
             if (lane == 0) {
-                if (NB == 1 && nuse)
-                    issue_qk(sk, 0);
-                else if (use && !nuse)
-                    umma_commit(&m->o_done[t]); // the tile's last values MMA
-                release(sv, use);
-                if (NB == 1 && next)
-                    release(sk, nuse);
+                umma_commit(&m->kv_empty[sv]);
+                if (next)
+                    umma_commit(&m->kv_empty[sk]);
             }
             __syncwarp();
         }
         if (!ok && lane == 0)
             atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-        // Drain: every MMA this warp issued completes before TMEM is freed.
+        // Drain: every MMA issued completes before TMEM is freed.
         if (lane == 0)
-            umma_commit(&m->drain[t]);
-        warp_wait(&m->drain[t], 0, lane);
+            umma_commit(&m->drain);
+        warp_wait(&m->drain, 0, lane);
     } else {
         // =========================================== softmax / epilogue (tiles 0, 1)
         const int wg = warp >> 2;
@@ -464,9 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             for (int k = 0; k < ntt; ++k) {
-                const int buf = k % NB;
-                const uint32_t sb = s_addr + (uint32_t)(buf * kTileN); // this tile's score buffer
-                ok = warp_wait(&m->s_full[wg][buf], (k / NB) & 1, lane);
+                const uint32_t sb = s_addr; // this tile's score buffer
+                ok = warp_wait(&m->s_full[wg], k & 1, lane);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
@@ -505,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // p = 2^(S * scale*log2e - m): one packed FFMA per two keys and
                 // one ex2 per key; the row sum in two packed chains.  P goes
-                // over the scores it came from (bf16: high parts in the first
-                // kTileN / 2 columns of the buffer, rounded remainders after).
+                // over the scores it came from: high parts in the first
+                // kTileN / 2 columns of the buffer, rounded remainders after.
                 const float nmu = m_used == -INFINITY ? 0.f : -m_used;
                 const float2 qs2 = make_float2(qs, qs), nmu2 = make_float2(nmu, nmu);
                 float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -521,24 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 pp = make_float2(ex2(z.x), ex2(z.y));
                         l2[j & 1] = __fadd2_rn(l2[j & 1], pp);
                         pk[j] = pack2<T>(pp.x, pp.y);
-                        if (kSplitP) {
-                            const float2 hf = unpack2<T>(pk[j]);
-                            lo[j] = pack2<T>(pp.x - hf.x, pp.y - hf.y);
-                        }
+                        const float2 hf = unpack2<T>(pk[j]);
+                        lo[j] = pack2<T>(pp.x - hf.x, pp.y - hf.y);
                     }
                     tmem_st16(sb + (uint32_t)(c * 16), pk);
-                    if (kSplitP)
-                        tmem_st16(sb + (uint32_t)(kTileN / 2 + c * 16), lo);
+                    tmem_st16(sb + (uint32_t)(kTileN / 2 + c * 16), lo);
                 }
                 l += (l2[0].x + l2[1].x) + (l2[0].y + l2[1].y);
                 if (__any_sync(0xffffffffu, need)) {
-                    // O must hold the values of key tiles 0..k-1.  With two
-                    // score buffers the values MMA of tile k-1 may still run
-                    // (the next scores were issued before it), so wait for
-                    // it; with one, S_k was committed after it.  Done after P
-                    // is written so the scores' registers are free.
-                    if (NB == 2 && !warp_wait(&m->pv_done[wg], (k - 1) & 1, lane))
-                        ok = false;
+                    // O holds the values of key tiles 0..k-1: the scores of k
+                    // were committed after that values MMA was issued.  Done
+                    // after P is written so the scores' registers are free.
                     tc_fence_after_sync();
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -572,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&m->p_full[wg][buf]);
+                    mbar_arrive(&m->p_full[wg]);
                 if (!ok)
                     break;
             }
@@ -639,7 +605,7 @@ cudaError_t launch_one(const CUtensorMap &pool, const CUtensorMap &qmap, const P
                        dim3 grid, cudaStream_t stream)
 {
     auto kern = prefill_tc_kernel<T, D, BS>;
-    constexpr int kSmem = smem_bytes<D, key_tile<T>()>();
+    constexpr int kSmem = smem_bytes<D>();
     static unsigned long long done_mask = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
