@@ -406,11 +406,29 @@ def decode_config_entry(name: str, args, peak_gbs: float, w=None) -> dict:
                        "bytes exceed the HBM rate; the unique bytes are the HBM-bound figure")
     if name == "tiny":
         res["note"] = "117,760 KV bytes: launch-latency bound, no HBM roofline applies"
+        res["c_abi_latency"] = c_abi_latency()
     if own:
         del w
     del ws, out
     torch.cuda.empty_cache()
     return res
+
+
+def c_abi_latency() -> dict | None:
+    """The library's own latency floor on the tiny workload, from the host
+    program built beside libpa.so (no Python in its timed loops): host time
+    per API call, device time per call, and a synchronous step."""
+    import paged_kv_cache_136_gb300 as pa
+    tool = os.path.join(os.path.dirname(pa.lib_path()), "pa_latency")
+    if not os.path.exists(tool):
+        return None
+    try:
+        r = subprocess.run([tool, "2000"], capture_output=True, text=True, timeout=120)
+    except subprocess.TimeoutExpired:
+        return {"error": "timed out"}
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip()[-200:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def run_ours(args) -> dict | None:

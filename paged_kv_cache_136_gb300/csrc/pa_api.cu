@@ -257,8 +257,9 @@ static cudaError_t launch_reduce_t(const ReduceParams &p, dim3 grid, cudaStream_
             splitk_reduce_warp_kernel<T, D>,
             dim3((grid.x + kReduceWarpHeads - 1) / kReduceWarpHeads, grid.y),
             dim3(32 * kReduceWarpHeads), 0, stream, p);
-    // Rows of many partitions: four thread groups split a row's partitions.
-    return launch_after_previous(splitk_reduce_kernel<T, D, 4>, grid, dim3(4 * D), 0, stream, p);
+    // Rows of many partitions: one CTA per row, its warps split the partitions.
+    return launch_after_previous(splitk_reduce_kernel<T, D>, grid, dim3(32 * kWideWarps), 0, stream,
+                                 p);
 }
 
 cudaError_t launch_reduce(int dtype, int head_size, const ReduceParams &p, int num_seqs,

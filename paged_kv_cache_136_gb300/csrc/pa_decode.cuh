@@ -410,35 +410,55 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // Log-sum-exp merge of the partitions of one (sequence, query head):
 // M = max_p m_p, out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p.
-// The weights w_p = 2^(m_p - M) are formed once per partition in shared
-// memory (chunks of kReduceChunk partitions) and the normaliser is a block
-// sum of w_p l_p.  GR groups of D threads split the partitions (group g
-// takes p = g, g + GR, ...); each thread sums its head_size element with four
-// independent accumulators, and the groups' sums are added at the end.  Many
-// partitions (long sequences) want GR > 1, so the loads of all partitions of
-// a row are in flight at once instead of one after another.
+// Rows of many partitions (long sequences): one CTA per row.  The weights
+// w_p = 2^(m_p - M) are formed once per partition in shared memory (chunks
+// of kReduceChunk partitions) and the normaliser is a block sum of w_p l_p.
+// The kWideWarps warps split the partitions (warp w takes p = w, w + 16, ...);
+// lane j loads elements j*E .. j*E+E-1 of a partition's head_size-vector as
+// one vector load, so a warp reads a partition's vector in one coalesced
+// request and all warps' requests are in flight together; the warps' sums are
+// added through shared memory at the end.
 constexpr int kReduceChunk = 512;
+constexpr int kWideWarps = 16;
 
-template <typename T, int D, int GR>
-__global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParams p)
+template <int E>
+struct VecF;
+template <>
+struct VecF<4> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[4])
+    {
+        const float4 x = *reinterpret_cast<const float4 *>(p);
+        v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    }
+};
+template <>
+struct VecF<2> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[2])
+    {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        v[0] = x.x, v[1] = x.y;
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kWideWarps) splitk_reduce_kernel(const ReduceParams p)
 {
-    constexpr int NT = D * GR;
-    constexpr int NW = NT / 32;
+    constexpr int NT = 32 * kWideWarps;
+    constexpr int E = D / 32; // elements per lane
     __shared__ float w_s[kReduceChunk];
-    __shared__ float red_s[NW];
-    __shared__ float num_s[GR > 1 ? GR - 1 : 1][D];
+    __shared__ float red_s[kWideWarps];
+    __shared__ float acc_s[kWideWarps][D];
     __shared__ float bc_s;
     griddep_wait(); // the partition kernel's states are complete
-    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
-    const int d = tid % D, g = tid / D, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.len_cap ? p.len_cap : L);
     const int np = (L + p.part_tokens - 1) / p.part_tokens;
     const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
     const size_t out0 = ((size_t)s * p.num_heads + h) * D;
     if (np == 0) {
-        if (g == 0)
-            put_out<T>(p.out, out0 + d, 0.f, p.out_f32);
+        if (tid < D)
+            put_out<T>(p.out, out0 + tid, 0.f, p.out_f32);
         if (p.lse && tid == 0)
             p.lse[(size_t)s * p.num_heads + h] = -INFINITY;
         return;
@@ -458,7 +478,7 @@ __global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParam
         __syncthreads();
         if (tid == 0) {
             float r = red_s[0];
-            for (int i = 1; i < NW; ++i)
+            for (int i = 1; i < kWideWarps; ++i)
                 r = is_max ? fmaxf(r, red_s[i]) : r + red_s[i];
             bc_s = r;
         }
@@ -470,7 +490,10 @@ __global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParam
         M = fmaxf(M, p.ws_ml[(row0 + q) * 2]);
     M = block_reduce(M, true);
     float den = 0.f; // this thread's share of sum_p w_p l_p
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    float a[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        a[e] = 0.f;
     for (int q0 = 0; q0 < np; q0 += kReduceChunk) {
         const int nq = min(kReduceChunk, np - q0);
         __syncthreads();
@@ -480,31 +503,29 @@ __global__ void __launch_bounds__(D * GR) splitk_reduce_kernel(const ReduceParam
             den = fmaf(w, p.ws_ml[(row0 + q0 + q) * 2 + 1], den);
         }
         __syncthreads();
-        const float *o = p.ws_o + (row0 + q0) * D + d;
-        int q = g;
-#pragma unroll 2
-        for (; q + 3 * GR < nq; q += 4 * GR) {
-            a0 = fmaf(w_s[q], o[(size_t)q * D], a0);
-            a1 = fmaf(w_s[q + GR], o[(size_t)(q + GR) * D], a1);
-            a2 = fmaf(w_s[q + 2 * GR], o[(size_t)(q + 2 * GR) * D], a2);
-            a3 = fmaf(w_s[q + 3 * GR], o[(size_t)(q + 3 * GR) * D], a3);
+        const float *o = p.ws_o + (row0 + q0) * D + lane * E;
+#pragma unroll 4
+        for (int q = warp; q < nq; q += kWideWarps) {
+            const float w = w_s[q];
+            float v[E];
+            VecF<E>::load(o + (size_t)q * D, v);
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                a[e] = fmaf(w, v[e], a[e]);
         }
-        for (; q < nq; q += GR)
-            a0 = fmaf(w_s[q], o[(size_t)q * D], a0);
     }
     den = block_reduce(den, false);
-    float num = (a0 + a1) + (a2 + a3);
-    if (GR > 1) {
-        if (g > 0)
-            num_s[g - 1][d] = num;
-        __syncthreads();
-        if (g == 0)
-            for (int i = 0; i < GR - 1; ++i)
-                num += num_s[i][d];
-    }
-    if (g == 0) {
-        put_out<T>(p.out, out0 + d, num / den, p.out_f32);
-        if (p.lse && d == 0)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        acc_s[warp][lane * E + e] = a[e];
+    __syncthreads();
+    if (tid < D) {
+        float num = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWideWarps; ++w)
+            num += acc_s[w][tid];
+        put_out<T>(p.out, out0 + tid, num / den, p.out_f32);
+        if (p.lse && tid == 0)
             p.lse[(size_t)s * p.num_heads + h] = (M + __log2f(den)) * 0.69314718055994531f;
     }
 }
