@@ -398,6 +398,8 @@ static pa_status check_decode_args(const void *out, const void *q, const void *k
 }
 
 static const float kLog2e = 1.4426950408889634f;
+// Full partitions per run item of the split-K work list (see the plan kernel).
+static const int kSplitRun = 4;
 
 extern "C" {
 
@@ -624,15 +626,31 @@ static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const 
             return PA_ERR_CUDA;
         uint32_t *hdr = reinterpret_cast<uint32_t *>(wsb);
         uint32_t *units = reinterpret_cast<uint32_t *>(wsb + lay.units);
+        const int sms = sm_count(&e);
+        if (!sms)
+            return PA_ERR_CUDA;
+        const size_t bound = (size_t)num_seqs * ngroups * parts;
+        const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
+        // Runs of kSplitRun full partitions per item for long sequences; each
+        // sequence keeps enough trailing single partitions that about three
+        // waves of single items end the work list.
+        int max_run = 1, keep_single = 0;
+        if (parts > 1 && parts <= 4096) {
+            max_run = kSplitRun;
+            const long long pairs = (long long)num_seqs * ngroups;
+            const long long want = 3LL * grid;
+            keep_single = (int)((want + pairs - 1) / pairs) - 1;
+            keep_single = keep_single < 0 ? 0 : keep_single;
+        }
         e = dtype == PA_BF16
                 ? launch_after_previous(tc::splitk_plan_kernel<__nv_bfloat16>, dim3(1), dim3(1024), 0,
                                         s, seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__nv_bfloat16 *>(out), lse,
-                                        err, out_f32 ? 1 : 0)
+                                        err, out_f32 ? 1 : 0, max_run, keep_single)
                 : launch_after_previous(tc::splitk_plan_kernel<__half>, dim3(1), dim3(1024), 0, s,
                                         seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__half *>(out), lse, err,
-                                        out_f32 ? 1 : 0);
+                                        out_f32 ? 1 : 0, max_run, keep_single);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
         tc::TcParams t = {};
@@ -655,11 +673,7 @@ static pa_status decode_splitk_impl(void *out, float *lse, const void *q, const 
         t.qscale = scale * kLog2e;
         t.lse = lse;
         t.out_f32 = out_f32 ? 1 : 0;
-        const int sms = sm_count(&e);
-        if (!sms)
-            return PA_ERR_CUDA;
-        const size_t bound = (size_t)num_seqs * ngroups * parts;
-        const unsigned grid = (unsigned)(bound < (size_t)sms ? bound : (size_t)sms);
+        t.runs = max_run > 1 ? 1 : 0;
         auto launch = dtype == PA_BF16 ? launch_decode_tc_bf16 : launch_decode_tc_f16;
         mark_before(s);
         e = launch(block_size, group, hg, true, pmap, qmap, t, dim3(grid), s);
@@ -1119,11 +1133,11 @@ static pa_status decode_fp8_impl(void *out, const void *q, const void *kv_cache,
                 ? launch_after_previous(tc::splitk_plan_kernel<__nv_bfloat16>, dim3(1), dim3(1024), 0,
                                         s, seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__nv_bfloat16 *>(out),
-                                        static_cast<float *>(nullptr), err, 0)
+                                        static_cast<float *>(nullptr), err, 0, 1, 0)
                 : launch_after_previous(tc::splitk_plan_kernel<__half>, dim3(1), dim3(1024), 0, s,
                                         seq_lens, num_seqs, num_heads, ngroups, partition_size,
                                         len_cap, hdr, units, static_cast<__half *>(out),
-                                        static_cast<float *>(nullptr), err, 0);
+                                        static_cast<float *>(nullptr), err, 0, 1, 0);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
         e = dtype == PA_BF16 ? launch_quantize_q_bf16(q, qparts, qscales, rows, s)

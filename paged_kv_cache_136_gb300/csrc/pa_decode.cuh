@@ -506,7 +506,11 @@ __global__ void __launch_bounds__(32 * kWideWarps) splitk_reduce_kernel(const Re
         const float *o = p.ws_o + (row0 + q0) * D + lane * E;
 #pragma unroll 4
         for (int q = warp; q < nq; q += kWideWarps) {
+            // A partition covered by a run of the one before it has weight 0
+            // and no vector: skip it.
             const float w = w_s[q];
+            if (w == 0.f)
+                continue;
             float v[E];
             VecF<E>::load(o + (size_t)q * D, v);
 #pragma unroll
@@ -585,7 +589,11 @@ __global__ void __launch_bounds__(32 * kReduceWarpHeads)
         acc[e] = 0.f;
 #pragma unroll 4
     for (int q = 0; q < np; ++q) {
+        // A partition covered by a run of the one before it has weight 0 and
+        // no vector: skip it.
         const float wq = __shfl_sync(0xffffffffu, w, q);
+        if (wq == 0.f)
+            continue;
 #pragma unroll
         for (int e = 0; e < E; ++e)
             acc[e] = fmaf(wq, o[(size_t)q * D + 32 * e], acc[e]);

@@ -82,7 +82,7 @@ constexpr int kOffMisc = kOffP + 2 * kPBytes;
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagStop = 4;
 
 struct StageDesc {
-    int s, group, part, nvalid, flags, nparts, pad0, pad1;
+    int s, group, part, nvalid, flags, nparts, run, pad1;
 };
 
 struct Misc {
@@ -108,7 +108,8 @@ struct TcParams {
     unsigned int *err;
     // split-K workspace (null in one-pass mode)
     uint32_t *hdr;               // [0] work counter, [1] total items
-    const uint32_t *units;       // (s << 16) | partition
+    const uint32_t *units;       // (s << 16) | partition, or with runs
+                                 // (s << 16) | ((run - 1) << 12) | partition
     float *ws_o;                 // [B, H, max_parts, 128]
     float *ws_ml;                // [B, H, max_parts, 2]
     int num_heads, num_kv_heads, num_groups, num_blocks, max_blocks;
@@ -116,6 +117,7 @@ struct TcParams {
     float qscale;
     float *lse;                  // [B, H] natural-log softmax denominators, or null
     int out_f32;                 // out holds float32 rows instead of T
+    int runs;                    // units carry a run length (see the plan kernel)
 };
 
 template <typename T>
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // changes.
         int nstep = 0;                    // steps of the next item done so far
         uint32_t nj_raw = 0, nj = 0, nu = 0;
-        int nL_raw = 0, ncur = -1, nnxt = -1, n_s = 0, n_group = 0, n_part = 0;
+        int nL_raw = 0, ncur = -1, nnxt = -1, n_s = 0, n_group = 0, n_part = 0, n_run = 1;
         bool n_have = false;
         auto next_step = [&]() {
             if (nstep == 0) {
@@ -261,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (nstep == 2 && n_have) {
                 n_group = (int)(nj % p.num_groups);
                 n_s = (int)(nu >> 16);
-                n_part = (int)(nu & 0xFFFFu);
+                n_part = p.runs ? (int)(nu & 0xFFFu) : (int)(nu & 0xFFFFu);
+                n_run = p.runs ? (int)((nu >> 12) & 0xFu) + 1 : 1;
                 nL_raw = __ldg(p.seq_lens + n_s);
                 // Table entries past the item's end are loaded but never used.
                 const int jb = n_part * p.part_tokens / BS;
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur = -1, nxt = -1;
         while (alive) {
             // ---- next work item: (sequence, group of HG kv heads, partition)
-            int s = 0, group = 0, part = 0, L = 0, nparts = 1;
+            int s = 0, group = 0, part = 0, L = 0, nparts = 1, run = 1;
             bool have = false;
             if (SPLIT) {
                 while (nstep < 3)
@@ -284,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s = n_s;
                     group = n_group;
                     part = n_part;
+                    run = n_run;
                     int Lr = nL_raw;
                     if (lane == 0)
                         Lr = clamp_len(Lr, p.len_cap, p.err);
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             const int kvh0 = group * HG;
             const int tok0 = SPLIT ? part * p.part_tokens : 0;
-            const int tok1 = SPLIT ? min(L, tok0 + p.part_tokens) : L;
+            const int tok1 = SPLIT ? min(L, tok0 + run * p.part_tokens) : L;
             const int jb0 = tok0 / BS;
             const int jend = (tok1 + BS - 1) / BS;
             const int nst = (tok1 - tok0 + TPS - 1) / TPS;
@@ -398,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     d.nvalid = nvalid;
                     d.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
                     d.nparts = nparts;
+                    d.run = run;
                     mbar_arrive_expect_tx(&m->full[slot], (uint32_t)(nch * 2 * BOX_BYTES));
                 }
                 __syncwarp();
@@ -515,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // values MMA overlaps work instead of stalling the ring at every item
         // change.  Its column sums of l wait in red2[fin_par].
         bool fin = false;
-        int fin_s = 0, fin_group = 0, fin_part = 0, fin_nparts = 1, fin_par = 0;
+        int fin_s = 0, fin_group = 0, fin_part = 0, fin_nparts = 1, fin_par = 0, fin_run = 1;
         float fin_m = 0.f; // running max of column t (t < NV) of that item
         int par = 0;
         // o = alpha*o + O_high + O_low for stage k, then free the O buffer.
@@ -565,6 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t == n) {
                         p.ws_ml[row * 2] = fin_m;
                         p.ws_ml[row * 2 + 1] = l[n];
+                    }
+                }
+                // A run covered the next fin_run - 1 partitions too: they
+                // carry no weight (the reduce skips them).
+                if (fin_run > 1 && t < NV) {
+                    const size_t row = (head0 + t) * p.max_parts + fin_part;
+                    for (int q = 1; q < fin_run; ++q) {
+                        p.ws_ml[(row + q) * 2] = -INFINITY;
+                        p.ws_ml[(row + q) * 2 + 1] = 0.f;
                     }
                 }
             }
@@ -709,6 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fin_s = d.s;
             fin_group = d.group;
             fin_part = d.part;
+            fin_run = d.run;
             fin_nparts = d.nparts;
             fin_par = par;
             par ^= 1;
@@ -723,13 +738,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Split-K plan (one CTA): zero the work counter, write zero
-// rows for empty sequences, and list every (sequence, partition) unit
-// longest first -- all full partitions, then each sequence's last, partial
-// partition in descending size (a counting sort over kPlanBuckets size
-// buckets) -- so the dynamically claimed work ends with the shortest items.
-// The item count (units x head groups) goes to hdr[1].
+// Split-K plan (one CTA): zero the work counter, write zero rows for empty
+// sequences, and list the work units of every sequence longest first, so the
+// dynamically claimed work ends with the shortest items:
+//   1. runs: max_run consecutive full partitions of one sequence, taken by
+//      one CTA as one item (fewer item changes, one partial state per run);
+//   2. single full partitions: a sequence's last keep_single full
+//      partitions (and those left over from its runs), in sequence order;
+//   3. each sequence's last, possibly partial, partition, in descending size
+//      (a counting sort over kPlanBuckets size buckets).
+// max_run == 1 lists every full partition singly.  A unit is (s << 16) |
+// partition, or with runs (s << 16) | ((run - 1) << 12) | partition (the
+// host enables runs only with fewer than 4096 partitions per sequence).  The
+// item count (units x head groups) goes to hdr[1].
 constexpr int kPlanBuckets = 256;
+constexpr int kRunShift = 12; // run length field of a unit, when runs are on
 
 template <typename T>
 __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_lens, int B, int H,
@@ -737,46 +760,75 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
                                                            int len_cap, uint32_t *hdr,
                                                            uint32_t *units,
                                                            T *out, float *lse,
-                                                           unsigned int *err, int out_f32)
+                                                           unsigned int *err, int out_f32,
+                                                           int max_run, int keep_single)
 {
-    __shared__ uint32_t warp_tot[32];
+    __shared__ unsigned long long warp_tot[32];
     __shared__ uint32_t bucket[kPlanBuckets];
-    __shared__ uint32_t carry_s;
+    __shared__ unsigned long long carry_s;
+    __shared__ uint32_t total_runs_s;
     // Launched as the dependent of the kernel before it (the cache write):
     // wait for its results, let the decode grid start its prologue.
     griddep_wait();
     griddep_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
+    const int R = max_run > 1 ? max_run : 1;
     for (int i = tid; i < kPlanBuckets; i += blockDim.x)
         bucket[i] = 0;
     if (tid == 0) {
         hdr[0] = 0;
         carry_s = 0;
+        total_runs_s = 0;
     }
     __syncthreads();
-    auto seq_len = [&](int s) {
+    auto seq_len = [&](int s, bool flag) {
         int L = seq_lens[s];
         if (L < 0 || L > len_cap) {
-            atomicOr(err, PA_DEVERR_SEQ_LEN_);
+            if (flag)
+                atomicOr(err, PA_DEVERR_SEQ_LEN_);
             L = L < 0 ? 0 : len_cap;
         }
         return L;
+    };
+    // Runs and single full partitions of a sequence of L tokens.
+    auto split_full = [&](int L, uint32_t &nruns, uint32_t &nsingle) {
+        const int n = (L + part_tokens - 1) / part_tokens;
+        const int nfull = n > 0 ? n - 1 : 0;
+        const int in_runs = (R > 1 && nfull > keep_single) ? nfull - keep_single : 0;
+        nruns = (uint32_t)(in_runs / R);
+        nsingle = (uint32_t)(nfull - (int)nruns * R);
     };
     // Size bucket of a last partition of `last` tokens: larger first.
     auto size_bucket = [&](int last) {
         const int b = (int)(((long long)(last - 1) * kPlanBuckets) / part_tokens);
         return kPlanBuckets - 1 - (b < kPlanBuckets - 1 ? b : kPlanBuckets - 1);
     };
-    // Pass 1: full partitions in sequence order; histogram of the last ones.
+    // Pass 0: how many run units come before the single partitions.
+    if (R > 1) {
+        uint32_t mine = 0;
+        for (int s = tid; s < B; s += blockDim.x) {
+            uint32_t nr, ns;
+            split_full(seq_len(s, false), nr, ns);
+            mine += nr;
+        }
+        if (mine)
+            atomicAdd(&total_runs_s, mine);
+        __syncthreads();
+    }
+    const uint32_t total_runs = total_runs_s;
+    // Pass 1: runs and single full partitions in sequence order (two
+    // prefix sums packed in one 64-bit scan: runs high, singles low);
+    // histogram of the last partitions.
     for (int c0 = 0; c0 < B; c0 += blockDim.x) {
         const int s = c0 + tid;
-        uint32_t nfull = 0;
+        uint32_t nr = 0, ns = 0;
+        int L = 0;
         if (s < B) {
-            const int L = seq_len(s);
+            L = seq_len(s, true);
             const int n = (L + part_tokens - 1) / part_tokens;
             if (n > 0) {
-                nfull = (uint32_t)(n - 1);
+                split_full(L, nr, ns);
                 atomicAdd(&bucket[size_bucket(L - (n - 1) * part_tokens)], 1u);
             } else {
                 for (int i = 0; i < H * 128; ++i)
@@ -786,10 +838,11 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
                         lse[(size_t)s * H + h] = -INFINITY;
             }
         }
-        uint32_t v = nfull;
+        const unsigned long long mine = ((unsigned long long)nr << 32) | ns;
+        unsigned long long v = mine;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, v, off);
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, v, off);
             if (lane >= off)
                 v += y;
         }
@@ -797,28 +850,36 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
             warp_tot[warp] = v;
         __syncthreads();
         if (warp == 0) {
-            uint32_t w = lane < nwarps ? warp_tot[lane] : 0;
+            unsigned long long w = lane < nwarps ? warp_tot[lane] : 0ull;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, w, off);
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, w, off);
                 if (lane >= off)
                     w += y;
             }
             warp_tot[lane] = w; // inclusive prefix over warps
         }
         __syncthreads();
-        const uint32_t base = carry_s + (warp ? warp_tot[warp - 1] : 0) + v - nfull;
-        for (uint32_t q = 0; q < nfull; ++q)
-            units[base + q] = ((uint32_t)s << 16) | q;
+        const unsigned long long base = carry_s + (warp ? warp_tot[warp - 1] : 0ull) + v - mine;
+        const uint32_t rbase = (uint32_t)(base >> 32);
+        const uint32_t sbase = total_runs + (uint32_t)(base & 0xFFFFFFFFull);
+        for (uint32_t q = 0; q < nr; ++q)
+            units[rbase + q] = ((uint32_t)s << 16) | ((uint32_t)(R - 1) << kRunShift) |
+                               (q * (uint32_t)R);
+        for (uint32_t q = 0; q < ns; ++q)
+            units[sbase + q] = ((uint32_t)s << 16) | (nr * (uint32_t)R + q);
         __syncthreads();
         if (tid == 0)
             carry_s += warp_tot[nwarps - 1];
         __syncthreads();
     }
-    // Bucket start offsets after the full partitions (buckets in size order):
-    // an exclusive scan of the counts over the first kPlanBuckets threads,
-    // one bucket each (the kernel is launched with 1024 threads).
+    // Bucket start offsets after the runs and single partitions (buckets in
+    // size order): an exclusive scan of the counts over the first
+    // kPlanBuckets threads, one bucket each (the kernel is launched with
+    // 1024 threads).
     static_assert(kPlanBuckets % 32 == 0 && kPlanBuckets <= 1024, "one bucket per thread");
+    const uint32_t first_last = total_runs + (uint32_t)(carry_s & 0xFFFFFFFFull);
+    __shared__ uint32_t warp_tot32[32];
     uint32_t bc = 0, bi = 0; // this thread's bucket count, inclusive scan in its warp
     if (tid < kPlanBuckets) {
         bc = bucket[tid];
@@ -830,13 +891,13 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
                 bi += y;
         }
         if (lane == 31)
-            warp_tot[warp] = bi;
+            warp_tot32[warp] = bi;
     }
     __syncthreads();
     if (tid < kPlanBuckets) {
-        uint32_t before = carry_s;
+        uint32_t before = first_last;
         for (int w = 0; w < warp; ++w)
-            before += warp_tot[w];
+            before += warp_tot32[w];
         bucket[tid] = before + bi - bc;
         if (tid == kPlanBuckets - 1)
             hdr[1] = (before + bi) * (uint32_t)num_groups;
@@ -844,7 +905,7 @@ __global__ void __launch_bounds__(1024) splitk_plan_kernel(const int32_t *seq_le
     __syncthreads();
     // Pass 2: place each last partition in its bucket.
     for (int s = tid; s < B; s += blockDim.x) {
-        const int L = seq_len(s);
+        const int L = seq_len(s, false);
         const int n = (L + part_tokens - 1) / part_tokens;
         if (n > 0) {
             const uint32_t pos = atomicAdd(&bucket[size_bucket(L - (n - 1) * part_tokens)], 1u);
