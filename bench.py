@@ -162,36 +162,88 @@ def kv_bytes(w) -> int:
     return w.kv_bytes()
 
 
-def _multi_part_rows(w, partition: int) -> int:
-    """(sequence, partition) units of sequences that span several partitions:
-    only those write partial states; a one-partition sequence writes its
-    output row directly."""
-    import torch
-    L = w.seq_lens.to(torch.int64)
-    parts = (L + partition - 1) // partition
-    return int(parts[parts > 1].sum().item())
+SPLIT_RUN = 4   # full partitions per run item of the library's split-K work list
+
+
+def _sm_count() -> int:
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return 152
+
+
+def split_partials(w, partition: int, sms: int | None = None) -> tuple[int, int, int]:
+    """Partial-state traffic of pa_decode_splitk for this workload: (bytes the
+    partition kernel writes, bytes the reduce reads, output bytes the reduce
+    writes).
+
+    It follows the library's split-K work list: with head_size 128 (the
+    tensor-core kernel) a one-partition sequence writes its output directly;
+    a longer one writes one partial state (o: head_size floats, m, l) per
+    work item -- a run of SPLIT_RUN partitions, a single partition or the
+    last one -- and two floats that mark each partition a run covered as
+    empty; each sequence keeps enough trailing single partitions that about
+    three waves of single items (of the persistent grid of at most one CTA
+    per SM) end the list.  The reduce reads every partition's (m, l) and the
+    vectors of the non-empty ones.  With head_size 64 (the CUDA-core kernel)
+    every partition of every sequence writes a partial state and the reduce
+    writes every output row."""
+    import math
+    sms = sms or _sm_count()
+    L = [int(x) for x in w.seq_lens.cpu().tolist()]
+    H, D = w.num_heads, w.head_size
+    el = w.kv_cache.element_size()
+    row_out = H * D * el
+    state = (D + 2) * 4
+    nparts = [(x + partition - 1) // partition for x in L]
+    if D != 128:
+        n_all = sum(nparts)
+        return H * n_all * state, H * n_all * state, sum(1 for n in nparts if n > 0) * row_out
+    G = H // w.num_kv_heads
+    hg = 16 // G if w.num_kv_heads % (16 // G) == 0 else 1
+    groups = w.num_kv_heads // hg
+    max_parts = max(1, math.ceil(max(L + [0]) / partition))
+    grid = min(w.num_seqs * groups * max_parts, sms)
+    runs = 1 < max_parts <= 4096
+    keep = max(0, math.ceil(3 * grid / (w.num_seqs * groups)) - 1) if runs else 0
+    written = read = out_rows = 0
+    for n in nparts:
+        if n <= 1:
+            continue
+        nfull = n - 1
+        in_runs = nfull - keep if runs and nfull > keep else 0
+        nruns = in_runs // SPLIT_RUN
+        items = nruns + (nfull - nruns * SPLIT_RUN) + 1
+        covered = nruns * (SPLIT_RUN - 1)
+        written += H * (items * state + covered * 8)
+        read += H * (n * 8 + items * D * 4)
+        out_rows += 1
+    return written, read, out_rows * row_out
 
 
 def decode_launch_bytes(w, split: bool, partition: int) -> int:
     """Bytes the whole decode call must move: KV rows once, q, out, the
     block-table entries in use, seq_lens, and for split-K the partial states
-    of multi-partition sequences, written by the partition kernel and read
-    back by the reduce."""
+    written by the partition kernel and read back by the reduce."""
     import torch
     el = w.kv_cache.element_size()
     L = w.seq_lens.to(torch.int64)
     nblk = int(((L + w.block_size - 1) // w.block_size).sum().item())
     b = kv_bytes(w) + 2 * w.q.numel() * el + nblk * 4 + w.num_seqs * 4
     if split:
-        b += 2 * _multi_part_rows(w, partition) * w.num_heads * (w.head_size + 2) * 4
+        written, read, _ = split_partials(w, partition)
+        b += written + read
     return b
 
 
 def decode_kernel_bytes(w, split: bool, partition: int) -> int:
     """Bytes the main attention kernel alone must move: KV rows once, q, the
-    block-table entries in use, seq_lens, the output rows of one-partition
-    sequences, and the partial states of multi-partition ones (written once;
-    the reduce reads them and writes those sequences' output rows)."""
+    block-table entries in use, seq_lens, the output rows it writes itself
+    and the partial states (written once; the reduce reads them and writes
+    the other output rows)."""
     import torch
     el = w.kv_cache.element_size()
     L = w.seq_lens.to(torch.int64)
@@ -199,10 +251,8 @@ def decode_kernel_bytes(w, split: bool, partition: int) -> int:
     b = kv_bytes(w) + w.q.numel() * el + nblk * 4 + w.num_seqs * 4
     if not split:
         return b + w.q.numel() * el
-    parts = (L + partition - 1) // partition
-    single = int((parts <= 1).sum().item())
-    row = w.num_heads * w.head_size * el
-    return b + single * row + _multi_part_rows(w, partition) * w.num_heads * (w.head_size + 2) * 4
+    written, _, reduce_out = split_partials(w, partition)
+    return b + (w.q.numel() * el - reduce_out) + written
 
 
 def decode_launches(w, split: bool, partition: int) -> int:

@@ -63,23 +63,38 @@ def test_bench_arguments(argv, expect):
     assert a.config == "long"
 
 
-def test_bench_byte_accounting_counts_partials_of_split_sequences_only():
-    """Algorithmic bytes of the decode call and of its main kernel on a small
-    CPU workload, written out by hand: one sequence of 1 token (one
-    partition, its output row written by the kernel), one of 65 tokens (two
-    partitions of 64: partial states written by the kernel, read by the
-    reduce)."""
+def test_bench_byte_accounting_follows_the_split_work_list():
+    """Algorithmic bytes of the decode call and of its main kernel, written
+    out by hand for two small CPU workloads.
+
+    head_size 64 (the CUDA-core kernel): one sequence of 1 token and one of
+    65 tokens (partitions of 64): every partition writes a partial state,
+    the reduce reads them all and writes both output rows.
+
+    head_size 128 (the tensor-core kernel, 4 kv heads per CTA, 2 head
+    groups): one sequence of 1 token (writes its output directly) and one of
+    321 tokens = 6 partitions of 64, 5 full ones.  With a grid of 2 CTAs the
+    list keeps ceil(3 * 2 / (2 seqs * 2 groups)) - 1 = 1 trailing single
+    full partition, so partitions 0-3 form one run, 4 is single, 5 is the
+    last: 3 partial states, 3 covered partitions marked empty."""
     import bench
     import workload as wl
     w = wl.make("tiny", device="cpu", lengths=[1, 65], seed=1)
-    el, H, Hkv, D, bs = 2, w.num_heads, w.num_kv_heads, w.head_size, w.block_size
+    el, H, Hkv, D = 2, w.num_heads, w.num_kv_heads, w.head_size
     kv = (1 + 65) * Hkv * D * el * 2
     q = 2 * H * D * el
     tables = (1 + 5) * 4 + 2 * 4          # blocks in use (bs 16) + seq_lens
-    partial = H * (D + 2) * 4             # one (sequence, head) partial state
+    state = H * (D + 2) * 4               # one partition's partial state, all heads
     assert bench.kv_bytes(w) == kv
+    assert bench.split_partials(w, 64, sms=2) == (3 * state, 3 * state, q)
     assert bench.decode_launch_bytes(w, False, 64) == kv + 2 * q + tables
-    assert bench.decode_launch_bytes(w, True, 64) == kv + 2 * q + tables + 2 * 2 * partial
+    assert bench.decode_launch_bytes(w, True, 64) == kv + 2 * q + tables + 6 * state
+    assert bench.decode_kernel_bytes(w, True, 64) == kv + q + tables + 3 * state
+
+    w = wl.make("gqa8b", device="cpu", lengths=[1, 321], seed=1)
+    H, Hkv, D = w.num_heads, w.num_kv_heads, w.head_size
+    assert (H, Hkv, D) == (32, 8, 128)
+    written = H * (3 * (D + 2) * 4 + 3 * 8)
+    read = H * (6 * 8 + 3 * D * 4)
     row = H * D * el
-    assert bench.decode_kernel_bytes(w, True, 64) == kv + q + tables + row + 2 * partial
-    assert bench.decode_kernel_bytes(w, False, 64) == kv + 2 * q + tables
+    assert bench.split_partials(w, 64, sms=2) == (written, read, row)
