@@ -128,6 +128,28 @@ def test_partition_size_invariance(pa):
         check_agree(out, one, what=f"partition {P} vs one-pass")
 
 
+def test_split_runs_match_oracle(pa):
+    """A sequence long enough that the split-K work list groups its full
+    partitions into runs of four consecutive partitions (one work item and
+    one partial state each; the partitions a run covers carry zero weight in
+    the reduce), beside a shorter one: with 64-token partitions and two
+    sequences, each keeps its last ceil(3 * 152 / 4) - 1 = 113 full
+    partitions single, so the first sequence's 130 full partitions give 4
+    runs.  Outputs and log-sum-exps match the oracle."""
+    w = wl.make("gqa8b", device="cuda", poison=True, lengths=[64 * 130 + 5, 3000], seed=12)
+    P = 64
+    msl = int(w.seq_lens.max().item())
+    ws = splitk_workspace(pa, w, msl, P)
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.num_seqs, w.num_heads, dtype=torch.float32, device="cuda")
+    pa.pa_decode_splitk_lse(out, lse, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                            w.block_size, msl, ws, P)
+    torch.cuda.synchronize()
+    check_attention(out, oracle_decode(w), what="runs of partitions")
+    check_lse(lse, oracle_decode_lse(w), what="runs of partitions")
+    assert pa.pa_device_errors(clear=True) == 0
+
+
 def test_reduce_many_partitions(pa):
     """More partitions per row than one shared-memory chunk of merge weights
     holds (625 and 514 of 64 tokens: the reduce walks two chunks, with thread
