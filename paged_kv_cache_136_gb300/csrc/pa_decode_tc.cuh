@@ -85,14 +85,26 @@ struct StageDesc {
     int s, group, part, nvalid, flags, nparts, run, pad1;
 };
 
+// Stage descriptors rotate over twice the ring, each with its own barrier:
+// the one of stage k is rewritten for stage k + 2 * kStages, once the scores
+// MMA of stage k + kStages has freed that slot, by which time the softmax of
+// stage k (its last reader) is long done.  The softmax waits on the
+// descriptor's barrier, not on the slot's K barrier: K of stage k + kStages
+// may land before the softmax of stage k starts, and a parity wait cannot
+// tell the two phases apart.
+constexpr int kDescs = 2 * kStages;
+
 struct Misc {
-    StageDesc desc[kStages];
+    StageDesc desc[kDescs];
+    int stop_v[kStages];   // the values warp's stop flag of a slot
     float red[2][4][kNQ];  // per-stage max, double-buffered by stage parity
     float red2[2][4][kNQ]; // normaliser sums at item end, double-buffered by item
     int bcast[4];
     uint32_t tmem_base;
     uint32_t pad;
-    uint64_t full[kStages];
+    uint64_t desc_full[kDescs]; // the stage descriptor written
+    uint64_t full_k[kStages];  // K and Q of the slot landed
+    uint64_t full_v[kStages];  // V of the slot landed
     uint64_t empty[kStages];   // V of the slot free (its values MMA is done)
     uint64_t empty_k[kStages]; // K and Q of the slot free (its scores MMA is done)
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
@@ -203,7 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&m->full[i], 1);
+            mbar_init(&m->full_k[i], 1);
+            mbar_init(&m->full_v[i], 1);
+        }
+        for (int i = 0; i < kDescs; ++i) {
+            mbar_init(&m->desc_full[i], 1);
             mbar_init(&m->empty[i], 1);
             mbar_init(&m->empty_k[i], 1);
         }
@@ -357,10 +373,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t *kv = smem + slot * kStageBytes;
                 uint8_t *qb = smem + kOffQ + slot * kQBytes;
+                // K and Q (with the stage's descriptor) and V land on
+                // separate barriers: the scores MMA and the softmax of a stage
+                // need not wait for its V, whose slot frees only when the
+                // values MMA of the stage kStages back is done.
                 if (lane == 0) {
-                    mbar_expect_tx(&m->full[slot], (uint32_t)(nch * 2 * BOX_BYTES + 2 * NV * 128));
-                    tma_load_2d(qb, &q_map, &m->full[slot], 0, qrow);
-                    tma_load_2d(qb + kNQ * 128, &q_map, &m->full[slot], 64, qrow);
+                    StageDesc &d = m->desc[gk % kDescs];
+                    d.s = s;
+                    d.group = group;
+                    d.part = part;
+                    d.nvalid = nvalid;
+                    d.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
+                    d.nparts = nparts;
+                    d.run = run;
+                    mbar_arrive(&m->desc_full[gk % kDescs]);
+                    mbar_arrive_expect_tx(&m->full_k[slot], (uint32_t)(nch * 2 * BOX_BYTES + 2 * NV * 128));
+                    tma_load_2d(qb, &q_map, &m->full_k[slot], 0, qrow);
+                    tma_load_2d(qb + kNQ * 128, &q_map, &m->full_k[slot], 64, qrow);
                 }
                 __syncwarp();
                 // One K/V box per lane: box i covers row chunk i/4 of plane
@@ -381,34 +410,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (lane < nch * 4 && plane == 0)
                     tma_load_4d_hint(kv + (lane & 1) * kRegion + c * BOX_BYTES, &pool_map,
-                                     &m->full[slot], (lane & 1) * 64, kvh0, row, 0, policy);
+                                     &m->full_k[slot], (lane & 1) * 64, kvh0, row, 0, policy);
                 if (gk >= kStages && !warp_wait(&m->empty[slot], ph, lane)) {
                     // Let the K and Q copies already issued land before leaving;
-                    // the other roles see a stop at this slot.
+                    // the values warp sees a stop at this slot (the others time
+                    // out at the next stage).
                     if (lane == 0) {
                         atomicOr(p.err, PA_DEVERR_TIMEOUT_);
-                        m->desc[slot].flags = kFlagStop;
-                        mbar_arrive(&m->full[slot]);
+                        m->stop_v[slot] = 1;
+                        mbar_arrive(&m->full_v[slot]);
                     }
-                    warp_wait(&m->full[slot], (gk / kStages) & 1, lane);
+                    warp_wait(&m->full_k[slot], (gk / kStages) & 1, lane);
                     alive = false;
                     break;
                 }
                 if (lane == 0) {
-                    StageDesc &d = m->desc[slot];
-                    d.s = s;
-                    d.group = group;
-                    d.part = part;
-                    d.nvalid = nvalid;
-                    d.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
-                    d.nparts = nparts;
-                    d.run = run;
-                    mbar_arrive_expect_tx(&m->full[slot], (uint32_t)(nch * 2 * BOX_BYTES));
+                    m->stop_v[slot] = 0;
+                    mbar_arrive_expect_tx(&m->full_v[slot], (uint32_t)(nch * 2 * BOX_BYTES));
                 }
                 __syncwarp();
                 if (lane < nch * 4 && plane == 1)
                     tma_load_4d_hint(kv + kPlane + (lane & 1) * kRegion + c * BOX_BYTES, &pool_map,
-                                     &m->full[slot], (lane & 1) * 64, kvh0, row, 1, policy);
+                                     &m->full_v[slot], (lane & 1) * 64, kvh0, row, 1, policy);
                 // Next item: claim it when three stages of this one are left
                 // to issue (claiming earlier would unbalance the tail), then
                 // its unit, then its length and table.
@@ -420,9 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (alive) {
             const int slot = gk % kStages;
             if (gk < kStages || warp_wait(&m->empty[slot], ((gk / kStages) - 1) & 1, lane)) {
+                // The values MMA of stage gk - kStages is done, so its scores
+                // MMA is too: both halves of the slot are free.
                 if (lane == 0) {
-                    m->desc[slot].flags = kFlagStop;
-                    mbar_arrive(&m->full[slot]);
+                    m->desc[gk % kDescs].flags = kFlagStop;
+                    m->stop_v[slot] = 1;
+                    mbar_arrive(&m->desc_full[gk % kDescs]);
+                    mbar_arrive(&m->full_k[slot]);
+                    mbar_arrive(&m->full_v[slot]);
                 }
             } else if (lane == 0) {
                 atomicOr(p.err, PA_DEVERR_TIMEOUT_);
@@ -435,14 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = k % kStages;
             const int b = k & 1;
             const int u = k >> 1;
-            if (!warp_wait(&m->full[slot], (k / kStages) & 1, lane)) {
+            if (!warp_wait(qk ? &m->full_k[slot] : &m->full_v[slot], (k / kStages) & 1, lane)) {
                 if (lane == 0)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT_);
                 break;
             }
             int stop = 0;
             if (lane == 0)
-                stop = m->desc[slot].flags & kFlagStop;
+                stop = qk ? (m->desc[k % kDescs].flags & kFlagStop) : m->stop_v[slot];
             if (__shfl_sync(0xffffffffu, stop, 0))
                 break;
             bool ok = true;
@@ -591,8 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = k % kStages;
             const int b = k & 1;
             const int u = k >> 1;
-            bool ok = mbar_wait(&m->full[slot], (k / kStages) & 1);
-            const StageDesc d = m->desc[slot];
+            bool ok = mbar_wait(&m->desc_full[k % kDescs], (k / kDescs) & 1);
+            const StageDesc d = m->desc[k % kDescs];
             if (bar_sync_or(kBarEpi, kEpiThreads, !ok)) {
                 if (t == 0)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT_);
@@ -676,6 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!valid) {
                 // V rows past the end may hold anything (stale tiles, NaN
                 // padding); P is 0 there, but 0 * NaN would still poison O.
+                // They are zeroed once V has landed.
+                if (!mbar_wait(&m->full_v[slot], (k / kStages) & 1))
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT_);
                 uint8_t *vrow = smem + slot * kStageBytes + kPlane + t * 128;
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
