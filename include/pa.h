@@ -282,10 +282,17 @@ size_t pa_cascade_decode_workspace_size(int num_seqs, int num_heads, int head_si
  * The first prefix_blocks entries of every block_tables row must be the same
  * physical blocks (row 0's), and every seq_len >= prefix_blocks * block_size;
  * a table or length that breaks this is flagged (PA_DEVERR_PREFIX) and its
- * output is not defined.  Steps, all on the given stream: a setup kernel
- * (suffix lengths and tables), one prefill pass of the B queries over the
- * prefix (tensor cores), a split-K decode of the suffixes with log-sum-exp,
- * and the merge.  prefix_blocks == 0 is plain pa_decode_splitk.  Other
+ * output is not defined.  Steps: one prefill pass of the B queries over the
+ * prefix (tensor cores); a setup kernel (suffix lengths and tables) and a
+ * split-K decode of the suffixes with log-sum-exp; the merge.  The prefix
+ * pass runs on a stream of the library's own (one per host thread and
+ * device, created on the first call outside a graph capture, at the
+ * device's highest stream priority), forked from `stream` when the call
+ * starts and joined back into it before the merge, so that the two passes
+ * share the SMs; the call stays ordered on `stream` like any other work
+ * (and can be captured into a graph).  Without that stream (its creation
+ * failed, or the first call comes inside a capture) every step runs on
+ * `stream`.  prefix_blocks == 0 is plain pa_decode_splitk.  Other
  * arguments, layouts and errors as pa_decode_splitk; the workspace must hold
  * pa_cascade_decode_workspace_size bytes, 256-byte aligned.
  */

@@ -824,28 +824,21 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<uint4 *>(out + (size_t)row * head_size + (size_t)v * 8) = res;
 }
 
-// Cascade setup, one CTA per sequence: the prefix pass's request metadata
-// (query_start_loc = {0, B}, seq_len = prefix tokens), each sequence's suffix
-// length and suffix block table (its entries after the prefix blocks), and a
-// check that every table starts with row 0's prefix blocks.
+// Cascade setup, one CTA per sequence: each sequence's suffix length and
+// suffix block table (its entries after the prefix blocks), and a check that
+// every table starts with row 0's prefix blocks.
 __global__ void cascade_setup_kernel(const int32_t *__restrict__ block_tables,
-                                     const int32_t *__restrict__ seq_lens, int num_seqs,
-                                     int max_blocks, int prefix_blocks, int block_size,
-                                     int suffix_cols, int32_t *__restrict__ hdr,
+                                     const int32_t *__restrict__ seq_lens, int max_blocks,
+                                     int prefix_blocks, int block_size, int suffix_cols,
                                      int32_t *__restrict__ suffix_lens,
                                      int32_t *__restrict__ suffix_tables, unsigned int *err)
 {
-    // The prefix pass that follows waits for this grid before it reads the
-    // metadata written here; it may get resident meanwhile.
+    // The plan kernel that follows waits for this grid before it reads the
+    // suffix lengths written here; it may get resident meanwhile.
     griddep_launch_dependents();
     const int s = blockIdx.x;
     const int P = prefix_blocks * block_size;
     const int32_t *row = block_tables + (size_t)s * max_blocks;
-    if (s == 0 && threadIdx.x == 0) {
-        hdr[0] = 0;
-        hdr[1] = num_seqs;
-        hdr[2] = P;
-    }
     if (threadIdx.x == 0) {
         const int L = seq_lens[s];
         if (L < P)
@@ -902,7 +895,8 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
                               int num_kv_heads, int head_size, int block_size, int num_blocks,
                               int max_blocks_per_seq, float scale, int causal, pa_dtype dtype,
                               int key_split, int chunk_tiles, int64_t part_stride,
-                              int64_t lse_part_stride, void *stream, bool out_f32 = false)
+                              int64_t lse_part_stride, void *stream, bool out_f32 = false,
+                              int fixed_len = -1)
 {
     if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
         num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_size <= 0 ||
@@ -914,7 +908,13 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
         return PA_ERR_UNSUPPORTED;
     if (num_reqs == 0 || num_tokens == 0 || max_query_len == 0)
         return PA_OK;
-    if (!out || !q || !kv_cache || !block_tables || !seq_lens || !query_start_loc)
+    // fixed_len >= 0 (the cascade's prefix pass): one request whose
+    // metadata is given by value.
+    if (fixed_len >= 0 && (num_reqs != 1 || max_query_len != num_tokens ||
+                           (int64_t)fixed_len > (int64_t)max_blocks_per_seq * block_size))
+        return PA_ERR_INVALID_ARG;
+    if (!out || !q || !kv_cache || !block_tables ||
+        (fixed_len < 0 && (!seq_lens || !query_start_loc)))
         return PA_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(lse, 4) ||
         !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
@@ -956,6 +956,7 @@ static pa_status prefill_impl(void *out, float *lse, const void *q, const void *
     p.part_stride = part_stride;
     p.lse_part_stride = lse_part_stride;
     p.out_f32 = out_f32 ? 1 : 0;
+    p.fixed_len = fixed_len;
     // At most 128 query rows per request and an even group size: a CTA's
     // two tiles take two query heads of one kv head (both busy, one K/V
     // stream); otherwise one CTA per 256 rows of one head.
@@ -1256,6 +1257,60 @@ pa_status pa_merge_attn_states(void *out, float *out_lse, const void *o_a, const
 // is split over at most kMaxPrefixSplits key chunks.
 constexpr int kMaxPrefixSplits = kMaxMergeParts - 1;
 
+// A side stream for work that may run beside the caller's: per host thread
+// and device, a non-blocking stream of the device's highest priority, with
+// one event that forks work onto it after the caller's stream and one that
+// joins it back.  Created on first use in a (device, driver context) pair and
+// kept for the life of the thread.  Returns nullptr, and the caller keeps all
+// its work on its own stream, if creation fails or if `caller` is being
+// captured into a graph and nothing exists yet (no stream or event is created
+// during a capture).
+struct SideStream {
+    int dev = -1;
+    void *ctx = nullptr;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream *side_stream(cudaStream_t caller)
+{
+    constexpr int kMaxDevices = 16;
+    static thread_local SideStream slots[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    void *ctx = current_driver_context();
+    SideStream &ss = slots[dev];
+    if (ss.stream && ss.dev == dev && ss.ctx == ctx)
+        return &ss;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return nullptr;
+    SideStream n;
+    n.dev = dev;
+    n.ctx = ctx;
+    int least = 0, greatest = 0;
+    bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+              cudaStreamCreateWithPriority(&n.stream, cudaStreamNonBlocking, greatest) ==
+                  cudaSuccess &&
+              cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        if (n.join)
+            cudaEventDestroy(n.join);
+        if (n.fork)
+            cudaEventDestroy(n.fork);
+        if (n.stream)
+            cudaStreamDestroy(n.stream);
+        cudaGetLastError();
+        return nullptr;
+    }
+    // Objects of an earlier context on this device died with it: not
+    // destroyed, only replaced.
+    ss = n;
+    return &ss;
+}
+
 struct CascadeLayout {
     size_t sl, bt, parts, lse, ws, ws_bytes, total;
     int suffix_cols, max_parts;
@@ -1270,7 +1325,7 @@ static CascadeLayout cascade_layout(int num_seqs, int num_heads, int head_size,
     const int prefix_tiles = (prefix_blocks * block_size + 127) / 128;
     c.max_parts = (prefix_tiles < kMaxPrefixSplits ? prefix_tiles : kMaxPrefixSplits) + 1;
     c.suffix_cols = max_blocks_per_seq - prefix_blocks > 0 ? max_blocks_per_seq - prefix_blocks : 1;
-    c.sl = 256;
+    c.sl = 0;
     c.bt = c.sl + round_up((size_t)num_seqs * 4, 256);
     c.parts = c.bt + round_up((size_t)num_seqs * c.suffix_cols * 4, 256);
     c.lse = c.parts + round_up((size_t)c.max_parts * rows * head_size * 4, 256);
@@ -1327,7 +1382,6 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     if (!err)
         return PA_ERR_CUDA;
     char *w = static_cast<char *>(workspace);
-    int32_t *hdr = reinterpret_cast<int32_t *>(w);
     int32_t *sl_suf = reinterpret_cast<int32_t *>(w + c.sl);
     int32_t *bt_suf = reinterpret_cast<int32_t *>(w + c.bt);
     const size_t rows = (size_t)num_seqs * num_heads;
@@ -1346,31 +1400,63 @@ pa_status pa_cascade_decode(void *out, const void *q, const void *kv_cache,
     nsplit = nsplit < 1 ? 1 : (nsplit > c.max_parts - 1 ? c.max_parts - 1 : nsplit);
     const int chunk_tiles = (prefix_tiles + nsplit - 1) / nsplit;
     nsplit = (prefix_tiles + chunk_tiles - 1) / chunk_tiles;
-    cascade_setup_kernel<<<num_seqs, 128, 0, s>>>(block_tables, seq_lens, num_seqs,
-                                                  max_blocks_per_seq, prefix_blocks, block_size,
-                                                  c.suffix_cols, hdr, sl_suf, bt_suf, err);
-    if (cudaGetLastError() != cudaSuccess)
-        return PA_ERR_CUDA;
+    // The prefix pass needs nothing from the other kernels (its request
+    // metadata goes by value) and the suffix decode nothing the prefix pass
+    // writes, so the prefix pass goes to the side stream, forked before the
+    // setup kernel and joined before the merge.  Launched first and at the
+    // higher priority, its CTAs take SMs while the suffix decode's persistent
+    // CTAs take the others and then the SMs the prefix pass frees, instead of
+    // the two passes running one after the other.
+    SideStream *side = side_stream(s);
+    cudaStream_t ps = s;
+    if (side) {
+        if (cudaEventRecord(side->fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+            return PA_ERR_CUDA;
+        ps = side->stream;
+    }
     // 1. Every query against the shared prefix, no causal mask: one request
     //    whose B query rows are the B sequences' queries, split over nsplit
     //    key chunks (parts 0 .. nsplit-1).
     const int64_t part_elems = (int64_t)rows * head_size;
-    st = prefill_impl(parts, lse_parts, q, kv_cache, block_tables, max_blocks_per_seq, hdr + 2,
-                      hdr, 1, num_seqs, num_seqs, num_heads, num_kv_heads, head_size,
+    st = prefill_impl(parts, lse_parts, q, kv_cache, block_tables, max_blocks_per_seq, nullptr,
+                      nullptr, 1, num_seqs, num_seqs, num_heads, num_kv_heads, head_size,
                       block_size, num_blocks, prefix_blocks, scale, 0, dtype, nsplit,
-                      chunk_tiles, part_elems, (int64_t)rows, stream, true);
+                      chunk_tiles, part_elems, (int64_t)rows, ps, true, P);
     if (st != PA_OK)
         return st;
-    // 2. Each sequence's own suffix (part nsplit).
+    if (side && cudaEventRecord(side->join, ps) != cudaSuccess)
+        return PA_ERR_CUDA;
+    // 2. Each sequence's own suffix (part nsplit), after the setup kernel
+    //    has written the suffix lengths and tables.
+    cascade_setup_kernel<<<num_seqs, 128, 0, s>>>(block_tables, seq_lens, max_blocks_per_seq,
+                                                  prefix_blocks, block_size, c.suffix_cols,
+                                                  sl_suf, bt_suf, err);
+    if (cudaGetLastError() != cudaSuccess)
+        return PA_ERR_CUDA;
     st = decode_splitk_impl(parts + (size_t)nsplit * part_elems * 4, lse_parts + (size_t)nsplit * rows,
                             q, kv_cache, bt_suf, sl_suf, num_seqs, num_heads, num_kv_heads,
                             head_size, block_size, num_blocks, c.suffix_cols, scale, dtype,
                             max_suffix, partition_size, w + c.ws, c.ws_bytes, stream, true);
     if (st != PA_OK)
         return st;
-    // 3. Merge the nsplit + 1 parts.
+    // 3. Merge the nsplit + 1 parts, after both passes.  After the join the
+    //    merge is a plain launch: it waits for everything before it.
+    if (side && cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
+        return PA_ERR_CUDA;
     const int64_t threads = (int64_t)rows * (head_size / 8);
     const unsigned grid = (unsigned)((threads + 255) / 256);
+    if (side) {
+        if (dtype == PA_BF16)
+            merge_parts_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+                static_cast<__nv_bfloat16 *>(out), reinterpret_cast<const float *>(parts),
+                static_cast<const float *>(lse_parts), nsplit + 1, (int64_t)rows, head_size);
+        else
+            merge_parts_kernel<__half><<<grid, 256, 0, s>>>(
+                static_cast<__half *>(out), reinterpret_cast<const float *>(parts),
+                static_cast<const float *>(lse_parts), nsplit + 1, (int64_t)rows, head_size);
+        return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     const cudaError_t me =
         dtype == PA_BF16
             ? launch_after_previous(merge_parts_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,

@@ -169,7 +169,17 @@ struct PrefillParams {
     // 2j+1 (same kv head) over the same 128 rows.
     int head_pairs;
     int out_f32;                    // out holds float32 rows instead of the input dtype
+    // >= 0: one request of num_tokens query rows over fixed_len keys, and
+    // query_start_loc / seq_lens are not read.
+    int fixed_len;
 };
+
+// The calling thread's current driver context (cuCtxGetCurrent, reached
+// through the runtime's driver entry point), or nullptr if there is none or
+// the driver does not export the call.  Caches of device objects key on it so
+// that a new context on a device (after cudaDeviceReset, or a caller that
+// switched driver contexts) gets new objects.
+void *current_driver_context();
 
 // Prefill over the paged cache on grid (ceil(max_query_len/128) x key_split, H, R).
 cudaError_t launch_prefill_f16(int head_size, int block_size, const CUtensorMap &pool,

@@ -24,20 +24,13 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_internal.h"
 
-namespace {
+namespace pa {
 
-// Scratch in device global memory.  In host code this name is only a
-// host-side stand-in for the symbol; the kernels get its real device address
-// from scratch_address().
-__device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
-
-// cuCtxGetCurrent through the runtime's driver entry point (no link against
-// the driver library).  Returns nullptr if the driver does not export it.
-typedef int (*ctx_get_current_fn)(void **ctx);
-
-ctx_get_current_fn ctx_get_current()
+void *current_driver_context()
 {
+    typedef int (*ctx_get_current_fn)(void **ctx);
     static ctx_get_current_fn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -48,8 +41,20 @@ ctx_get_current_fn ctx_get_current()
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<ctx_get_current_fn>(p);
     });
-    return fn;
+    void *ctx = nullptr;
+    if (!fn || fn(&ctx) != 0)
+        return nullptr;
+    return ctx;
 }
+
+} // namespace pa
+
+namespace {
+
+// Scratch in device global memory.  In host code this name is only a
+// host-side stand-in for the symbol; the kernels get its real device address
+// from scratch_address().
+__device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_noalloc_scratch in the current device's current
 // context.  The lookup is done once per (device, context) and cached: a new
@@ -71,10 +76,7 @@ void *scratch_address(cudaError_t *err)
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess)
         return nullptr;
-    void *ctx = nullptr;
-    ctx_get_current_fn get_ctx = ctx_get_current();
-    if (get_ctx && get_ctx(&ctx) != 0)
-        ctx = nullptr;
+    void *ctx = pa::current_driver_context();
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n_cached; ++i)
         if (cache[i].dev == dev && cache[i].ctx == ctx) {
@@ -87,8 +89,8 @@ void *scratch_address(cudaError_t *err)
         return nullptr;
     // With no context current before the lookup, the runtime has just made
     // the device's primary context current: key the entry on that one.
-    if (!ctx && get_ctx && get_ctx(&ctx) != 0)
-        ctx = nullptr;
+    if (!ctx)
+        ctx = pa::current_driver_context();
     // Replace an entry of the same device (its context is gone or no longer
     // current), else append; a full table recycles its oldest slot.
     int slot = -1;

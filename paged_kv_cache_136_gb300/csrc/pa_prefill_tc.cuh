@@ -189,9 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_cta = hp ? kTileM : kRowsPerCta;
     auto toff = [&](int t) { return hp ? 0 : t * kTileM; };  // tile t's first row
     auto thead = [&](int t) { return hp ? h + t : h; };       // tile t's query head
-    const int q0 = __ldg(p.query_start_loc + r);
-    const int q1 = __ldg(p.query_start_loc + r + 1);
-    const int L = __ldg(p.seq_lens + r);
+    const bool fixed = p.fixed_len >= 0;
+    const int q0 = fixed ? 0 : __ldg(p.query_start_loc + r);
+    const int q1 = fixed ? p.num_tokens : __ldg(p.query_start_loc + r + 1);
+    const int L = fixed ? p.fixed_len : __ldg(p.seq_lens + r);
     const int q_len = q1 - q0;
     if (q0 < 0 || q1 > p.num_tokens || q_len < 0 || q_len > p.max_query_len || L < q_len ||
         L > p.max_blocks * BS) {

@@ -179,3 +179,73 @@ def test_cascade_flags_a_table_without_the_prefix(pa):
     w.block_tables = bt
     _cascade(pa, w, pb, part=64)
     assert pa.pa_device_errors(clear=True) & pa.DEVERR_PREFIX
+
+
+def test_cascade_in_a_graph_and_in_stream_order(pa):
+    """The prefix pass runs on the library's side stream, forked from and
+    joined back into the caller's: a graph captured on the caller's stream
+    replays the same result, and work queued after the call on that stream
+    sees the finished output."""
+    w = wl.make("prefix", device="cuda", poison=True, num_seqs=24, seed=44)
+    pb = w.meta["shared_blocks"]
+    eager = _cascade(pa, w, pb, part=128)
+    msl = int(w.seq_lens.max())
+    n = pa.pa_cascade_decode_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                            w.block_tables.shape[1], pb, msl, w.block_size, 128)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.full_like(w.q, float("nan"))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pa.pa_cascade_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                             w.block_size, pb, msl, ws, 128)
+        after = out.clone()
+    s.synchronize()
+    assert torch.equal(after.view(torch.int16), eager.view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        pa.pa_cascade_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens, w.scale,
+                             w.block_size, pb, msl, ws, 128)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_cascade_first_call_inside_a_capture(pa):
+    """A host thread whose first cascade call comes inside a graph capture
+    gets no side stream (nothing is created during a capture): every step
+    runs on the caller's stream, with the same result."""
+    import threading
+    w = wl.make("prefix", device="cuda", poison=True, num_seqs=12, seed=45)
+    pb = w.meta["shared_blocks"]
+    eager = _cascade(pa, w, pb, part=64)
+    msl = int(w.seq_lens.max())
+    n = pa.pa_cascade_decode_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                            w.block_tables.shape[1], pb, msl, w.block_size, 64)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.full_like(w.q, float("nan"))
+    errors = []
+
+    def capture_and_replay():
+        try:
+            torch.cuda.set_device(out.device)
+            s = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                pa.pa_cascade_decode(out, w.q, w.kv_cache, w.block_tables, w.seq_lens,
+                                     w.scale, w.block_size, pb, msl, ws, 64)
+            g.replay()
+            torch.cuda.synchronize()
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    t = threading.Thread(target=capture_and_replay)
+    t.start()
+    t.join()
+    assert not errors, errors
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert pa.pa_device_errors(clear=True) == 0
