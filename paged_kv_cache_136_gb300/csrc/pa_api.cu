@@ -1284,7 +1284,11 @@ static SideStream *side_stream(cudaStream_t caller)
     if (ss.stream && ss.dev == dev && ss.ctx == ctx)
         return &ss;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess) {
+        cudaGetLastError(); // not this call's error to report
+        return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone)
         return nullptr;
     SideStream n;
     n.dev = dev;
