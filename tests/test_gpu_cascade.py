@@ -249,3 +249,43 @@ def test_cascade_first_call_inside_a_capture(pa):
     assert not errors, errors
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     assert pa.pa_device_errors(clear=True) == 0
+
+
+def test_cascade_from_two_host_threads(pa):
+    """Two host threads, each with its own stream and workspace, run the
+    cascade at the same time: each thread's calls fork onto that thread's
+    own side stream, and both results match the single-thread result."""
+    import threading
+    w = wl.make("prefix", device="cuda", poison=True, num_seqs=16, seed=46)
+    pb = w.meta["shared_blocks"]
+    eager = _cascade(pa, w, pb, part=128)
+    msl = int(w.seq_lens.max())
+    n = pa.pa_cascade_decode_workspace_size(w.num_seqs, w.num_heads, w.head_size,
+                                            w.block_tables.shape[1], pb, msl, w.block_size, 128)
+    outs = [torch.full_like(w.q, float("nan")) for _ in range(2)]
+    wss = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    errors = []
+    start = threading.Barrier(2)
+
+    def run(i):
+        try:
+            torch.cuda.set_device(w.q.device)
+            s = torch.cuda.Stream()
+            start.wait()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    pa.pa_cascade_decode(outs[i], w.q, w.kv_cache, w.block_tables, w.seq_lens,
+                                         w.scale, w.block_size, pb, msl, wss[i], 128)
+            s.synchronize()
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    ts = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), eager.view(torch.int16))
+    assert pa.pa_device_errors(clear=True) == 0
